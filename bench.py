@@ -1,0 +1,393 @@
+"""Benchmark of the SplitZip codec on one GB300 (or N, as independent shards).
+
+Workload (default): the BF16 KV cache [layers=32, K/V=2, tokens=4096,
+kv_heads=8, head_dim=128] = 268,435,456 elements (512 MiB), one codebook per
+(layer, K/V) slice -> 64 tensors of 4,194,304 elements, values N(0, 1) times a
+per-(layer, K/V, head, channel) log-uniform scale in [0.1, 20] with 1 % of the
+channels at 30x (synthetic, seeded; see weight_compression_codec_gb300/inputs.py).
+
+One step = the whole hot path over the 64 tensors: sz_calibrate_many (exponent
+histograms + Top-16 select) -> sz_encode_many (split, pack, ordered escape
+compaction, payload assembly) -> sz_decode_many (dense decode + escape patch).
+The inputs (512 MiB) are larger than L2 (126 MB), so no flush is needed.
+
+Reported: ``value`` = raw BF16 bytes of the workload / step time (GB/s), the
+three main kernels' raw-BF16 GB/s and HBM roofline fractions, the payload
+ratio, ``e2e`` (the same step with the input in pinned host memory, copied in,
+and the decoded tensors copied back), clocks sampled during the timed region,
+and the CPU oracle on a bounded sample of the workload (``cpu_baseline``).
+
+``--impl reference`` times the CPU oracle (the reference arm of this build) on
+a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "encode/decode raw-BF16 GB/s on 1 GB300 and % of HBM roofline; compression ratio"
+WORKLOAD = "kv_cache_bf16_32x2x4096x8x128_64_codebooks"
+UNIT = "GB/s"
+CSRC = ROOT / "weight_compression_codec_gb300" / "csrc"
+TRAFFIC_FILE = ROOT / "profiles" / "ncu_traffic.json"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=32, help="KV-cache layers (64 tensors at 32)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_arrays(layers: int, rank: int) -> list[np.ndarray]:
+    from weight_compression_codec_gb300 import inputs
+
+    # each rank holds its own cache (weak scaling): layers are offset by rank
+    return [inputs.kv_cache_tensor(rank * layers + l, kv) for l in range(layers) for kv in range(2)]
+
+
+# ---------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+
+
+def cpu_oracle_sample(arrays: list[np.ndarray], budget_s: float) -> dict:
+    """The oracle (as it stands) on the host: calibrate + encode + decode of the
+    workload's tensors in order until ``budget_s`` seconds have passed."""
+    import oracle
+
+    done_bytes, t0, k = 0, time.perf_counter(), 0
+    while True:
+        x = arrays[k % len(arrays)]
+        cb = oracle.calibrate(x)
+        p, m = oracle.encode(x, cb)
+        y = oracle.decode(p, m, cb.dec_lut)
+        assert y.size == x.size
+        done_bytes += 2 * x.size
+        k += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done_bytes / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{k} KV-cache tensors of {arrays[0].size} elements (calibrate+encode+decode, "
+                      f"single-threaded C), {dt:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    arrays = workload_arrays(2, 0)  # 4 of the workload's tensors per step
+    for _ in range(args.warmup):
+        cpu_oracle_sample(arrays[:1], 0.0)
+    times = []
+    import oracle
+
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        for x in arrays:
+            cb = oracle.calibrate(x)
+            p, m = oracle.encode(x, cb)
+            oracle.decode(p, m, cb.dec_lut)
+        times.append(time.perf_counter() - t0)
+    step = float(np.mean(times))
+    raw = sum(2 * a.size for a in arrays)
+    value = raw / step / 1e9
+    sample = f"{len(arrays)} of the 64 KV-cache tensors per step ({raw / 2**20:.0f} MiB raw)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- GPU
+
+
+def measured_peaks() -> dict:
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_sources_sha() -> str:
+    h = hashlib.sha256()
+    for f in sorted(CSRC.glob("*")):
+        if f.suffix in (".cu", ".cuh", ".h"):
+            h.update(f.read_bytes())
+    h.update((ROOT / "include" / "splitzip.h").read_bytes())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, sha: str):
+    if not TRAFFIC_FILE.exists():
+        return None
+    d = json.loads(TRAFFIC_FILE.read_text())
+    rec = d.get(kernel)
+    if not rec or rec.get("source_sha") != sha:
+        return None
+    return rec.get("bytes_per_launch_full_workload")
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import weight_compression_codec_gb300 as sz
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    sz.build()
+
+    arrays = workload_arrays(args.layers, rank)
+    n_total = sum(a.size for a in arrays)
+    raw_bytes = 2 * n_total
+    xs = [torch.from_numpy(a.view(np.int16)).to(dev) for a in arrays]
+    batch = sz.Batch(xs)
+    ws_cal, ws_enc, ws_dec = sz.Workspace(dev), sz.Workspace(dev), sz.Workspace(dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        sz.sz_calibrate_many(batch.table, workspace=ws_cal)
+        sz.sz_encode_many(batch.table, workspace=ws_enc)
+        sz.sz_decode_many(batch.table, workspace=ws_dec)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    # correctness gate before timing: device flags clear, round trip exact
+    for w in (ws_cal, ws_enc, ws_dec):
+        assert sz.sz_workspace_flags(w.buf) == 0
+    for i in (0, len(xs) // 2, len(xs) - 1):
+        assert torch.equal(batch.out_view(i).view(torch.int16), xs[i].view(torch.int16)), f"round trip {i}"
+    metas = [sz.meta_from_bytes(batch.metas[i].cpu().numpy()) for i in range(len(xs))]
+    comp_total = sum(m.comp_bytes for m in metas)
+
+    K = args.steps
+    ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(K)] for k in
+          ("cb", "ca", "eb", "ea", "db", "da")}
+    for lst in ev.values():  # create the underlying CUDA events
+        for e in lst:
+            e.record(stream)
+    step_start = torch.cuda.Event(enable_timing=True)
+    step_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    step_start.record(stream)
+    for k in range(K):
+        sz.sz_set_timing_events(ev["cb"][k], ev["ca"][k])
+        sz.sz_calibrate_many(batch.table, workspace=ws_cal)
+        sz.sz_set_timing_events(ev["eb"][k], ev["ea"][k])
+        sz.sz_encode_many(batch.table, workspace=ws_enc)
+        sz.sz_set_timing_events(ev["db"][k], ev["da"][k])
+        sz.sz_decode_many(batch.table, workspace=ws_dec)
+    sz.sz_set_timing_events(None, None)
+    step_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = step_start.elapsed_time(step_end)
+    t_cal = [ev["cb"][k].elapsed_time(ev["ca"][k]) for k in range(K)]
+    t_enc = [ev["eb"][k].elapsed_time(ev["ea"][k]) for k in range(K)]
+    t_dec = [ev["db"][k].elapsed_time(ev["da"][k]) for k in range(K)]
+    for w in (ws_cal, ws_enc, ws_dec):
+        assert sz.sz_workspace_flags(w.buf) == 0
+
+    ms_step = total_ms / K
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    # e2e: the same step through the public API with host-resident input and output
+    e2e = None
+    if not args.no_e2e:
+        host_in = [torch.from_numpy(a.view(np.int16)).pin_memory() for a in arrays]
+        host_out = [torch.empty(a.size, dtype=torch.int16).pin_memory() for a in arrays]
+        host_meta = torch.empty(batch.metas.shape, dtype=torch.uint8).pin_memory()
+
+        def e2e_step():
+            for hi, xd in zip(host_in, batch.xs):
+                xd.view(torch.int16).copy_(hi, non_blocking=True)
+            step()
+            for i, ho in enumerate(host_out):
+                ho.copy_(batch.out_view(i).view(torch.int16), non_blocking=True)
+            host_meta.copy_(batch.metas, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        ke = max(3, K // 2)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(ke):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / ke
+        assert all(torch.equal(ho, hi) for ho, hi in zip(host_out[:2], host_in[:2]))
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * raw_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": raw_bytes, "d2h_bytes_per_step": raw_bytes + batch.metas.numel(),
+               "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"]
+    ms = {"calibrate": float(np.mean(t_cal)), "encode": float(np.mean(t_enc)), "decode": float(np.mean(t_dec))}
+    alg = {"calibrate": raw_bytes, "encode": raw_bytes + comp_total, "decode": comp_total + raw_bytes}
+    kname = {"calibrate": "cal_hist", "encode": "enc_main", "decode": "dec_main"}
+    sha = kernel_sources_sha()
+    kernels = {}
+    for k in ms:
+        achieved = alg[k] / (ms[k] * 1e-3) / 1e9
+        kernels[k] = {"kernel": kname[k], "ms": ms[k], "raw_gbs": raw_bytes / (ms[k] * 1e-3) / 1e9,
+                      "achieved_gbs": achieved, "frac": achieved / peak, "alg_bytes": alg[k],
+                      "traffic": recorded_traffic(kname[k], sha)}
+    dom = max(ms, key=ms.get)
+    value = world * raw_bytes / (ms_step * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(arrays, args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "u16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tensors": len(arrays), "elements": n_total, "raw_bytes": raw_bytes,
+                   "step": "calibrate+encode+decode", "l2": "inputs 512 MiB > L2, no flush",
+                   "parallelism": f"{world} independent shards" if world > 1 else "single GPU"},
+        "ratio": comp_total / raw_bytes, "compression": raw_bytes / comp_total,
+        "n_esc": int(sum(m.n_esc for m in metas)),
+        "encode_gbs": kernels["encode"]["raw_gbs"], "decode_gbs": kernels["decode"]["raw_gbs"],
+        "calibrate_gbs": kernels["calibrate"]["raw_gbs"],
+        "roofline": {"bound": "hbm", "kernel": kernels[dom]["kernel"], "achieved": kernels[dom]["achieved_gbs"],
+                     "peak": peak, "unit": "GB/s", "frac": kernels[dom]["frac"],
+                     "traffic": kernels[dom]["traffic"], "peak_source": peaks["source"]},
+        "kernels": kernels,
+        "clocks": clk,
+        "gpu_launches": 7 * K,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "source_sha": sha,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,223 @@
+/*
+ * splitzip.h -- C ABI of the GB300 (sm_103a) SplitZip lossless BF16 codec.
+ *
+ * The method (from "splitzip_codec.py", module docstring, and
+ * "docs/developer/splitzip.md", "What it does"): view each BF16 value as a
+ * 16-bit pattern x; split it into the exponent byte exp = (x >> 7) & 0xFF and
+ * the sign + low-7-mantissa byte sm = ((x >> 8) & 0x80) | (x & 0x7F).  A
+ * per-tensor codebook maps the 16 most frequent exponents to 4-bit codes; sm is
+ * stored verbatim; every element whose exponent is not in the codebook goes to
+ * an ordered escape stream with chunk-local positions (chunk = 1024).  Decode
+ * rebuilds x = ((sm & 0x80) << 8) | (exp << 7) | (sm & 0x7F) bit for bit.
+ *
+ * Payload (wire) layout, from "splitzip_codec.py" assemble_payload / PayloadMeta
+ * and "docs/developer/splitzip.md" "Invariants common to both routes" item 1;
+ * all integers little-endian, align4(v) = (v + 3) & ~3:
+ *   off_pk   = 0                          uint8  pk[n_pairs], n_pairs = ceil(n/2)
+ *   off_sm   = align4(n_pairs)            uint8  sm[n]
+ *   off_cid  = align4(off_sm + n)         int32  chunk_id[n_esc]
+ *   off_lpos = off_cid + 4 n_esc          uint16 local_pos[n_esc]
+ *   off_ev   = align4(off_lpos + 2 n_esc) uint8  esc_val[n_esc]
+ *   comp_bytes = off_ev + n_esc; every pad byte is 0.
+ * Conventions this codec fixes (the pages leave them open or disagree):
+ *   - element 2i is the LOW nibble of pk[i], element 2i+1 the high nibble
+ *     (the pages' pure-PyTorch codec uses the opposite order; a per-byte nibble
+ *     swap converts between the two);
+ *   - an escaped element is stored in pk as code 0; escapes are listed in
+ *     ascending element index (chunk_id non-decreasing);
+ *   - Top-16 ties are broken by ascending exponent value;
+ *   - n == 0 is valid: empty payload, codebook with no codes, coverage 1.0.
+ *
+ * Memory and streams.  Every pointer argument is named d_* (device memory) or
+ * h_* (host memory).  The library allocates nothing: the caller owns every
+ * buffer, including the workspace, whose size the *_workspace_bytes queries
+ * give.  All compute calls are asynchronous on `stream` (a cudaStream_t; NULL
+ * is the legacy default stream), never synchronise, and may be captured in a
+ * CUDA graph.  A workspace may be reused by calls ordered on one stream; calls
+ * that may overlap on the GPU need separate workspaces.
+ *
+ * Alignment.  Every BF16 input/output and payload pointer must be 16-byte
+ * aligned; codebook, meta and item-table pointers 16-byte aligned; workspaces
+ * 256-byte aligned.  Violations are rejected with SZ_ERR_ALIGN (single-tensor
+ * calls) or flagged on the device with SZ_FLAG_ALIGN (item tables).
+ *
+ * Errors.  Every call returns an sz_status.  Host-side checks (null pointers,
+ * sizes, alignment, workspace size) happen before anything is launched and
+ * leave all buffers untouched.  Conditions only the GPU can see (a capacity
+ * overrun, a malformed payload, a wait that timed out) never fault the GPU:
+ * the kernels skip the offending writes, record SZ_FLAG_* bits in the
+ * workspace's status word (and in sz_meta.status for encode), and the caller
+ * reads them with sz_workspace_flags after the work completes.
+ */
+#ifndef SPLITZIP_H
+#define SPLITZIP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SZ_API __attribute__((visibility("default")))
+#else
+#define SZ_API
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* sz_stream; /* the same type as cudaStream_t */
+
+#define SZ_VERSION 1
+#define SZ_CHUNK_SIZE 1024u     /* escape chunk ("splitzip_codec.py" encode_torch chunk_size) */
+#define SZ_TILE_ELEMS 8192u     /* elements per work tile; items start on tile boundaries   */
+#define SZ_ESCAPE_CODE 16u      /* enc_lut value of an exponent outside the codebook          */
+#define SZ_MAX_ELEMS 4294967295ull       /* largest n per tensor (chunk_id fits int32)      */
+#define SZ_MANY_MAX_ITEMS 65535u         /* largest item count of the *_many calls           */
+
+/* Status codes returned by every call. */
+typedef enum sz_status {
+  SZ_OK = 0,
+  SZ_ERR_ARG = 1,        /* null pointer, size out of range, count out of range   */
+  SZ_ERR_ALIGN = 2,      /* a pointer breaks the alignment rules above             */
+  SZ_ERR_CAPACITY = 3,   /* a host-known size does not fit its buffer             */
+  SZ_ERR_META = 4,       /* a host meta disagrees with the wire layout for its n  */
+  SZ_ERR_WORKSPACE = 5,  /* workspace null, misaligned or smaller than required   */
+  SZ_ERR_CUDA = 6,       /* a CUDA runtime call failed (launch, copy, no device)  */
+  SZ_ERR_DEVICE = 7      /* sz_workspace_flags found SZ_FLAG_* bits set           */
+} sz_status;
+
+/* Device-side status bits (sz_workspace_flags, sz_meta.status). */
+#define SZ_FLAG_CAPACITY 0x01u    /* encode: payload larger than the item's capacity      */
+#define SZ_FLAG_META 0x02u        /* decode: meta disagrees with the layout / capacity    */
+#define SZ_FLAG_ESCAPE 0x04u      /* decode: an escape points outside its tile or tensor  */
+#define SZ_FLAG_TIMEOUT 0x08u     /* a bounded wait gave up (results of the call invalid) */
+#define SZ_FLAG_ALIGN 0x10u       /* an item-table pointer breaks the alignment rules     */
+#define SZ_FLAG_ITEMS 0x20u       /* item table: tile_begin chain inconsistent            */
+#define SZ_FLAG_SIZE 0x40u        /* an item's n is out of range for the call             */
+
+/* Per-tensor codebook ("splitzip_codec.py" SplitZipCodebook and
+ * calibrate_codebook).  304 bytes, 16-byte aligned in device memory. */
+typedef struct sz_codebook {
+  uint8_t enc_lut[256];  /* exponent byte -> code 0..15, or SZ_ESCAPE_CODE (the page's enc_lut_marked) */
+  uint8_t dec_lut[16];   /* code -> exponent byte; codes >= n_top hold 0                              */
+  uint32_t n_top;        /* min(16, number of distinct exponents)                                     */
+  uint32_t reserved0;
+  uint64_t top_count;    /* elements whose exponent has a code                                        */
+  uint64_t n;            /* elements the codebook was calibrated on                                   */
+  double coverage;       /* top_count / n as an IEEE double division; 1.0 when n == 0                 */
+} sz_codebook;
+
+/* Payload metadata ("splitzip_codec.py" PayloadMeta).  96 bytes. */
+typedef struct sz_meta {
+  uint64_t n, n_pairs, n_esc, comp_bytes;
+  uint64_t off_pk, off_sm, off_cid, off_lpos, off_ev;
+  uint32_t chunk_size;   /* always SZ_CHUNK_SIZE                            */
+  uint32_t status;       /* encode: SZ_FLAG_* bits of this tensor (0 = ok)   */
+  double coverage;       /* copied from the codebook used to encode          */
+  uint64_t reserved1;
+} sz_meta;
+
+/* One tensor of a *_many call, in device memory.  64 bytes.
+ * Fields a call does not use are ignored (see each call). */
+typedef struct sz_item {
+  const uint16_t* x;       /* calibrate/encode: n BF16 bit patterns                   */
+  uint16_t* out;           /* decode: n BF16 bit patterns written                     */
+  uint8_t* payload;        /* encode: written (capacity bytes); decode: read          */
+  sz_codebook* codebook;   /* calibrate: written; encode/decode: read                 */
+  sz_meta* meta;           /* encode: written; decode: read                           */
+  uint64_t n;              /* elements                                                */
+  uint64_t capacity;       /* bytes available at payload                              */
+  uint64_t tile_begin;     /* *_many only: sum of sz_tiles(n) of the items before it  */
+} sz_item;
+
+/* ------------------------------------------------------------------ host-only queries */
+
+SZ_API int sz_version(void);
+SZ_API const char* sz_strerror(int status);
+
+/* Tiles of SZ_TILE_ELEMS elements covering n elements: ceil(n / 8192). */
+SZ_API uint64_t sz_tiles(uint64_t n);
+
+/* Fills h_meta's sizes and offsets for n elements with n_esc escapes (the
+ * wire layout above); status and coverage are set to 0.  SZ_ERR_ARG if
+ * n > SZ_MAX_ELEMS or n_esc > n. */
+SZ_API int sz_layout(uint64_t n, uint64_t n_esc, sz_meta* h_meta);
+
+/* comp_bytes of a payload of n elements and n_esc escapes. */
+SZ_API uint64_t sz_payload_bytes(uint64_t n, uint64_t n_esc);
+
+/* Largest possible payload of n elements (every element escaped):
+ * a payload buffer of this size never overflows. */
+SZ_API uint64_t sz_max_payload_bytes(uint64_t n);
+
+/* Fills tile_begin of h_items[0..count) (host copy of an item table) and
+ * returns the total tile count in *h_total_tiles. */
+SZ_API int sz_items_prepare(sz_item* h_items, uint32_t count, uint64_t* h_total_tiles);
+
+/* Workspace sizes (bytes) of the compute calls. */
+SZ_API size_t sz_calibrate_workspace_bytes(uint32_t count);
+SZ_API size_t sz_encode_workspace_bytes(uint32_t count, uint64_t total_tiles);
+SZ_API size_t sz_decode_workspace_bytes(uint32_t count, uint64_t total_tiles);
+
+/* Copies the workspace's SZ_FLAG_* word to *h_flags after synchronising
+ * `stream`.  Returns SZ_OK when no bit is set, SZ_ERR_DEVICE otherwise. */
+SZ_API int sz_workspace_flags(const void* d_workspace, uint32_t* h_flags, sz_stream stream);
+
+/* ------------------------------------------------------------------ single tensor */
+
+/* Calibration ("splitzip_codec.py" calibrate_codebook): histogram of the
+ * exponent bytes of d_x[0..n), then the 16 most frequent values (ties by
+ * ascending value) become codes 0..15; writes *d_codebook. */
+SZ_API int sz_calibrate(const uint16_t* d_x, uint64_t n, sz_codebook* d_codebook,
+                        void* d_workspace, size_t workspace_bytes, sz_stream stream);
+
+/* Encode ("splitzip_codec.py" encode_torch + assemble_payload) of d_x[0..n)
+ * with *d_codebook (any codebook: escapes follow from it) into
+ * d_payload[0..comp_bytes); writes *d_meta.  If the payload would exceed
+ * `capacity`, the payload is not valid and d_meta->status and the workspace
+ * flags get SZ_FLAG_CAPACITY; no byte beyond capacity is written. */
+SZ_API int sz_encode(const uint16_t* d_x, uint64_t n, const sz_codebook* d_codebook,
+                     uint8_t* d_payload, uint64_t capacity, sz_meta* d_meta,
+                     void* d_workspace, size_t workspace_bytes, sz_stream stream);
+
+/* Decode ("splitzip_codec.py" decode_torch) of the payload described by
+ * *d_meta (payload_bytes readable bytes at d_payload) with d_codebook->dec_lut
+ * into d_out[0..n).  n must equal d_meta->n; a meta that disagrees with the
+ * layout or with payload_bytes sets SZ_FLAG_META and leaves d_out unwritten;
+ * an escape outside the tensor sets SZ_FLAG_ESCAPE and is skipped. */
+SZ_API int sz_decode(const uint8_t* d_payload, uint64_t payload_bytes, const sz_meta* d_meta,
+                     const sz_codebook* d_codebook, uint16_t* d_out, uint64_t n,
+                     void* d_workspace, size_t workspace_bytes, sz_stream stream);
+
+/* ------------------------------------------------------------------ many tensors, one launch per step */
+
+/* The same three operations over `count` (1..SZ_MANY_MAX_ITEMS) tensors of
+ * any size, each with its own codebook and meta, described by the device
+ * item table d_items (tile_begin filled as sz_items_prepare does;
+ * total_tiles = its total).  Work is spread over all SMs tile by tile, so a
+ * few large tensors and many mid-size ones run equally well.
+ *   calibrate: reads x, n, tile_begin; writes *codebook.
+ *   encode:    reads x, n, codebook, payload, capacity, tile_begin; writes payload, *meta.
+ *   decode:    reads payload (capacity readable bytes), meta, codebook, n, tile_begin; writes out. */
+SZ_API int sz_calibrate_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles,
+                             void* d_workspace, size_t workspace_bytes, sz_stream stream);
+SZ_API int sz_encode_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles,
+                          void* d_workspace, size_t workspace_bytes, sz_stream stream);
+SZ_API int sz_decode_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles,
+                          void* d_workspace, size_t workspace_bytes, sz_stream stream);
+
+/* ------------------------------------------------------------------ measurement */
+
+/* Timing hook: `before` and `after` are cudaEvent_t handles (or NULL to
+ * clear).  While set, every compute call made by the calling host thread
+ * records `before` on its stream just before its main kernel (the streaming
+ * pass: cal_hist, enc_main or dec_main) and `after` just after it, so the
+ * caller can time that kernel alone with cudaEventElapsedTime.  The events are
+ * borrowed, never destroyed. */
+SZ_API int sz_set_timing_events(void* before, void* after);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPLITZIP_H */

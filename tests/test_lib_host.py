@@ -1,0 +1,141 @@
+"""CPU-side checks of libsplitzip.so: it builds for sm_103a, loads, exports every
+symbol include/splitzip.h declares, and its host-only calls (sizes, layout,
+argument checks) behave -- no GPU needed, no kernel launched."""
+from __future__ import annotations
+
+import ctypes
+import re
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+import weight_compression_codec_gb300 as sz
+from weight_compression_codec_gb300 import binding as B
+
+HEADER = Path(__file__).resolve().parents[1] / "include" / "splitzip.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sz.build()
+    return B.lib()
+
+
+def declared_symbols() -> list[str]:
+    text = HEADER.read_text()
+    return re.findall(r"SZ_API\s+[\w\s\*]+?\b(sz_\w+)\s*\(", text)
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for must in ("sz_calibrate", "sz_encode", "sz_decode", "sz_calibrate_many", "sz_encode_many",
+                 "sz_decode_many", "sz_max_payload_bytes", "sz_workspace_flags"):
+        assert must in names
+    assert set(names) == set(B.SIGNATURES), "binding signatures and header declarations differ"
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert lib.sz_version() == 1
+
+
+def test_exports_are_only_the_abi(lib):
+    import subprocess
+
+    out = subprocess.run(["nm", "-D", "--defined-only", str(B.library_path())], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    ours = {s for s in exported if s.startswith("sz_")}
+    assert ours == set(declared_symbols())
+
+
+def test_struct_sizes_match_header(lib):
+    assert ctypes.sizeof(B.SzCodebook) == 304 and ctypes.sizeof(B.SzMeta) == 96 and ctypes.sizeof(B.SzItem) == 64
+
+
+@pytest.mark.parametrize("n", [0, 1, 2, 3, 5, 1023, 1024, 1025, 8191, 8192, 8193, 65536, 100_000_003, 2**31, 2**32 - 1])
+def test_layout_matches_oracle(lib, oracle, n):
+    for e in sorted({0, 1, 3, n // 7, n}):
+        if e > n:
+            continue
+        m = sz.sz_layout(n, e)
+        o = oracle.layout(n, e)
+        assert m.as_tuple() == o.as_tuple()
+        assert sz.sz_payload_bytes(n, e) == o.comp_bytes
+    assert sz.sz_max_payload_bytes(n) == oracle.layout(n, n).comp_bytes
+    assert sz.sz_tiles(n) == (n + 8191) // 8192
+
+
+def test_layout_rejects_bad_sizes(lib):
+    m = B.SzMeta()
+    assert lib.sz_layout(10, 11, ctypes.byref(m)) == B.SZ_ERR_ARG
+    assert lib.sz_layout(2**32, 0, ctypes.byref(m)) == B.SZ_ERR_ARG
+    assert lib.sz_layout(10, 0, None) == B.SZ_ERR_ARG
+
+
+def test_items_prepare(lib):
+    ns = [0, 5, 8192, 8193, 0, 1]
+    arr = (B.SzItem * len(ns))()
+    for i, n in enumerate(ns):
+        arr[i].n = n
+    total = ctypes.c_uint64()
+    assert lib.sz_items_prepare(arr, len(ns), ctypes.byref(total)) == 0
+    assert [arr[i].tile_begin for i in range(len(ns))] == [0, 0, 1, 2, 4, 4]
+    assert total.value == 5
+
+
+def test_workspace_sizes_monotone(lib):
+    for f in (lambda c: lib.sz_calibrate_workspace_bytes(c),):
+        assert f(1) <= f(2) <= f(100)
+    assert lib.sz_encode_workspace_bytes(1, 10) < lib.sz_encode_workspace_bytes(1, 11)
+    assert lib.sz_decode_workspace_bytes(1, 10) <= lib.sz_decode_workspace_bytes(1, 11)
+    # encode staging holds local_pos and esc_val of every element of every tile
+    assert lib.sz_encode_workspace_bytes(1, 100) >= 100 * 8192 * 3
+
+
+def test_host_argument_checks_launch_nothing(lib):
+    """Invalid arguments are rejected on the host before any CUDA call, so these
+    run without a GPU."""
+    ws = 4096  # fake aligned addresses: never dereferenced on these paths
+    al = 1 << 20
+    # null codebook / meta / data
+    assert lib.sz_calibrate(al, 10, None, ws * 256, 1 << 20, None) == B.SZ_ERR_ARG
+    assert lib.sz_calibrate(None, 10, al, ws * 256, 1 << 20, None) == B.SZ_ERR_ARG
+    assert lib.sz_encode(al, 10, al, al, 1000, None, ws * 256, 1 << 20, None) == B.SZ_ERR_ARG
+    assert lib.sz_decode(al, 1000, None, al, al, 10, ws * 256, 1 << 20, None) == B.SZ_ERR_ARG
+    # misaligned pointers
+    assert lib.sz_calibrate(al + 2, 10, al, ws * 256, 1 << 20, None) == B.SZ_ERR_ALIGN
+    assert lib.sz_encode(al, 10, al + 8, al, 1000, al, ws * 256, 1 << 20, None) == B.SZ_ERR_ALIGN
+    assert lib.sz_decode(al + 4, 1000, al, al, al, 10, ws * 256, 1 << 20, None) == B.SZ_ERR_ALIGN
+    # too-large n
+    assert lib.sz_calibrate(al, 2**32, al, ws * 256, 1 << 20, None) == B.SZ_ERR_ARG
+    # capacity below the dense part of the layout
+    assert lib.sz_encode(al, 1000, al, al, 1000, al, ws * 256, 1 << 30, None) == B.SZ_ERR_CAPACITY
+    assert lib.sz_decode(al, 1000, al, al, al, 1000, ws * 256, 1 << 30, None) == B.SZ_ERR_CAPACITY
+    # workspace missing / misaligned / too small
+    assert lib.sz_calibrate(al, 10, al, None, 1 << 20, None) == B.SZ_ERR_WORKSPACE
+    assert lib.sz_calibrate(al, 10, al, ws * 256 + 16, 1 << 20, None) == B.SZ_ERR_WORKSPACE
+    assert lib.sz_encode(al, 10**6, al, al, 10**7, al, ws * 256, 1024, None) == B.SZ_ERR_WORKSPACE
+    # *_many: count and table checks
+    assert lib.sz_calibrate_many(al, 0, 1, ws * 256, 1 << 20, None) == B.SZ_ERR_ARG
+    assert lib.sz_encode_many(None, 3, 1, ws * 256, 1 << 20, None) == B.SZ_ERR_ARG
+    assert lib.sz_decode_many(al + 8, 3, 1, ws * 256, 1 << 20, None) == B.SZ_ERR_ALIGN
+    assert lib.sz_decode_many(al, 70000, 1, ws * 256, 1 << 20, None) == B.SZ_ERR_ARG
+    for s in range(8):
+        assert lib.sz_strerror(s)
+
+
+def test_python_binding_rejects_cpu_and_wrong_dtype(lib):
+    import torch
+
+    with pytest.raises(ValueError):
+        sz.sz_calibrate(torch.zeros(8, dtype=torch.float32))
+    with pytest.raises(ValueError):
+        sz.sz_calibrate(torch.zeros(8, dtype=torch.bfloat16))  # not on a CUDA device
+
+
+def test_meta_bytes_round_trip(lib, oracle):
+    om = oracle.layout(12345, 67, 0.5)
+    m = sz.meta_from_bytes(np.frombuffer(sz.meta_to_bytes(om), np.uint8))
+    assert m.as_tuple() == om.as_tuple() and m.coverage == 0.5

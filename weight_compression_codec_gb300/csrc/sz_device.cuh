@@ -1,0 +1,282 @@
+// Device-side building blocks shared by the SplitZip kernels (sm_103a only).
+//
+// - wire-layout arithmetic of the GPU path (payload offsets, tiles);
+// - inline-PTX wrappers for mbarriers, bulk (TMA) copies, cp.async with
+//   zero-fill, proxy fences, acquire/release accesses and the global timer;
+// - the item table view used by every multi-tensor kernel;
+// - the workspace layouts.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "splitzip.h"
+
+namespace sz {
+
+constexpr uint32_t kChunk = SZ_CHUNK_SIZE;          // 1024
+constexpr uint32_t kTile = SZ_TILE_ELEMS;           // 8192
+constexpr uint32_t kChunksPerTile = kTile / kChunk; // 8
+constexpr uint32_t kEscape = SZ_ESCAPE_CODE;        // 16
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded waits give up after 2 s
+
+// ------------------------------------------------------------------ layout
+// Wire layout of "splitzip_codec.py" assemble_payload: pk | sm | chunk_id |
+// local_pos | esc_val, each section start rounded up to 4 bytes except
+// local_pos, which follows chunk_id directly.
+struct Layout {
+  uint64_t n_pairs, off_sm, off_cid, off_lpos, off_ev, comp_bytes;
+};
+
+__host__ __device__ inline uint64_t round_up4(uint64_t v) { return (v + 3u) & ~uint64_t(3); }
+__host__ __device__ inline uint64_t tiles_of(uint64_t n) { return (n + kTile - 1) / kTile; }
+
+__host__ __device__ inline Layout layout_of(uint64_t n, uint64_t n_esc) {
+  Layout l;
+  l.n_pairs = (n + 1) >> 1;
+  l.off_sm = round_up4(l.n_pairs);
+  l.off_cid = round_up4(l.off_sm + n);
+  l.off_lpos = l.off_cid + 4 * n_esc;
+  l.off_ev = round_up4(l.off_lpos + 2 * n_esc);
+  l.comp_bytes = l.off_ev + n_esc;
+  return l;
+}
+
+// ------------------------------------------------------------------ items
+// A kernel sees its tensors either through a device item table or, for the
+// single-tensor entry points, through one item passed by value.
+struct Items {
+  const sz_item* table;  // nullptr: use `one`
+  sz_item one;
+  uint32_t count;
+  uint64_t total_tiles;
+};
+
+__device__ __forceinline__ const sz_item& item_at(const Items& it, uint32_t i) {
+  return it.table ? it.table[i] : it.one;
+}
+
+// Index of the item whose tile range holds global tile `tile` (items are in
+// ascending tile_begin order; empty items own no tile).
+__device__ inline uint32_t find_item(const Items& it, uint64_t tile) {
+  if (it.table == nullptr) return 0;
+  uint32_t lo = 0, hi = it.count;  // answer in [lo, hi)
+  while (hi - lo > 1) {
+    uint32_t mid = (lo + hi) >> 1;
+    if (it.table[mid].tile_begin <= tile) lo = mid; else hi = mid;
+  }
+  // skip empty items that share the same tile_begin
+  while (lo + 1 < it.count && it.table[lo + 1].tile_begin <= tile) ++lo;
+  return lo;
+}
+
+// ------------------------------------------------------------------ workspace
+// Every workspace starts with this header (256 bytes).
+struct WsHeader {
+  uint32_t flags;        // SZ_FLAG_* bits
+  uint32_t pad0;
+  unsigned long long ticket;  // dynamic tile counter (encode)
+  uint32_t reserved[60];
+};
+static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
+
+__host__ __device__ inline uint64_t round_up256(uint64_t v) { return (v + 255u) & ~uint64_t(255); }
+
+// calibrate: header | hist[count][256] u32 | done[count] u32
+struct CalWs {
+  WsHeader* hdr;
+  uint32_t* hist;
+  uint32_t* done;
+};
+__host__ __device__ inline uint64_t cal_ws_bytes(uint32_t count) {
+  return 256 + round_up256(uint64_t(count) * 1024) + round_up256(uint64_t(count) * 4);
+}
+__host__ __device__ inline CalWs cal_ws(void* base, uint32_t count) {
+  char* p = static_cast<char*>(base);
+  CalWs w;
+  w.hdr = reinterpret_cast<WsHeader*>(p);
+  w.hist = reinterpret_cast<uint32_t*>(p + 256);
+  w.done = reinterpret_cast<uint32_t*>(p + 256 + round_up256(uint64_t(count) * 1024));
+  return w;
+}
+
+// encode: header | item_flags[count] u32 | status[total_tiles] u64 |
+//         lpos staging[total_tiles * 8192] u16 | ev staging[total_tiles * 8192] u8
+struct EncWs {
+  WsHeader* hdr;
+  uint32_t* item_flags;
+  unsigned long long* status;
+  uint16_t* lpos;
+  uint8_t* ev;
+};
+__host__ __device__ inline uint64_t enc_ws_bytes(uint32_t count, uint64_t tiles) {
+  return 256 + round_up256(uint64_t(count) * 4) + round_up256(tiles * 8) + round_up256(tiles * kTile * 2) +
+         round_up256(tiles * kTile);
+}
+__host__ __device__ inline EncWs enc_ws(void* base, uint32_t count, uint64_t tiles) {
+  char* p = static_cast<char*>(base);
+  EncWs w;
+  w.hdr = reinterpret_cast<WsHeader*>(p);
+  p += 256;
+  w.item_flags = reinterpret_cast<uint32_t*>(p);
+  p += round_up256(uint64_t(count) * 4);
+  w.status = reinterpret_cast<unsigned long long*>(p);
+  p += round_up256(tiles * 8);
+  w.lpos = reinterpret_cast<uint16_t*>(p);
+  p += round_up256(tiles * kTile * 2);
+  w.ev = reinterpret_cast<uint8_t*>(p);
+  return w;
+}
+
+// decode: header | item_flags[count] u32 | ranges[total_tiles] (k0, k1) u32x2
+struct DecWs {
+  WsHeader* hdr;
+  uint32_t* item_flags;
+  uint2* ranges;
+};
+__host__ __device__ inline uint64_t dec_ws_bytes(uint32_t count, uint64_t tiles) {
+  return 256 + round_up256(uint64_t(count) * 4) + round_up256(tiles * 8);
+}
+__host__ __device__ inline DecWs dec_ws(void* base, uint32_t count, uint64_t tiles) {
+  char* p = static_cast<char*>(base);
+  DecWs w;
+  w.hdr = reinterpret_cast<WsHeader*>(p);
+  p += 256;
+  w.item_flags = reinterpret_cast<uint32_t*>(p);
+  p += round_up256(uint64_t(count) * 4);
+  w.ranges = reinterpret_cast<uint2*>(p);
+  return w;
+}
+
+#ifdef __CUDACC__
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `bar` with the given parity to complete; gives up
+// after kWaitTimeoutNs and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0 && global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+  }
+}
+
+// Bulk (TMA) copy global -> shared; completion is reported to `bar` as
+// transaction bytes.  dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Bulk (TMA) copy shared -> global, tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Make this thread's generic-proxy writes to shared memory visible to the
+// async proxy (before a bulk store reads them).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 16-byte cp.async that reads only `src_bytes` (0..16) bytes and zero-fills
+// the rest of the destination; nothing beyond src + src_bytes is read.
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+// Arrive on `bar` once all cp.async issued so far by this thread completed
+// (the arrival is counted in the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Named barrier over `threads` threads that also returns the OR of `pred`
+// across them.
+__device__ __forceinline__ bool named_bar_red_or(uint32_t id, uint32_t threads, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"(uint32_t(pred)), "r"(id), "r"(threads)
+      : "memory");
+  return out != 0;
+}
+
+__device__ __forceinline__ void set_flag(WsHeader* h, uint32_t bits) { atomicOr(&h->flags, bits); }
+
+#endif  // __CUDACC__
+
+}  // namespace sz

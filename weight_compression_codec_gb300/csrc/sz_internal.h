@@ -1,0 +1,32 @@
+// Internal launch interface between the C ABI (sz_api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "sz_device.cuh"
+
+namespace sz {
+
+struct DeviceInfo {
+  int device;
+  int num_sms;
+};
+
+// Cached per-device properties (SM count); also opts kernels into large
+// dynamic shared memory once per device.
+cudaError_t device_info(DeviceInfo* info);
+
+cudaError_t launch_calibrate(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
+cudaError_t launch_encode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
+cudaError_t launch_decode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
+
+// Optional timing hook: when set (non-null), launchers record `before` just
+// before and `after` just after their main kernel on the launch stream.
+struct TimingHook {
+  cudaEvent_t before;
+  cudaEvent_t after;
+};
+extern thread_local TimingHook g_timing;
+
+}  // namespace sz
