@@ -36,6 +36,6 @@ from .codec import (  # noqa: F401
 
 def build(force: bool = False) -> str:
     """Compile libsplitzip.so for sm_103a (in-tree) and return its path."""
-    from .build import build as _b
+    from .buildlib import build as _b
 
     return str(_b(force=force))

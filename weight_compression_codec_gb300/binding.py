@@ -10,7 +10,7 @@ from __future__ import annotations
 import ctypes
 from pathlib import Path
 
-from . import build as _build
+from . import buildlib as _build
 
 SZ_CHUNK_SIZE = 1024
 SZ_TILE_ELEMS = 8192
