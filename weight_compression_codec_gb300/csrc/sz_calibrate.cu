@@ -5,29 +5,32 @@
 // Two launches per call (after a 256-byte header memset):
 //   cal_prepare  zeroes the per-item histograms and completion counters,
 //                validates the item table, writes the codebook of n == 0 items;
-//   cal_hist     streams every tile once (16-byte loads, ~48 KiB in flight per
-//                SM) into privatised shared-memory counters, flushes them with
-//                one global atomic per non-zero bin, and the CTA that flushes
-//                an item's last tiles ranks the 256 bins and writes the
-//                codebook (ties by ascending exponent value).
+//   cal_hist     streams every tile once into privatised shared-memory
+//                counters, flushes them with one global atomic per non-zero
+//                bin, and the CTA that flushes an item's last tiles ranks the
+//                256 bins and writes the codebook (ties by ascending exponent
+//                value).
 //
-// Counters: 16-bit halves of a 32-bit word, word (bin >> 1) of the thread's
-// own column -- cnt[(bin >> 1) * kHistThreads + tid] -- so the 32 lanes of a
-// warp always hit 32 different banks whatever their bins are, and the adds
-// are shared-memory reductions with no return value (no read-modify-write
-// dependency chain).  A thread adds at most 64 per tile, so a flush every
-// kFlushTiles tiles keeps every half below 65536.
+// The histogram is bound by instruction issue, not by the atomics' conflicts,
+// so the counters are laid out to make an element as cheap as possible: one
+// 32-bit counter per (bin, thread), cnt[bin][tid] with 64 threads, so the
+// byte offset of an element's counter is its exponent byte times 256 -- a
+// shift and a mask of the BF16 pattern -- and the 32 lanes of a warp always
+// hit 32 different banks whatever their bins.  The adds are shared-memory
+// reductions without a return value.  Each thread keeps the next tile's
+// 16 x 16 bytes in flight (register double buffer) while it counts the
+// current one.
 #include "sz_internal.h"
 
 namespace sz {
 namespace {
 
-constexpr int kHistThreads = 128;
+constexpr int kHistThreads = 64;
 constexpr int kHistCtasPerSm = 3;
-constexpr int kPairs = 128;                       // 256 bins / 2 per word
-constexpr uint32_t kFlushTiles = 1000;            // 1000 * 64 < 65536
-constexpr size_t kHistSmem = size_t(kPairs) * kHistThreads * 4;  // 64 KiB
+constexpr int kVecPerThread = kTile / 8 / kHistThreads;  // 16 x 16-byte vectors per tile
+constexpr size_t kHistSmem = size_t(256) * kHistThreads * 4;  // 64 KiB
 constexpr uint32_t kItemInvalid = 0x80000000u;
+
 
 __device__ void write_empty_codebook(sz_codebook* cb) {
   for (int v = 0; v < 256; ++v) cb->enc_lut[v] = kEscape;
@@ -112,7 +115,7 @@ __device__ void select_top16(const sz_item& it, const uint32_t* __restrict__ ghi
 
 __global__ void __launch_bounds__(kHistThreads, kHistCtasPerSm)
     cal_hist(const __grid_constant__ Items items, CalWs ws) {
-  extern __shared__ __align__(16) uint32_t cnt[];  // [kPairs][kHistThreads]
+  extern __shared__ __align__(16) uint32_t cnt[];  // [256 bins][kHistThreads]
   __shared__ uint32_t h[256];
   __shared__ uint8_t dl[16];
   __shared__ unsigned long long s_top;
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(kHistThreads, kHistCtasPerSm)
   const int tid = threadIdx.x;
   // an inconsistent item table (flagged by cal_prepare) is never walked
   if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
-  for (int q = 0; q < kPairs; ++q) cnt[q * kHistThreads + tid] = 0;
+  for (int b = 0; b < 256; ++b) cnt[b * kHistThreads + tid] = 0;
 
   const uint64_t T = items.total_tiles;
   const uint64_t per = (T + gridDim.x - 1) / gridDim.x;
@@ -136,33 +139,43 @@ __global__ void __launch_bounds__(kHistThreads, kHistCtasPerSm)
   uint64_t cur_tiles = tiles_of(item_at(items, cur).n);
   uint32_t run = 0;  // tiles counted since the last flush
 
-  uint32_t* mycol = cnt + tid;
-  auto count = [&](uint32_t x) {
-    const uint32_t b = (x >> 7) & 0xFFu;
-    atomicAdd(mycol + (b >> 1) * kHistThreads, 1u << ((b & 1u) << 4));
+  // this thread's counter column, as a byte address: counter of bin b is at
+  // col + 256 * b
+  char* const col = reinterpret_cast<char*>(cnt + tid);
+  auto count_lo = [&](uint32_t w) {  // element in bits 0..15
+    atomicAdd(reinterpret_cast<uint32_t*>(col + ((w << 1) & 0xFF00u)), 1u);
   };
-  auto count_word = [&](uint32_t w) {
-    count(w & 0xFFFFu);
-    count(w >> 16);
+  auto count_hi = [&](uint32_t w) {  // element in bits 16..31
+    atomicAdd(reinterpret_cast<uint32_t*>(col + ((w >> 15) & 0xFF00u)), 1u);
+  };
+  auto count_vec = [&](const uint4& v) {
+    count_lo(v.x);
+    count_hi(v.x);
+    count_lo(v.y);
+    count_hi(v.y);
+    count_lo(v.z);
+    count_hi(v.z);
+    count_lo(v.w);
+    count_hi(v.w);
   };
 
   auto flush = [&]() {
     __syncthreads();
     {
-      const int q = tid;  // bins 2q, 2q+1
-      uint32_t lo = 0, hi = 0;
-      uint32_t* row = cnt + q * kHistThreads;
-#pragma unroll 8
-      for (int j = 0; j < kHistThreads; ++j) {
-        const int c = (j + tid) & (kHistThreads - 1);
-        const uint32_t w = row[c];
-        row[c] = 0;
-        lo += w & 0xFFFFu;
-        hi += w >> 16;
-      }
       uint32_t* gh = ws.hist + uint64_t(cur) * 256;
-      if (lo) atomicAdd(gh + 2 * q, lo);
-      if (hi) atomicAdd(gh + 2 * q + 1, hi);
+#pragma unroll
+      for (int q = 0; q < 256 / kHistThreads; ++q) {
+        const int b = tid * (256 / kHistThreads) + q;
+        uint32_t* row = cnt + b * kHistThreads;
+        uint32_t sum = 0;
+#pragma unroll 8
+        for (int j = 0; j < kHistThreads; ++j) {
+          const int c = (j + tid) & (kHistThreads - 1);  // lanes read 32 different banks
+          sum += row[c];
+          row[c] = 0;
+        }
+        if (sum) atomicAdd(gh + b, sum);
+      }
     }
     __threadfence();
     __syncthreads();
@@ -175,15 +188,21 @@ __global__ void __launch_bounds__(kHistThreads, kHistCtasPerSm)
     run = 0;
   };
 
+  // r holds the current full tile once `have` is set: the next full tile of
+  // the same item is loaded before the current one is counted.
+  uint4 r[kVecPerThread];
+  bool have = false;
   for (uint64_t t = t0; t < t1; ++t) {
     if (t >= cur_begin + cur_tiles) {
       if (run) flush();
       cur = find_item(items, t);
       cur_begin = item_at(items, cur).tile_begin;
       cur_tiles = tiles_of(item_at(items, cur).n);
+      have = false;
     }
     const sz_item& it = item_at(items, cur);
     if ((ws.done[cur] & kItemInvalid) || t - cur_begin >= cur_tiles) {  // invalid item: nothing is read
+      have = false;
       continue;
     }
     const uint64_t base = (t - cur_begin) * kTile;
@@ -191,29 +210,31 @@ __global__ void __launch_bounds__(kHistThreads, kHistCtasPerSm)
     const uint32_t nt = left < kTile ? uint32_t(left) : kTile;
     const uint4* src = reinterpret_cast<const uint4*>(it.x + base);
     if (nt == kTile) {
-      uint4 r[8];
+      if (!have) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) r[k] = __ldg(src + tid + k * kHistThreads);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        count_word(r[k].x);
-        count_word(r[k].y);
-        count_word(r[k].z);
-        count_word(r[k].w);
+        for (int k = 0; k < kVecPerThread; ++k) r[k] = __ldg(src + tid + k * kHistThreads);
       }
+      const bool next_full = (t + 1 < t1) && (t + 1 < cur_begin + cur_tiles) && (left >= 2 * uint64_t(kTile));
+      uint4 q[kVecPerThread];
+      if (next_full) {
+#pragma unroll
+        for (int k = 0; k < kVecPerThread; ++k) q[k] = __ldg(src + kTile / 8 + tid + k * kHistThreads);
+      }
+#pragma unroll
+      for (int k = 0; k < kVecPerThread; ++k) count_vec(r[k]);
+      if (next_full) {
+#pragma unroll
+        for (int k = 0; k < kVecPerThread; ++k) r[k] = q[k];
+      }
+      have = next_full;
     } else {
+      have = false;
       const uint32_t nvec = nt >> 3;
-      for (uint32_t v = tid; v < nvec; v += kHistThreads) {
-        const uint4 r = __ldg(src + v);
-        count_word(r.x);
-        count_word(r.y);
-        count_word(r.z);
-        count_word(r.w);
-      }
+      for (uint32_t v = tid; v < nvec; v += kHistThreads) count_vec(__ldg(src + v));
       const uint32_t rem = nt & 7u;
-      if (uint32_t(tid) < rem) count(it.x[base + (nvec << 3) + tid]);
+      if (uint32_t(tid) < rem) count_lo(it.x[base + (nvec << 3) + tid]);
     }
-    if (++run == kFlushTiles) flush();
+    ++run;
   }
   if (run) flush();
 }

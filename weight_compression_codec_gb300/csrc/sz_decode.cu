@@ -79,37 +79,101 @@ __device__ uint32_t item_problems(const Items& items, uint32_t i) {
   return bad;
 }
 
-// First k in [0, e) with cid[k] >= target (e if none).
-__device__ uint32_t lower_bound_cid(const int32_t* cid, uint32_t e, uint32_t target) {
-  uint32_t lo = 0, hi = e;
-  while (lo < hi) {
-    const uint32_t mid = (lo + hi) >> 1;
-    if (uint32_t(__ldg(cid + mid)) < target) lo = mid + 1; else hi = mid;
+// First k in [0, e) with cid[k] >= target (e if none), found by the 16 lanes
+// of a half warp (hl = lane within the half, half_mask = its lanes): each
+// round probes 16 evenly spaced positions, so the search takes
+// ceil(log16(e)) + 1 dependent loads instead of log2(e).
+__device__ uint32_t lower_bound_cid16(const int32_t* cid, uint32_t e, uint32_t target, uint32_t hl,
+                                      uint32_t half_mask) {
+  uint32_t lo = 0, hi = e;  // the answer lies in [lo, hi]
+  while (hi - lo > 16) {
+    const uint32_t step = (hi - lo + 15) / 16;
+    uint32_t p = lo + (hl + 1) * step - 1;
+    if (p > hi - 1) p = hi - 1;
+    const uint32_t c = __popc(__ballot_sync(half_mask, uint32_t(__ldg(cid + p)) < target));
+    if (c == 0) {
+      hi = lo + step - 1;  // the first probe already holds cid >= target
+    } else {
+      uint32_t last_less = lo + c * step - 1;
+      if (last_less > hi - 1) last_less = hi - 1;
+      if (c < 16) {
+        uint32_t first_ge = lo + (c + 1) * step - 1;
+        if (first_ge < hi) hi = first_ge;
+      }
+      lo = last_less + 1;
+    }
   }
-  return lo;
+  const uint32_t p = lo + hl;
+  const bool less = (p < hi) && uint32_t(__ldg(cid + p)) < target;
+  return lo + __popc(__ballot_sync(half_mask, less));
 }
 
-__global__ void dec_prepare(const __grid_constant__ Items items, DecWs ws) {
-  const uint64_t nthreads = uint64_t(gridDim.x) * blockDim.x;
-  const uint64_t gtid = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (uint64_t i = gtid; i < items.count; i += nthreads) {
-    const uint32_t bad = item_problems(items, uint32_t(i));
-    ws.item_flags[i] = bad;
-    if (bad) set_flag(ws.hdr, bad);
-  }
-  for (uint64_t t = gtid; t < items.total_tiles; t += nthreads) {
-    const uint32_t i = find_item(items, t);
+constexpr int kPrepWarps = 8;
+
+// Escape ranges per tile.  blockIdx.y = item; each warp owns a group of 32
+// consecutive tiles of that item (lane l <-> tile ta + l).  The two half
+// warps bracket the group's escapes with 16-ary searches for the first
+// escape of tile ta and of tile ta + 32; the warp then reads the bracketed
+// chunk_id slice once, coalesced, counting escapes per tile in shared
+// memory, and a warp scan of the counts gives every tile's [k0, k1).
+__global__ void __launch_bounds__(kPrepWarps * 32) dec_prepare(const __grid_constant__ Items items, DecWs ws) {
+  __shared__ uint32_t s_bad;
+  __shared__ uint32_t counts[kPrepWarps][32];
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t warp = threadIdx.x >> 5;
+  for (uint32_t i = blockIdx.y; i < items.count; i += gridDim.y) {
     const sz_item& it = item_at(items, i);
-    uint2 r = make_uint2(kRangeInvalid, 0);
-    if (item_problems(items, i) == 0 && t - it.tile_begin < tiles_of(it.n)) {
-      const uint32_t lt = uint32_t(t - it.tile_begin);
-      const sz_meta* mp = it.meta;
-      const uint32_t e = uint32_t(mp->n_esc);
-      const int32_t* cid = reinterpret_cast<const int32_t*>(it.payload + mp->off_cid);
-      r.x = lower_bound_cid(cid, e, lt * kChunksPerTile);
-      r.y = lower_bound_cid(cid, e, lt * kChunksPerTile + kChunksPerTile);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      s_bad = item_problems(items, i);
+      if (blockIdx.x == 0) {
+        ws.item_flags[i] = s_bad;
+        if (s_bad) set_flag(ws.hdr, s_bad);
+      }
     }
-    ws.ranges[t] = r;
+    __syncthreads();
+    const bool bad = s_bad != 0;
+    const uint64_t tiles = (it.n > SZ_MAX_ELEMS) ? 0 : tiles_of(it.n);
+    const uint32_t e = bad ? 0u : uint32_t(it.meta->n_esc);
+    const int32_t* cid = bad ? nullptr : reinterpret_cast<const int32_t*>(it.payload + it.meta->off_cid);
+    const uint32_t half_mask = lane < 16 ? 0x0000FFFFu : 0xFFFF0000u;
+    for (uint64_t ta = (uint64_t(blockIdx.x) * kPrepWarps + warp) * 32; ta < tiles;
+         ta += uint64_t(gridDim.x) * kPrepWarps * 32) {
+      const uint32_t ng = (tiles - ta < 32) ? uint32_t(tiles - ta) : 32u;
+      uint2 r = make_uint2(kRangeInvalid, 0);
+      if (!bad) {
+        const uint32_t target = uint32_t(ta) * kChunksPerTile + (lane < 16 ? 0u : 32u * kChunksPerTile);
+        const uint32_t k = lower_bound_cid16(cid, e, target, lane & 15u, half_mask);
+        const uint32_t k_lo = __shfl_sync(0xFFFFFFFFu, k, 0);
+        const uint32_t k_hi = __shfl_sync(0xFFFFFFFFu, k, 16);
+        counts[warp][lane] = 0;
+        __syncwarp();
+        // 8 independent loads per lane per round, then the shared-memory counts
+        for (uint32_t kb = k_lo; kb < k_hi; kb += 32 * 8) {
+          uint32_t c8[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint32_t kk = kb + lane + 32u * u;
+            c8[u] = kk < k_hi ? uint32_t(__ldg(cid + kk)) : 0xFFFFFFFFu;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint32_t rel = (c8[u] >> 3) - uint32_t(ta);  // tile within the group
+            if (c8[u] != 0xFFFFFFFFu && rel < 32u) atomicAdd(&counts[warp][rel], 1u);
+          }
+        }
+        __syncwarp();
+        const uint32_t c = counts[warp][lane];
+        uint32_t incl = c;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+          const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+          if (lane >= uint32_t(d)) incl += o;
+        }
+        r = make_uint2(k_lo + incl - c, k_lo + incl);
+      }
+      if (lane < ng) ws.ranges[it.tile_begin + ta + lane] = r;
+    }
   }
 }
 
@@ -364,10 +428,13 @@ cudaError_t launch_decode(const Items& items, void* ws_base, cudaStream_t stream
   cudaError_t err = cudaMemsetAsync(ws_base, 0, sizeof(WsHeader), stream);
   if (err != cudaSuccess) return err;
   {
-    const uint64_t work = items.total_tiles > items.count ? items.total_tiles : items.count;
-    const uint64_t blocks = (work + 255) / 256;
-    const unsigned grid = unsigned(blocks < 4096 ? (blocks ? blocks : 1) : 4096);
-    dec_prepare<<<grid, 256, 0, stream>>>(items, ws);
+    // blockIdx.y = item; x covers the average item's 32-tile groups (8 per block)
+    const uint64_t per_item = items.count ? (items.total_tiles + items.count - 1) / items.count : 0;
+    uint64_t gx = (per_item + 32 * kPrepWarps - 1) / (32 * kPrepWarps);
+    if (gx < 1) gx = 1;
+    if (gx > 1024) gx = 1024;
+    const unsigned gy = items.count < 65535u ? items.count : 65535u;
+    dec_prepare<<<dim3(unsigned(gx), gy), kPrepWarps * 32, 0, stream>>>(items, ws);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   if (items.total_tiles == 0) return cudaSuccess;

@@ -100,18 +100,25 @@ __host__ __device__ inline CalWs cal_ws(void* base, uint32_t count) {
   return w;
 }
 
-// encode: header | item_flags[count] u32 | status[total_tiles] u64 |
+// encode: header | item_flags[count] u32 | item_esc[count] u32 (escape total) |
+//         seg_ticket[count] u32 | status[total_tiles] u64 (segment lookback words,
+//         at each segment's first tile) | chunk_cnt[total_tiles * 8] u16 |
 //         lpos staging[total_tiles * 8192] u16 | ev staging[total_tiles * 8192] u8
+// Staging slot of chunk c (global chunk index tile * 8 + chunk) starts at
+// entry c * 1024 and holds the chunk's escapes in element order.
 struct EncWs {
   WsHeader* hdr;
   uint32_t* item_flags;
+  uint32_t* item_esc;
+  uint32_t* seg_ticket;
   unsigned long long* status;
+  uint16_t* chunk_cnt;
   uint16_t* lpos;
   uint8_t* ev;
 };
 __host__ __device__ inline uint64_t enc_ws_bytes(uint32_t count, uint64_t tiles) {
-  return 256 + round_up256(uint64_t(count) * 4) + round_up256(tiles * 8) + round_up256(tiles * kTile * 2) +
-         round_up256(tiles * kTile);
+  return 256 + 3 * round_up256(uint64_t(count) * 4) + round_up256(tiles * 8) + round_up256(tiles * 16) +
+         round_up256(tiles * kTile * 2) + round_up256(tiles * kTile);
 }
 __host__ __device__ inline EncWs enc_ws(void* base, uint32_t count, uint64_t tiles) {
   char* p = static_cast<char*>(base);
@@ -120,8 +127,14 @@ __host__ __device__ inline EncWs enc_ws(void* base, uint32_t count, uint64_t til
   p += 256;
   w.item_flags = reinterpret_cast<uint32_t*>(p);
   p += round_up256(uint64_t(count) * 4);
+  w.item_esc = reinterpret_cast<uint32_t*>(p);
+  p += round_up256(uint64_t(count) * 4);
+  w.seg_ticket = reinterpret_cast<uint32_t*>(p);
+  p += round_up256(uint64_t(count) * 4);
   w.status = reinterpret_cast<unsigned long long*>(p);
   p += round_up256(tiles * 8);
+  w.chunk_cnt = reinterpret_cast<uint16_t*>(p);
+  p += round_up256(tiles * 16);
   w.lpos = reinterpret_cast<uint16_t*>(p);
   p += round_up256(tiles * kTile * 2);
   w.ev = reinterpret_cast<uint8_t*>(p);
@@ -254,6 +267,18 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
 
 __device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Relaxed GPU-scope accesses: coherent single-copy-atomic 64-bit words with
+// no ordering of other memory (enough for a word that carries its own data).
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {

@@ -1,46 +1,48 @@
-// Encode ("splitzip_codec.py" encode_torch + assemble_payload), one pass over
-// the input with in-order escape compaction.
+// Encode ("splitzip_codec.py" encode_torch + assemble_payload): one streaming
+// pass over the input, then the in-order placement of the escape stream.
 //
 // Launches per call (after a 256-byte header memset):
-//   enc_prepare  validates the item table and zeroes the tile status words;
-//   enc_main     persistent CTAs take 8192-element tiles from a device-wide
-//                ticket (so tiles start in ascending order), stream them in
-//                with TMA bulk copies through a 4-stage shared-memory ring and
-//                write pk and sm with coalesced stores.  Warp w of the 8
-//                consumer warps owns chunk w of the tile, so its ballot/popc
-//                escape count is the chunk's; a block scan gives the tile's
-//                count, and a decoupled lookback over the tile status words
-//                gives the tile's first global escape index.  chunk_id is then
-//                written in place (its offset depends on n only); local_pos
-//                and esc_val go to a per-item staging area because their
-//                offsets depend on the total escape count;
-//   enc_tail     moves local_pos/esc_val to their final offsets, zeroes every
-//                pad byte and writes the meta.
-//
-// Lookback status word per tile (64 bits): flag in the high half (1 = tile
-// aggregate, 2 = inclusive prefix), escape count in the low half.  Every wait
-// is bounded (kWaitTimeoutNs); on timeout SZ_FLAG_TIMEOUT is raised.
+//   enc_prepare  validates the item table, zeroes per-tensor escape totals,
+//                segment tickets and segment status words;
+//   enc_main     persistent CTAs own contiguous runs of 8192-element tiles.
+//                A producer warp streams each tile (and the tensor's enc_lut)
+//                into a 4-stage shared-memory ring with TMA bulk copies; 8
+//                chunk warps -- warp w owns chunk w (1024 elements) -- split
+//                and pack with coalesced pk/sm stores, and compact the chunk's
+//                escapes with ballot/popc in element order into the chunk's
+//                staging slot.  The chunk counts and each tensor's escape
+//                total are recorded.  No warp ever waits on another CTA.
+//   enc_place    per tensor, segments of 256 chunks (claimed by ticket, so
+//                segments start in order): a block scan of the chunk counts
+//                and a decoupled lookback across the tensor's segments give
+//                each escape its global index; chunk_id, local_pos and
+//                esc_val are then written once, in order, at their final
+//                offsets (the tensor's total is already known, so every
+//                offset is).  The segment holding chunk 0 also zeroes the pad
+//                bytes and writes the meta.
+// Every wait is bounded (kWaitTimeoutNs); on timeout SZ_FLAG_TIMEOUT is raised.
 #include "sz_internal.h"
 
 namespace sz {
 namespace {
 
 constexpr int kEncStages = 4;
-constexpr int kEncConsumerWarps = kChunksPerTile;  // one warp per chunk
-constexpr int kEncConsumers = kEncConsumerWarps * 32;
-constexpr int kEncThreads = kEncConsumers + 32;    // + producer warp
+constexpr int kEncChunkWarps = kChunksPerTile;  // one warp per chunk
+constexpr int kProducerWarp = kEncChunkWarps;
+constexpr int kEncThreads = (kEncChunkWarps + 1) * 32;
 constexpr int kEncCtasPerSm = 2;
 constexpr uint32_t kStageEnd = 1u, kStageInvalid = 2u;
+constexpr unsigned FULL = 0xFFFFFFFFu;
+constexpr uint32_t kSegChunks = 256;                     // chunks per placement segment
+constexpr uint32_t kSegTiles = kSegChunks / kChunksPerTile;  // 32
 constexpr unsigned long long kAgg = 1ull << 32, kIncl = 2ull << 32;
 
 struct __align__(128) EncStage {
-  uint16_t x[kTile];      // the tile's BF16 bit patterns
-  uint8_t enc_lut[256];   // the item's codebook enc_lut
-  unsigned long long ticket;
+  uint16_t x[kTile];     // the tile's BF16 bit patterns
+  uint8_t enc_lut[256];  // the tensor's codebook enc_lut
+  unsigned long long tile;  // global tile index
   uint8_t* payload;
-  uint16_t* lpos_stage;
-  uint8_t* ev_stage;
-  uint64_t off_sm, off_cid, capacity;
+  uint64_t off_sm;
   uint32_t lt, n_tile, flags, item;
 };
 
@@ -48,9 +50,6 @@ struct EncShared {
   EncStage st[kEncStages];
   uint64_t full[kEncStages];
   uint64_t empty[kEncStages];
-  uint32_t warp_cnt[kEncConsumerWarps];
-  uint32_t warp_off[kEncConsumerWarps];
-  uint32_t tile_base;
 };
 
 __global__ void enc_prepare(const __grid_constant__ Items items, EncWs ws) {
@@ -72,39 +71,98 @@ __global__ void enc_prepare(const __grid_constant__ Items items, EncWs ws) {
       if (i + 1 == items.count && it.tile_begin + tiles_of(it.n) != items.total_tiles) bad |= SZ_FLAG_ITEMS;
     }
     ws.item_flags[i] = bad;
+    ws.item_esc[i] = 0;
+    ws.seg_ticket[i] = 0;
     if (bad) set_flag(ws.hdr, bad);
-  }
-}
-
-// Walks back from tile j (inclusive) accumulating aggregates until an
-// inclusive prefix is found.  Returns the exclusive prefix of tile j + 1.
-__device__ uint32_t lookback(const unsigned long long* status, uint64_t j, bool* timed_out) {
-  uint32_t excl = 0;
-  uint64_t t0 = 0;
-  uint32_t spins = 0;
-  for (;;) {
-    const unsigned long long v = ld_acquire_u64(status + j);
-    const unsigned long long flag = v & ~0xFFFFFFFFull;
-    if (flag == 0) {
-      if ((++spins & 31) == 0) {
-        const uint64_t now = global_timer_ns();
-        if (t0 == 0) t0 = now;
-        else if (now - t0 > kWaitTimeoutNs) {
-          *timed_out = true;
-          return excl;
-        }
-      }
-      continue;
-    }
-    excl += uint32_t(v);
-    if (flag == kIncl) return excl;
-    --j;
   }
 }
 
 __device__ __forceinline__ uint32_t sm_pair(uint32_t w) {
   // two BF16 patterns in w -> sm bytes at byte 0 and byte 2
   return (w & 0x007F007Fu) | ((w >> 8) & 0x00800080u);
+}
+
+// Bounded mbarrier wait agreed by the whole warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+  return __all_sync(FULL, mbar_wait(bar, parity));
+}
+
+// enc_lut codes of the 4 elements held in v (element k in bits 16k..16k+15 of
+// v.x, v.y), one per byte (element k in byte k).  Shifting a word left by one
+// puts the exponent bytes of its two elements at bytes 1 and 3.
+__device__ __forceinline__ uint32_t codes4(const uint8_t* lut, uint2 v) {
+  const uint32_t ax = v.x << 1, ay = v.y << 1;
+  const uint32_t c0 = lut[__byte_perm(ax, 0, 0x4441)];
+  const uint32_t c1 = lut[__byte_perm(ax, 0, 0x4443)];
+  const uint32_t c2 = lut[__byte_perm(ay, 0, 0x4441)];
+  const uint32_t c3 = lut[__byte_perm(ay, 0, 0x4443)];
+  return c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+}
+
+// Split + pack of chunk `warp` of the tile in `st`, with its escapes compacted
+// in element order into (lslot, eslot).  Each lane handles 4 consecutive
+// elements per row of 128.  Escape handling is byte-parallel: an enc_lut value
+// >= 16 (a non-zero high nibble) marks an escape, stored in pk as code 0.
+// Returns the chunk's escape count.  FULL_TILE: all 8192 elements exist.
+template <bool FULL_TILE>
+__device__ __forceinline__ uint32_t encode_chunk(const EncStage& st, uint32_t warp, uint32_t lane, uint16_t* lslot,
+                                                 uint8_t* eslot) {
+  const uint8_t* lut = st.enc_lut;
+  const uint32_t nt = st.n_tile;
+  const uint64_t g = uint64_t(st.lt) * kTile;
+  const uint32_t e0 = warp * kChunk + lane * 4u;  // element of this lane in row 0
+  const uint16_t* xw = st.x + e0;
+  uint8_t* pkw = st.payload + (g >> 1) + (e0 >> 1);
+  uint8_t* smw = st.payload + st.off_sm + g + e0;
+  const uint32_t lane_lt = (1u << lane) - 1u;
+  uint32_t run = 0;  // escapes of this chunk so far (warp-uniform)
+#pragma unroll
+  for (int row = 0; row < 8; ++row) {
+    const uint2 v = *reinterpret_cast<const uint2*>(xw + row * 128);
+    uint32_t packed = codes4(lut, v);
+    uint32_t nvalid = 4;
+    if (!FULL_TILE) {
+      const uint32_t il = e0 + uint32_t(row) * 128u;
+      nvalid = (il < nt) ? ((nt - il) < 4u ? nt - il : 4u) : 0u;
+      if (nvalid < 4) packed &= (1u << (8 * nvalid)) - 1u;  // absent elements: code 0, no escape
+    }
+    const uint32_t hi = packed & 0xF0F0F0F0u;
+    uint32_t clean = packed & 0x0F0F0F0Fu;
+    uint32_t m = 0;
+    if (hi) {
+      m = ((hi >> 4) + 0x7F7F7F7Fu) & 0x80808080u;  // bit 7 of each escape byte
+      clean &= ~((m >> 7) * 0xFFu);
+    }
+    const uint32_t t = clean | (clean >> 4);  // byte 0 = c0 | c1 << 4, byte 2 = c2 | c3 << 4
+    const uint32_t pk16 = __byte_perm(t, 0, 0x4420);
+    const uint32_t sm4 = __byte_perm(sm_pair(v.x), sm_pair(v.y), 0x6420);
+    if (FULL_TILE || nvalid == 4) {
+      *reinterpret_cast<uint16_t*>(pkw + row * 64) = uint16_t(pk16);
+      *reinterpret_cast<uint32_t*>(smw + row * 128) = sm4;
+    } else if (nvalid > 0) {
+      pkw[row * 64] = uint8_t(pk16);
+      if (nvalid > 2) pkw[row * 64 + 1] = uint8_t(pk16 >> 8);
+      for (uint32_t k = 0; k < nvalid; ++k) smw[row * 128 + k] = uint8_t(sm4 >> (8 * k));
+    }
+    if (__ballot_sync(FULL, m != 0)) {
+      const uint32_t escm = ((m >> 7) & 1u) | ((m >> 14) & 2u) | ((m >> 21) & 4u) | ((m >> 28) & 8u);
+      const uint32_t b0 = __ballot_sync(FULL, escm & 1u), b1 = __ballot_sync(FULL, escm & 2u);
+      const uint32_t b2 = __ballot_sync(FULL, escm & 4u), b3 = __ballot_sync(FULL, escm & 8u);
+      uint32_t pos = run + __popc(b0 & lane_lt) + __popc(b1 & lane_lt) + __popc(b2 & lane_lt) +
+                     __popc(b3 & lane_lt);
+      const uint32_t ex[4] = {(v.x >> 7) & 0xFFu, (v.x >> 23) & 0xFFu, (v.y >> 7) & 0xFFu, (v.y >> 23) & 0xFFu};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if ((escm >> k) & 1u) {
+          lslot[pos] = uint16_t(row * 128 + lane * 4 + k);
+          eslot[pos] = uint8_t(ex[k]);
+          ++pos;
+        }
+      }
+      run += __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
+    }
+  }
+  return run;
 }
 
 __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
@@ -117,32 +175,32 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
   // an inconsistent item table (flagged by enc_prepare) is never walked
   if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
 
+  const uint64_t T = items.total_tiles;
+  const uint64_t per = (T + gridDim.x - 1) / gridDim.x;
+  const uint64_t t0 = uint64_t(blockIdx.x) * per;
+  const uint64_t t1 = (t0 + per < T) ? t0 + per : T;
+
   if (tid == 0) {
     for (int s = 0; s < kEncStages; ++s) {
       mbar_init(&sh.full[s], 1 + 32);
-      mbar_init(&sh.empty[s], kEncConsumerWarps);
+      mbar_init(&sh.empty[s], kEncChunkWarps);
     }
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kEncConsumerWarps) {
+  if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer warp
-    unsigned long long ticket = 0;
-    if (lane == 0) ticket = atomicAdd(&ws.hdr->ticket, 1ull);
-    uint32_t cur = 0xFFFFFFFFu;
-    uint64_t cur_begin = 0;
-    for (uint32_t it = 0;; ++it) {
+    uint32_t cur = 0;
+    uint64_t cur_begin = 0, cur_end = 0;
+    for (uint64_t t = t0, it = 0;; ++t, ++it) {
       const int s = int(it % kEncStages);
-      if (it >= uint32_t(kEncStages)) {
-        if (!mbar_wait(&sh.empty[s], ((it / kEncStages) - 1) & 1)) {
-          if (lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
-          return;
-        }
+      if (it >= uint64_t(kEncStages) && !warp_wait(&sh.empty[s], uint32_t((it / kEncStages) - 1) & 1)) {
+        if (lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+        return;
       }
-      ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
       EncStage& st = sh.st[s];
-      if (ticket >= items.total_tiles) {
+      if (t >= t1) {
         if (lane == 0) {
           st.flags = kStageEnd;
           mbar_arrive(&sh.full[s]);
@@ -150,164 +208,61 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
         cp_async_mbar_arrive_noinc(&sh.full[s]);
         return;
       }
-      if (cur == 0xFFFFFFFFu || ticket < cur_begin || ticket >= cur_begin + tiles_of(item_at(items, cur).n)) {
-        cur = find_item(items, ticket);
+      if (t >= cur_end) {
+        cur = find_item(items, t);
         cur_begin = item_at(items, cur).tile_begin;
+        cur_end = cur_begin + tiles_of(item_at(items, cur).n);
       }
       const sz_item& itm = item_at(items, cur);
-      const uint32_t lt = uint32_t(ticket - cur_begin);
+      const uint32_t lt = uint32_t(t - cur_begin);
       const uint64_t g = uint64_t(lt) * kTile;
       const bool invalid = ws.item_flags[cur] != 0 || g >= itm.n;
       const uint32_t nt = invalid ? 0u : ((itm.n - g < kTile) ? uint32_t(itm.n - g) : kTile);
-      const uint32_t bulk = invalid ? 0u : ((nt * 2u) & ~15u);
-      const uint32_t tail = invalid ? 0u : (nt * 2u - bulk);
+      const uint32_t bulk = (nt * 2u) & ~15u;
+      const uint32_t tail = nt * 2u - bulk;
       if (lane == 0) {
-        st.ticket = ticket;
+        st.tile = t;
         st.item = cur;
         st.lt = lt;
         st.n_tile = nt;
         st.flags = invalid ? kStageInvalid : 0u;
         if (!invalid) {
-          const Layout l = layout_of(itm.n, 0);
           st.payload = itm.payload;
-          st.off_sm = l.off_sm;
-          st.off_cid = l.off_cid;
-          st.capacity = itm.capacity;
-          st.lpos_stage = ws.lpos + cur_begin * kTile;
-          st.ev_stage = ws.ev + cur_begin * kTile;
-        }
-        if (invalid) {
-          mbar_arrive(&sh.full[s]);
-        } else {
+          st.off_sm = layout_of(itm.n, 0).off_sm;
           mbar_arrive_expect_tx(&sh.full[s], bulk + 256u);
           if (bulk) bulk_g2s(st.x, itm.x + g, bulk, &sh.full[s]);
           bulk_g2s(st.enc_lut, itm.codebook->enc_lut, 256u, &sh.full[s]);
+        } else {
+          mbar_arrive(&sh.full[s]);
         }
       } else if (lane == 1 && tail) {
         cp_async16_zfill(reinterpret_cast<uint8_t*>(st.x) + bulk,
                          reinterpret_cast<const uint8_t*>(itm.x + g) + bulk, tail);
       }
       cp_async_mbar_arrive_noinc(&sh.full[s]);
-      if (lane == 0) ticket = atomicAdd(&ws.hdr->ticket, 1ull);
     }
   }
 
-  // ------------------------------------------------------------------ consumer warps
-  const unsigned FULL = 0xFFFFFFFFu;
-  const uint32_t lane_lt = (1u << lane) - 1u;
+  // ------------------------------------------------------------------ chunk warps
   for (uint32_t it = 0;; ++it) {
     const int s = int(it % kEncStages);
-    // every consumer thread waits (bounded); the vote keeps all warps on the
-    // same path so no named barrier below can be left short of threads
-    const bool ok = mbar_wait(&sh.full[s], (it / kEncStages) & 1);
-    if (named_bar_red_or(1, kEncConsumers, !ok)) {
-      if (tid == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+    if (!warp_wait(&sh.full[s], (it / kEncStages) & 1)) {
+      if (lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
       break;
     }
     const EncStage& st = sh.st[s];
     const uint32_t flags = st.flags;
     if (flags & kStageEnd) break;
-    const bool valid = !(flags & kStageInvalid);
-    const uint32_t nt = st.n_tile;
-    const uint32_t lt = st.lt;
-    const uint64_t g = uint64_t(lt) * kTile;
-    uint32_t wcnt = 0, esc_rows = 0;
-
-    if (valid) {
-      uint8_t* const pk = st.payload + (g >> 1);
-      uint8_t* const smp = st.payload + st.off_sm + g;
-#pragma unroll 2
-      for (int row = 0; row < 8; ++row) {
-        const uint32_t il = uint32_t(warp) * kChunk + uint32_t(row) * 128u + uint32_t(lane) * 4u;
-        const uint2 v = *reinterpret_cast<const uint2*>(st.x + il);
-        const uint32_t e0 = (v.x >> 7) & 0xFFu, e1 = (v.x >> 23) & 0xFFu;
-        const uint32_t e2 = (v.y >> 7) & 0xFFu, e3 = (v.y >> 23) & 0xFFu;
-        uint32_t c0 = st.enc_lut[e0], c1 = st.enc_lut[e1], c2 = st.enc_lut[e2], c3 = st.enc_lut[e3];
-        const uint32_t nvalid = (il < nt) ? ((nt - il) < 4u ? nt - il : 4u) : 0u;
-        if (nvalid < 4) {
-          if (nvalid < 4) c3 = 0;
-          if (nvalid < 3) c2 = 0;
-          if (nvalid < 2) c1 = 0;
-          if (nvalid < 1) c0 = 0;
-        }
-        // any enc_lut value >= 16 marks an escape, stored as code 0
-        const uint32_t escm = uint32_t(c0 > 15u) | (uint32_t(c1 > 15u) << 1) | (uint32_t(c2 > 15u) << 2) |
-                              (uint32_t(c3 > 15u) << 3);
-        c0 = c0 > 15u ? 0u : c0;
-        c1 = c1 > 15u ? 0u : c1;
-        c2 = c2 > 15u ? 0u : c2;
-        c3 = c3 > 15u ? 0u : c3;
-        const uint32_t pk16 = c0 | (c1 << 4) | (c2 << 8) | (c3 << 12);
-        const uint32_t sm4 = __byte_perm(sm_pair(v.x), sm_pair(v.y), 0x6420);
-        if (nvalid == 4) {
-          *reinterpret_cast<uint16_t*>(pk + (il >> 1)) = uint16_t(pk16);
-          *reinterpret_cast<uint32_t*>(smp + il) = sm4;
-        } else if (nvalid > 0) {
-          pk[il >> 1] = uint8_t(pk16);
-          if (nvalid > 2) pk[(il >> 1) + 1] = uint8_t(pk16 >> 8);
-          for (uint32_t k = 0; k < nvalid; ++k) smp[il + k] = uint8_t(sm4 >> (8 * k));
-        }
-        const uint32_t rowcnt = __reduce_add_sync(FULL, __popc(escm));
-        if (rowcnt) {
-          esc_rows |= 1u << row;
-          wcnt += rowcnt;
-        }
-      }
-    }
-    if (lane == 0) sh.warp_cnt[warp] = wcnt;
-    named_bar_sync(1, kEncConsumers);
-    if (tid == 0) {
-      uint32_t agg = 0;
-      for (int w = 0; w < kEncConsumerWarps; ++w) {
-        sh.warp_off[w] = agg;
-        agg += sh.warp_cnt[w];
-      }
-      unsigned long long* status = ws.status;
-      const unsigned long long ticket = st.ticket;
-      uint32_t base = 0;
-      if (!valid || lt == 0) {
-        st_release_u64(status + ticket, kIncl | agg);
-      } else {
-        st_release_u64(status + ticket, kAgg | agg);
-        bool timed_out = false;
-        base = lookback(status, ticket - 1, &timed_out);
-        if (timed_out) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
-        st_release_u64(status + ticket, kIncl | (base + agg));
-      }
-      sh.tile_base = base;
-    }
-    named_bar_sync(1, kEncConsumers);
-    if (esc_rows) {
-      uint32_t e_idx = sh.tile_base + sh.warp_off[warp];
-      const uint32_t chunk_id = lt * kChunksPerTile + uint32_t(warp);
-      uint8_t* const cidp = st.payload + st.off_cid;
-      const uint64_t cap = st.capacity;
-      uint16_t* const lps = st.lpos_stage;
-      uint8_t* const evs = st.ev_stage;
-      for (int row = 0; row < 8; ++row) {
-        if (!((esc_rows >> row) & 1u)) continue;
-        const uint32_t il = uint32_t(warp) * kChunk + uint32_t(row) * 128u + uint32_t(lane) * 4u;
-        const uint2 v = *reinterpret_cast<const uint2*>(st.x + il);
-        uint32_t e[4] = {(v.x >> 7) & 0xFFu, (v.x >> 23) & 0xFFu, (v.y >> 7) & 0xFFu, (v.y >> 23) & 0xFFu};
-        uint32_t escm = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if (il + k < nt && st.enc_lut[e[k]] > 15u) escm |= 1u << k;
-        const uint32_t b0 = __ballot_sync(FULL, escm & 1u), b1 = __ballot_sync(FULL, escm & 2u);
-        const uint32_t b2 = __ballot_sync(FULL, escm & 4u), b3 = __ballot_sync(FULL, escm & 8u);
-        uint32_t pos = e_idx + __popc(b0 & lane_lt) + __popc(b1 & lane_lt) + __popc(b2 & lane_lt) +
-                       __popc(b3 & lane_lt);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if ((escm >> k) & 1u) {
-            const uint64_t cid_off = st.off_cid + 4ull * pos;
-            if (cid_off + 4 <= cap) *reinterpret_cast<uint32_t*>(cidp + 4ull * pos) = chunk_id;
-            lps[pos] = uint16_t(row * 128 + lane * 4 + k);
-            evs[pos] = uint8_t(e[k]);
-            ++pos;
-          }
-        }
-        e_idx += __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
+    if (!(flags & kStageInvalid)) {
+      const uint64_t chunk = st.tile * kChunksPerTile + uint32_t(warp);  // global chunk index
+      uint16_t* lslot = ws.lpos + chunk * kChunk;
+      uint8_t* eslot = ws.ev + chunk * kChunk;
+      const uint32_t run = (st.n_tile == kTile)
+                               ? encode_chunk<true>(st, uint32_t(warp), uint32_t(lane), lslot, eslot)
+                               : encode_chunk<false>(st, uint32_t(warp), uint32_t(lane), lslot, eslot);
+      if (lane == 0) {
+        ws.chunk_cnt[chunk] = uint16_t(run);
+        if (run) atomicAdd(ws.item_esc + st.item, run);
       }
     }
     __syncwarp();
@@ -315,57 +270,152 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
   }
 }
 
-// One CTA row (blockIdx.y) per item; blockIdx.x strides over its escapes.
-__global__ void enc_tail(const __grid_constant__ Items items, EncWs ws) {
+// Decoupled lookback over the placement segments of one tensor: lane l reads
+// the status of segment j - l (status word at the segment's first tile,
+// tile_begin + seg * kSegTiles).  Segment 0 always publishes an inclusive
+// prefix.  Returns the exclusive prefix of segment j + 1.  Bounded.
+__device__ uint32_t segment_lookback(const unsigned long long* status, uint64_t tile_begin, int64_t j,
+                                     bool* timed_out) {
+  const uint32_t lane = threadIdx.x & 31u;
+  uint32_t excl = 0;
+  uint64_t t0 = 0;
+  uint32_t spins = 0;
+  for (;;) {
+    if (j < 0) return excl;  // cannot happen: segment 0 is inclusive
+    const int64_t seg = j - int64_t(lane);
+    const unsigned long long v = seg >= 0 ? ld_relaxed_u64(status + tile_begin + uint64_t(seg) * kSegTiles) : kIncl;
+    const unsigned long long flag = v & ~0xFFFFFFFFull;
+    const uint32_t incl = __ballot_sync(FULL, flag == kIncl);
+    const uint32_t zero = __ballot_sync(FULL, flag == 0);
+    const uint32_t stop = incl ? uint32_t(__ffs(incl) - 1) : 31u;
+    const uint32_t upto = (stop == 31u) ? FULL : ((2u << stop) - 1u);
+    if (zero & upto) {
+      __nanosleep(32);
+      if ((++spins & 15) == 0) {
+        const uint64_t now = global_timer_ns();
+        if (t0 == 0) {
+          t0 = now;
+        } else if (now - t0 > kWaitTimeoutNs) {
+          *timed_out = true;
+          return excl;
+        }
+      }
+      continue;
+    }
+    excl += __reduce_add_sync(FULL, lane <= stop ? uint32_t(v) : 0u);
+    if (incl) return excl;
+    j -= 32;
+  }
+}
+
+constexpr int kPlaceThreads = kSegChunks;  // one thread per chunk of the segment
+
+__global__ void __launch_bounds__(kPlaceThreads) enc_place(const __grid_constant__ Items items, EncWs ws) {
+  __shared__ uint32_t off[kSegChunks + 1];  // exclusive offsets of the segment's chunks, then the total
+  __shared__ uint32_t wsum[kPlaceThreads / 32];
+  __shared__ uint32_t s_seg, s_base;
+  const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+  if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
   for (uint32_t i = blockIdx.y; i < items.count; i += gridDim.y) {
     const sz_item& it = item_at(items, i);
     uint32_t flags = ws.item_flags[i];
-    const uint64_t tiles = tiles_of(it.n);
-    uint64_t e = 0;
-    if (!flags && tiles) {
-      const unsigned long long v = ws.status[it.tile_begin + tiles - 1];
-      if ((v & ~0xFFFFFFFFull) != kIncl) flags |= SZ_FLAG_TIMEOUT;
-      e = uint32_t(v);
-    }
-    const Layout l = layout_of(it.n, e);
+    const uint64_t n = (flags & SZ_FLAG_SIZE) ? 0 : it.n;
+    const uint32_t e = ws.item_esc[i];
+    const Layout l = layout_of(n, e);
     if (!flags && l.comp_bytes > it.capacity) flags |= SZ_FLAG_CAPACITY;
-    if (!flags) {
-      uint8_t* p = it.payload;
-      const uint16_t* lps = ws.lpos + it.tile_begin * kTile;
-      const uint8_t* evs = ws.ev + it.tile_begin * kTile;
-      const uint64_t stride = uint64_t(gridDim.x) * blockDim.x;
-      for (uint64_t k = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < e; k += stride) {
-        *reinterpret_cast<uint16_t*>(p + l.off_lpos + 2 * k) = lps[k];
-        p[l.off_ev + k] = evs[k];
-      }
-      if (blockIdx.x == 0 && threadIdx.x < 16) {
+    if (blockIdx.x == 0) {
+      if (!flags && tid < 12) {
         // pad bytes: pk -> sm, sm -> chunk_id, local_pos -> esc_val (each < 4 bytes)
-        const uint32_t t = threadIdx.x;
-        if (t < 4 && l.n_pairs + t < l.off_sm) p[l.n_pairs + t] = 0;
-        if (t >= 4 && t < 8 && l.off_sm + it.n + (t - 4) < l.off_cid) p[l.off_sm + it.n + (t - 4)] = 0;
-        if (t >= 8 && t < 12 && l.off_lpos + 2 * e + (t - 8) < l.off_ev) p[l.off_lpos + 2 * e + (t - 8)] = 0;
+        uint8_t* p = it.payload;
+        if (tid < 4 && l.n_pairs + tid < l.off_sm) p[l.n_pairs + tid] = 0;
+        if (tid >= 4 && tid < 8 && l.off_sm + n + (tid - 4) < l.off_cid) p[l.off_sm + n + (tid - 4)] = 0;
+        if (tid >= 8 && l.off_lpos + 2ull * e + (tid - 8) < l.off_ev) p[l.off_lpos + 2ull * e + (tid - 8)] = 0;
+      }
+      if (tid == 0) {
+        if (flags) set_flag(ws.hdr, flags);
+        if (it.meta != nullptr && (reinterpret_cast<uintptr_t>(it.meta) & 15) == 0) {
+          sz_meta m;
+          m.n = n;
+          m.n_pairs = l.n_pairs;
+          m.n_esc = e;
+          m.comp_bytes = l.comp_bytes;
+          m.off_pk = 0;
+          m.off_sm = l.off_sm;
+          m.off_cid = l.off_cid;
+          m.off_lpos = l.off_lpos;
+          m.off_ev = l.off_ev;
+          m.chunk_size = kChunk;
+          m.status = flags;
+          m.coverage = (it.codebook && !(reinterpret_cast<uintptr_t>(it.codebook) & 15)) ? it.codebook->coverage : 0.0;
+          m.reserved1 = 0;
+          *it.meta = m;
+        }
       }
     }
-    if (flags) {
-      if (blockIdx.x == 0 && threadIdx.x == 0) set_flag(ws.hdr, flags);
-    }
-    if (blockIdx.x == 0 && threadIdx.x == 0 && it.meta != nullptr &&
-        (reinterpret_cast<uintptr_t>(it.meta) & 15) == 0) {
-      sz_meta m;
-      m.n = it.n;
-      m.n_pairs = l.n_pairs;
-      m.n_esc = e;
-      m.comp_bytes = l.comp_bytes;
-      m.off_pk = 0;
-      m.off_sm = l.off_sm;
-      m.off_cid = l.off_cid;
-      m.off_lpos = l.off_lpos;
-      m.off_ev = l.off_ev;
-      m.chunk_size = kChunk;
-      m.status = flags;
-      m.coverage = (it.codebook && !(reinterpret_cast<uintptr_t>(it.codebook) & 15)) ? it.codebook->coverage : 0.0;
-      m.reserved1 = 0;
-      *it.meta = m;
+    if (flags) continue;
+    const uint64_t chunks = (n + kChunk - 1) / kChunk;
+    const uint64_t segs = (chunks + kSegChunks - 1) / kSegChunks;
+    const uint64_t chunk_base = it.tile_begin * kChunksPerTile;
+    uint8_t* const cid_p = it.payload + l.off_cid;
+    uint8_t* const lpos_p = it.payload + l.off_lpos;
+    uint8_t* const ev_p = it.payload + l.off_ev;
+    for (;;) {
+      __syncthreads();  // the previous segment's s_seg / off are no longer read
+      if (tid == 0) s_seg = atomicAdd(ws.seg_ticket + i, 1u);
+      __syncthreads();
+      const uint64_t seg = s_seg;
+      if (seg >= segs) break;
+      // block exclusive scan of the segment's chunk counts
+      const uint64_t c = seg * kSegChunks + tid;
+      const uint32_t cnt = (c < chunks) ? ws.chunk_cnt[chunk_base + c] : 0u;
+      uint32_t incl = cnt;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t o = __shfl_up_sync(FULL, incl, d);
+        if (lane >= uint32_t(d)) incl += o;
+      }
+      if (lane == 31) wsum[warp] = incl;
+      __syncthreads();
+      uint32_t wbase = 0;
+      for (uint32_t w = 0; w < warp; ++w) wbase += wsum[w];
+      off[tid] = wbase + incl - cnt;
+      if (tid == kPlaceThreads - 1) off[kSegChunks] = wbase + incl;
+      __syncthreads();
+      const uint32_t agg = off[kSegChunks];
+      if (warp == 0) {
+        unsigned long long* st = ws.status + it.tile_begin + seg * kSegTiles;
+        uint32_t base = 0;
+        if (seg == 0) {
+          if (lane == 0) st_relaxed_u64(st, kIncl | agg);
+        } else {
+          if (lane == 0) st_relaxed_u64(st, kAgg | agg);
+          bool timed_out = false;
+          base = segment_lookback(ws.status, it.tile_begin, int64_t(seg) - 1, &timed_out);
+          if (lane == 0) {
+            if (timed_out) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+            st_relaxed_u64(st, kIncl | (base + agg));
+          }
+        }
+        if (lane == 0) s_base = base;
+      }
+      __syncthreads();
+      const uint32_t base = s_base;
+      // scatter: escape j of the segment -> global index base + j
+      for (uint32_t j = tid; j < agg; j += kPlaceThreads) {
+        uint32_t lo = 0, hi = kSegChunks;  // last chunk q with off[q] <= j
+        while (hi - lo > 1) {
+          const uint32_t mid = (lo + hi) >> 1;
+          if (off[mid] <= j) lo = mid; else hi = mid;
+        }
+        const uint32_t k = j - off[lo];
+        const uint64_t slot = (chunk_base + seg * kSegChunks + lo) * kChunk + k;
+        const uint64_t gidx = uint64_t(base) + j;
+        if (gidx < e) {
+          *reinterpret_cast<uint32_t*>(cid_p + 4 * gidx) = uint32_t(seg * kSegChunks + lo);
+          *reinterpret_cast<uint16_t*>(lpos_p + 2 * gidx) = ws.lpos[slot] & uint16_t(kChunk - 1);
+          ev_p[gidx] = ws.ev[slot];
+        }
+      }
     }
   }
 }
@@ -400,13 +450,13 @@ cudaError_t launch_encode(const Items& items, void* ws_base, cudaStream_t stream
     if (err != cudaSuccess) return err;
   }
   {
-    uint64_t per_item = items.count ? items.total_tiles / items.count : 0;
-    uint64_t gx = per_item / 8;
-    const uint64_t gx_cap = uint64_t(dev.num_sms) * 2;
+    // blockIdx.y = tensor; x covers the average tensor's segments
+    const uint64_t per_item = items.count ? (items.total_tiles + items.count - 1) / items.count : 0;
+    uint64_t gx = (per_item + kSegTiles - 1) / kSegTiles;
     if (gx < 1) gx = 1;
-    if (gx > gx_cap) gx = gx_cap;
+    if (gx > 1024) gx = 1024;
     const unsigned gy = items.count < 65535u ? items.count : 65535u;
-    enc_tail<<<dim3(unsigned(gx), gy), 256, 0, stream>>>(items, ws);
+    enc_place<<<dim3(unsigned(gx), gy), kPlaceThreads, 0, stream>>>(items, ws);
     err = cudaGetLastError();
   }
   return err;
