@@ -46,7 +46,35 @@ struct __align__(128) EncStage {
   uint32_t lt, n_tile, flags, item;
 };
 
+constexpr uint32_t kRun = 4;  // tiles per ticket
+
+// What the producer needs of an item; cached in shared memory for tables of
+// up to kCachedItems items, so mapping a ticket to its item costs no global
+// round trip.
+constexpr uint32_t kCachedItems = 128;
+struct ItemLite {
+  uint64_t tile_begin, n;
+  const uint16_t* x;
+  uint8_t* payload;
+  const uint8_t* enc_lut;
+  uint32_t flags, pad;
+};
+
+__device__ __forceinline__ ItemLite item_lite(const Items& items, const EncWs& ws, uint32_t i) {
+  const sz_item& it = item_at(items, i);
+  ItemLite l;
+  l.tile_begin = it.tile_begin;
+  l.n = it.n;
+  l.x = it.x;
+  l.payload = it.payload;
+  l.flags = ws.item_flags[i];
+  l.enc_lut = l.flags ? nullptr : it.codebook->enc_lut;
+  l.pad = 0;
+  return l;
+}
+
 struct EncShared {
+  ItemLite item[kCachedItems];
   EncStage st[kEncStages];
   uint64_t full[kEncStages];
   uint64_t empty[kEncStages];
@@ -165,6 +193,117 @@ __device__ __forceinline__ uint32_t encode_chunk(const EncStage& st, uint32_t wa
   return run;
 }
 
+// sm bytes of the two BF16 patterns of w at bytes 0 and 2 (bytes 1 and 3 are
+// don't-care): bit 7 of each comes from bit 15 of its pattern.
+__device__ __forceinline__ uint32_t sm_pair_lo(uint32_t w) {
+  const uint32_t s = w >> 8;
+  return (w & 0x007F007Fu) | (s & ~0x007F007Fu);  // one bit-select
+}
+
+// Exclusive warp prefix of per-lane counts `c` (0..8) and the warp total.
+// Most rows hold at most one escape per lane: then two ballots suffice.
+__device__ __forceinline__ uint32_t warp_prefix(uint32_t c, uint32_t lane, uint32_t* total) {
+  const uint32_t lane_lt = (1u << lane) - 1u;
+  const uint32_t b1 = __ballot_sync(FULL, c >= 1);
+  const uint32_t b2 = __ballot_sync(FULL, c >= 2);
+  if (b2 == 0) {
+    *total = __popc(b1);
+    return __popc(b1 & lane_lt);
+  }
+  uint32_t incl = c;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t o = __shfl_up_sync(FULL, incl, d);
+    if (lane >= uint32_t(d)) incl += o;
+  }
+  *total = __shfl_sync(FULL, incl, 31);
+  return incl - c;
+}
+
+// Full tile, 8 elements per lane per row of 256 (4 rows per chunk).
+// Same output as encode_chunk<true>: pk/sm of the chunk, its escapes in
+// element order in (lslot, eslot); returns the escape count.
+__device__ __forceinline__ uint32_t encode_chunk8(const EncStage& st, uint32_t warp, uint32_t lane, uint16_t* lslot,
+                                                  uint8_t* eslot) {
+  const uint8_t* lut = st.enc_lut;
+  const uint64_t g = uint64_t(st.lt) * kTile;
+  const uint32_t e0 = warp * kChunk + lane * 8u;
+  const uint16_t* xw = st.x + e0;
+  uint8_t* pkw = st.payload + (g >> 1) + (e0 >> 1);
+  uint8_t* smw = st.payload + st.off_sm + g + e0;
+  const bool sm8 = ((st.off_sm & 7u) == 0);
+  uint32_t lane_esc = 0;  // bit 8*row + k: element k of this lane's 8 in `row` escapes
+#pragma unroll
+  for (int row = 0; row < 4; ++row) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xw + row * 256);
+    const uint32_t a0 = v.x << 1, a1 = v.y << 1, a2 = v.z << 1, a3 = v.w << 1;
+    const uint32_t lo = uint32_t(lut[__byte_perm(a0, 0, 0x4441)]) | (uint32_t(lut[__byte_perm(a0, 0, 0x4443)]) << 8) |
+                        (uint32_t(lut[__byte_perm(a1, 0, 0x4441)]) << 16) |
+                        (uint32_t(lut[__byte_perm(a1, 0, 0x4443)]) << 24);
+    const uint32_t hi = uint32_t(lut[__byte_perm(a2, 0, 0x4441)]) | (uint32_t(lut[__byte_perm(a2, 0, 0x4443)]) << 8) |
+                        (uint32_t(lut[__byte_perm(a3, 0, 0x4441)]) << 16) |
+                        (uint32_t(lut[__byte_perm(a3, 0, 0x4443)]) << 24);
+    uint32_t clo = lo & 0x0F0F0F0Fu, chi = hi & 0x0F0F0F0Fu;
+    if ((lo | hi) & 0xF0F0F0F0u) {  // an enc_lut value >= 16: escape, stored as code 0
+      const uint32_t mlo = (((lo & 0xF0F0F0F0u) >> 4) + 0x7F7F7F7Fu) & 0x80808080u;
+      const uint32_t mhi = (((hi & 0xF0F0F0F0u) >> 4) + 0x7F7F7F7Fu) & 0x80808080u;
+      clo &= ~((mlo >> 7) * 0xFFu);
+      chi &= ~((mhi >> 7) * 0xFFu);
+      // gather bit 7 of each byte (element k of the 8) into bit k of this row's byte
+      const uint32_t g = ((((mlo >> 7) * 0x00204081u) >> 21) & 0xFu) | (((((mhi >> 7) * 0x00204081u) >> 21) & 0xFu) << 4);
+      lane_esc |= g << (8 * row);
+    }
+    const uint32_t tlo = clo | (clo >> 4), thi = chi | (chi >> 4);
+    *reinterpret_cast<uint32_t*>(pkw + row * 128) = __byte_perm(tlo, thi, 0x6420);
+    const uint32_t s01 = __byte_perm(sm_pair_lo(v.x), sm_pair_lo(v.y), 0x6420);
+    const uint32_t s23 = __byte_perm(sm_pair_lo(v.z), sm_pair_lo(v.w), 0x6420);
+    if (sm8) {
+      *reinterpret_cast<uint2*>(smw + row * 256) = make_uint2(s01, s23);
+    } else {
+      *reinterpret_cast<uint32_t*>(smw + row * 256) = s01;
+      *reinterpret_cast<uint32_t*>(smw + row * 256 + 4) = s23;
+    }
+  }
+  // Escapes of the chunk, in element order (row, lane, k): one pass per chunk.
+  if (__ballot_sync(FULL, lane_esc != 0) == 0) return 0;
+  const uint32_t lane_lt = (1u << lane) - 1u;
+  uint32_t c[4], before[4];
+  bool simple = true;  // at most one escape per lane and row: ballots give the prefixes
+#pragma unroll
+  for (int row = 0; row < 4; ++row) {
+    c[row] = __popc((lane_esc >> (8 * row)) & 0xFFu);
+    simple &= (c[row] <= 1);
+  }
+  uint32_t run = 0;
+  if (__all_sync(FULL, simple)) {
+#pragma unroll
+    for (int row = 0; row < 4; ++row) {
+      const uint32_t b = __ballot_sync(FULL, c[row] != 0);
+      before[row] = run + __popc(b & lane_lt);
+      run += __popc(b);
+    }
+  } else {
+#pragma unroll
+    for (int row = 0; row < 4; ++row) {
+      uint32_t total;
+      before[row] = run + warp_prefix(c[row], lane, &total);
+      run += total;
+    }
+  }
+  const uint16_t* xc = st.x + warp * kChunk;
+#pragma unroll
+  for (int row = 0; row < 4; ++row) {
+    uint32_t pos = before[row];
+    for (uint32_t m = (lane_esc >> (8 * row)) & 0xFFu; m; m &= m - 1) {
+      const uint32_t elem = uint32_t(row) * 256u + lane * 8u + uint32_t(__ffs(m) - 1);  // chunk-local
+      lslot[pos] = uint16_t(elem);
+      eslot[pos] = uint8_t((xc[elem] >> 7) & 0xFFu);
+      ++pos;
+    }
+  }
+  return run;
+}
+
 __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
     enc_main(const __grid_constant__ Items items, EncWs ws) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -176,9 +315,6 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
   if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
 
   const uint64_t T = items.total_tiles;
-  const uint64_t per = (T + gridDim.x - 1) / gridDim.x;
-  const uint64_t t0 = uint64_t(blockIdx.x) * per;
-  const uint64_t t1 = (t0 + per < T) ? t0 + per : T;
 
   if (tid == 0) {
     for (int s = 0; s < kEncStages; ++s) {
@@ -187,20 +323,32 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
     }
     fence_mbar_init();
   }
+  if (items.count <= kCachedItems)
+    for (uint32_t i = tid; i < items.count; i += kEncThreads) sh.item[i] = item_lite(items, ws, i);
   __syncthreads();
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer warp
-    uint32_t cur = 0;
-    uint64_t cur_begin = 0, cur_end = 0;
-    for (uint64_t t = t0, it = 0;; ++t, ++it) {
+    // Tiles are handed out in runs of kRun from a device-wide ticket, so CTAs
+    // that run faster (SM placement, neighbours) take more of them.
+    unsigned long long run_base = 0;
+    uint32_t run_pos = kRun;
+    uint32_t cur = 0xFFFFFFFFu;
+    ItemLite itm{};
+    for (uint32_t it = 0;; ++it) {
       const int s = int(it % kEncStages);
-      if (it >= uint64_t(kEncStages) && !warp_wait(&sh.empty[s], uint32_t((it / kEncStages) - 1) & 1)) {
+      if (it >= uint32_t(kEncStages) && !warp_wait(&sh.empty[s], ((it / kEncStages) - 1) & 1)) {
         if (lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
         return;
       }
+      if (run_pos == kRun) {
+        if (lane == 0) run_base = atomicAdd(&ws.hdr->ticket, 1ull * kRun);
+        run_base = __shfl_sync(FULL, run_base, 0);
+        run_pos = 0;
+      }
+      const uint64_t t = run_base + run_pos++;
       EncStage& st = sh.st[s];
-      if (t >= t1) {
+      if (t >= T) {
         if (lane == 0) {
           st.flags = kStageEnd;
           mbar_arrive(&sh.full[s]);
@@ -208,15 +356,25 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
         cp_async_mbar_arrive_noinc(&sh.full[s]);
         return;
       }
-      if (t >= cur_end) {
-        cur = find_item(items, t);
-        cur_begin = item_at(items, cur).tile_begin;
-        cur_end = cur_begin + tiles_of(item_at(items, cur).n);
+      if (cur == 0xFFFFFFFFu || t < itm.tile_begin || t >= itm.tile_begin + tiles_of(itm.n)) {
+        if (items.count <= kCachedItems) {
+          // last cached item with tile_begin <= t (empty items own no tile)
+          uint32_t lo = 0, hi = items.count;
+          while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (sh.item[mid].tile_begin <= t) lo = mid; else hi = mid;
+          }
+          cur = lo;
+          itm = sh.item[cur];
+        } else {
+          cur = find_item(items, t);
+          itm = item_lite(items, ws, cur);
+        }
       }
-      const sz_item& itm = item_at(items, cur);
+      const uint64_t cur_begin = itm.tile_begin;
       const uint32_t lt = uint32_t(t - cur_begin);
       const uint64_t g = uint64_t(lt) * kTile;
-      const bool invalid = ws.item_flags[cur] != 0 || g >= itm.n;
+      const bool invalid = itm.flags != 0 || g >= itm.n;
       const uint32_t nt = invalid ? 0u : ((itm.n - g < kTile) ? uint32_t(itm.n - g) : kTile);
       const uint32_t bulk = (nt * 2u) & ~15u;
       const uint32_t tail = nt * 2u - bulk;
@@ -231,7 +389,7 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
           st.off_sm = layout_of(itm.n, 0).off_sm;
           mbar_arrive_expect_tx(&sh.full[s], bulk + 256u);
           if (bulk) bulk_g2s(st.x, itm.x + g, bulk, &sh.full[s]);
-          bulk_g2s(st.enc_lut, itm.codebook->enc_lut, 256u, &sh.full[s]);
+          bulk_g2s(st.enc_lut, itm.enc_lut, 256u, &sh.full[s]);
         } else {
           mbar_arrive(&sh.full[s]);
         }
@@ -244,6 +402,10 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
   }
 
   // ------------------------------------------------------------------ chunk warps
+  // Escape totals per tensor are accumulated per warp and added to the global
+  // total only when the tensor changes: one global atomic per chunk would pile
+  // hundreds of thousands of updates onto a few words (one L2 slice).
+  uint32_t acc_item = 0xFFFFFFFFu, acc = 0;
   for (uint32_t it = 0;; ++it) {
     const int s = int(it % kEncStages);
     if (!warp_wait(&sh.full[s], (it / kEncStages) & 1)) {
@@ -258,16 +420,20 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
       uint16_t* lslot = ws.lpos + chunk * kChunk;
       uint8_t* eslot = ws.ev + chunk * kChunk;
       const uint32_t run = (st.n_tile == kTile)
-                               ? encode_chunk<true>(st, uint32_t(warp), uint32_t(lane), lslot, eslot)
+                               ? encode_chunk8(st, uint32_t(warp), uint32_t(lane), lslot, eslot)
                                : encode_chunk<false>(st, uint32_t(warp), uint32_t(lane), lslot, eslot);
-      if (lane == 0) {
-        ws.chunk_cnt[chunk] = uint16_t(run);
-        if (run) atomicAdd(ws.item_esc + st.item, run);
+      if (st.item != acc_item) {
+        if (lane == 0 && acc) atomicAdd(ws.item_esc + acc_item, acc);
+        acc_item = st.item;
+        acc = 0;
       }
+      acc += run;
+      if (lane == 0) ws.chunk_cnt[chunk] = uint16_t(run);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty[s]);
   }
+  if (lane == 0 && acc) atomicAdd(ws.item_esc + acc_item, acc);
 }
 
 // Decoupled lookback over the placement segments of one tensor: lane l reads
