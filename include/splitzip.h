@@ -207,6 +207,32 @@ SZ_API int sz_encode_many(const sz_item* d_items, uint32_t count, uint64_t total
 SZ_API int sz_decode_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles,
                           void* d_workspace, size_t workspace_bytes, sz_stream stream);
 
+/* ------------------------------------------------------------------ decode without a caller workspace */
+
+#define SZ_NOALLOC_MAX_ELEMS 268435456ull  /* 2^28 elements (512 MiB of BF16) */
+
+/* Decode for callers that cannot allocate device memory when they decode --
+ * e.g. a host framework that owns all device memory and does not let
+ * libraries allocate, or a latency-critical path that must not call
+ * cudaMalloc (which may synchronise the device).  No counterpart in the
+ * SplitZip pages: it is sz_decode with the workspace replaced by a fixed
+ * scratch array inside the library (a file-scope __device__ array of about
+ * 257 KiB, present on every device that loads the library until the process
+ * exits).  Nothing is allocated per call: no cudaMalloc, cudaFree or
+ * allocating library routine.
+ *   Arguments are those of sz_decode, without the workspace; n must not
+ *   exceed SZ_NOALLOC_MAX_ELEMS (larger tensors: SZ_ERR_ARG, use sz_decode).
+ *   d_flags: optional device pointer (4-byte aligned) that receives the
+ *   call's SZ_FLAG_* word asynchronously (0 = no device-side problem).
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  All calls on a device share the one array and each call starts
+ * by resetting what it reads, but calls whose work may overlap on the GPU
+ * (different streams without ordering) race on it: order them. */
+SZ_API int sz_decode_noalloc(const uint8_t* d_payload, uint64_t payload_bytes, const sz_meta* d_meta,
+                             const sz_codebook* d_codebook, uint16_t* d_out, uint64_t n, uint32_t* d_flags,
+                             sz_stream stream);
+
 /* ------------------------------------------------------------------ measurement */
 
 /* Timing hook: `before` and `after` are cudaEvent_t handles (or NULL to

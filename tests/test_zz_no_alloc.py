@@ -1,0 +1,87 @@
+"""sz_decode_noalloc: decode for callers that cannot allocate device memory when
+they decode (a framework that owns all device memory, or a latency-critical
+path that must not call cudaMalloc).  It keeps its scratch in a fixed array
+inside the library instead of taking a workspace.
+
+Checked through the C ABI against sz_decode (which takes a caller workspace):
+identical output on two calls in a row (the second reuses the array the first
+left behind), the status word reported through d_flags, and the size limit.
+This file is collected last so that a run stopping at the first failure has
+already run every other test.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import weight_compression_codec_gb300 as sz
+from weight_compression_codec_gb300 import binding as B
+from weight_compression_codec_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    sz.build()
+    torch.cuda.set_device(DEV)
+    return B.lib()
+
+
+def _encoded(x: np.ndarray):
+    xd = torch.from_numpy(x.view(np.int16)).to(DEV)
+    cb = sz.sz_calibrate(xd)
+    payload, meta = sz.sz_encode(xd, cb)
+    return payload, meta, cb
+
+
+def _noalloc(lib, payload, meta, cb, n, out, flags):
+    stream = torch.cuda.current_stream().cuda_stream
+    return lib.sz_decode_noalloc(payload.data_ptr(), payload.numel(), meta.data_ptr(), cb.data_ptr(),
+                                 out.data_ptr() if n else None, n, flags.data_ptr(), stream)
+
+
+def test_noalloc_decode_matches_workspace_decode_twice(lib):
+    cases = [inputs.gaussian(3 * 8192 + 555, 0.02, seed=21), inputs.edge_case(40_001, seed=22)]
+    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for x in cases:  # two calls in a row; the second finds the first one's scratch contents
+        payload, meta, cb = _encoded(x)
+        ref = sz.sz_decode(payload, meta, cb, x.size)
+        out = torch.full((x.size,), 7, dtype=torch.int16, device=DEV)
+        flags.fill_(-1)
+        assert _noalloc(lib, payload, meta, cb, x.size, out, flags) == B.SZ_OK
+        torch.cuda.synchronize()
+        assert int(flags.item()) == 0
+        assert torch.equal(out, ref.view(torch.int16))
+        assert np.array_equal(out.cpu().numpy().view(np.uint16), x)
+
+
+def test_noalloc_reports_device_flags_and_recovers(lib):
+    x = inputs.gaussian(20_000, 1.0, seed=23)
+    payload, meta, cb = _encoded(x)
+    flags = torch.zeros(1, dtype=torch.int32, device=DEV)
+    bad = sz.read_meta(meta)
+    import dataclasses
+
+    bad_meta = torch.frombuffer(bytearray(sz.meta_to_bytes(dataclasses.replace(bad, off_sm=bad.off_sm + 4))),
+                                dtype=torch.uint8).to(DEV)
+    out = torch.full((x.size,), 7, dtype=torch.int16, device=DEV)
+    assert _noalloc(lib, payload, bad_meta, cb, x.size, out, flags) == B.SZ_OK
+    torch.cuda.synchronize()
+    assert int(flags.item()) & B.SZ_FLAG_META and torch.all(out == 7)
+    # the next call starts from a clean status word
+    assert _noalloc(lib, payload, meta, cb, x.size, out, flags) == B.SZ_OK
+    torch.cuda.synchronize()
+    assert int(flags.item()) == 0
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), x)
+
+
+def test_noalloc_rejects_tensors_over_the_limit(lib):
+    p = ctypes.c_void_p(1 << 20)  # never dereferenced: the call returns before any launch
+    assert lib.sz_decode_noalloc(p, 1 << 40, p, p, p, B.SZ_NOALLOC_MAX_ELEMS + 1, None, None) == B.SZ_ERR_ARG

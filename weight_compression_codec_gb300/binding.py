@@ -101,7 +101,10 @@ SIGNATURES = {
     "sz_encode_many": (_INT, [_VP, _U32, _U64, _VP, _SZ, _VP]),
     "sz_decode_many": (_INT, [_VP, _U32, _U64, _VP, _SZ, _VP]),
     "sz_set_timing_events": (_INT, [_VP, _VP]),
+    "sz_decode_noalloc": (_INT, [_VP, _U64, _VP, _VP, _VP, _U64, _VP, _VP]),
 }
+
+SZ_NOALLOC_MAX_ELEMS = 268435456
 
 _LIB = None
 
