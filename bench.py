@@ -195,21 +195,28 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def kernel_sources_sha() -> str:
+KERNEL_SOURCES = {"cal_hist": "sz_calibrate.cu", "enc_main": "sz_encode.cu", "enc_place": "sz_encode.cu",
+                  "dec_main": "sz_decode.cu"}
+
+
+def kernel_source_sha(kernel: str) -> str:
+    """Hash of the sources a kernel is built from (its .cu file, the shared
+    device header and the ABI header): a recorded ncu traffic figure is only
+    reported while this matches."""
     h = hashlib.sha256()
-    for f in sorted(CSRC.glob("*")):
-        if f.suffix in (".cu", ".cuh", ".h"):
-            h.update(f.read_bytes())
-    h.update((ROOT / "include" / "splitzip.h").read_bytes())
+    for f in (CSRC / KERNEL_SOURCES[kernel], CSRC / "sz_device.cuh", CSRC / "sz_internal.h",
+              ROOT / "include" / "splitzip.h"):
+        h.update(f.read_bytes())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, sha: str):
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` at the full benchmark workload, from
+    the committed ncu summary, or None if the kernel changed since."""
     if not TRAFFIC_FILE.exists():
         return None
-    d = json.loads(TRAFFIC_FILE.read_text())
-    rec = d.get(kernel)
-    if not rec or rec.get("source_sha") != sha:
+    rec = json.loads(TRAFFIC_FILE.read_text()).get(kernel)
+    if not rec or rec.get("source_sha") != kernel_source_sha(kernel):
         return None
     return rec.get("bytes_per_launch_full_workload")
 
@@ -252,8 +259,10 @@ def run_ours(args, world, rank, local):
     comp_total = sum(m.comp_bytes for m in metas)
 
     K = args.steps
+    # kernel events (set through the library's timing hook around each call's
+    # streaming kernel) and call events (around each whole API call)
     ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(K)] for k in
-          ("cb", "ca", "eb", "ea", "db", "da")}
+          ("cb", "ca", "eb", "ea", "db", "da", "o0", "o1", "o2", "o3")}
     for lst in ev.values():  # create the underlying CUDA events
         for e in lst:
             e.record(stream)
@@ -272,12 +281,16 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     step_start.record(stream)
     for k in range(K):
+        ev["o0"][k].record(stream)
         sz.sz_set_timing_events(ev["cb"][k], ev["ca"][k])
         sz.sz_calibrate_many(batch.table, workspace=ws_cal)
+        ev["o1"][k].record(stream)
         sz.sz_set_timing_events(ev["eb"][k], ev["ea"][k])
         sz.sz_encode_many(batch.table, workspace=ws_enc)
+        ev["o2"][k].record(stream)
         sz.sz_set_timing_events(ev["db"][k], ev["da"][k])
         sz.sz_decode_many(batch.table, workspace=ws_dec)
+        ev["o3"][k].record(stream)
     sz.sz_set_timing_events(None, None)
     step_end.record(stream)
     torch.cuda.synchronize()
@@ -288,6 +301,8 @@ def run_ours(args, world, rank, local):
     t_cal = [ev["cb"][k].elapsed_time(ev["ca"][k]) for k in range(K)]
     t_enc = [ev["eb"][k].elapsed_time(ev["ea"][k]) for k in range(K)]
     t_dec = [ev["db"][k].elapsed_time(ev["da"][k]) for k in range(K)]
+    t_ops = {name: float(np.mean([ev[a][k].elapsed_time(ev[b][k]) for k in range(K)]))
+             for name, a, b in (("calibrate", "o0", "o1"), ("encode", "o1", "o2"), ("decode", "o2", "o3"))}
     for w in (ws_cal, ws_enc, ws_dec):
         assert sz.sz_workspace_flags(w.buf) == 0
 
@@ -340,15 +355,22 @@ def run_ours(args, world, rank, local):
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"]
     ms = {"calibrate": float(np.mean(t_cal)), "encode": float(np.mean(t_enc)), "decode": float(np.mean(t_dec))}
-    alg = {"calibrate": raw_bytes, "encode": raw_bytes + comp_total, "decode": comp_total + raw_bytes}
+    # algorithmic bytes of each streaming kernel: cal_hist reads x; enc_main
+    # reads x and writes the pk and sm sections (the escape streams are
+    # written by enc_place); dec_main reads the payload and writes x
+    dense_bytes = sum(m.off_cid for m in metas)
+    alg = {"calibrate": raw_bytes, "encode": raw_bytes + dense_bytes, "decode": comp_total + raw_bytes}
+    alg_ops = {"calibrate": raw_bytes, "encode": raw_bytes + comp_total, "decode": comp_total + raw_bytes}
     kname = {"calibrate": "cal_hist", "encode": "enc_main", "decode": "dec_main"}
-    sha = kernel_sources_sha()
     kernels = {}
     for k in ms:
         achieved = alg[k] / (ms[k] * 1e-3) / 1e9
         kernels[k] = {"kernel": kname[k], "ms": ms[k], "raw_gbs": raw_bytes / (ms[k] * 1e-3) / 1e9,
                       "achieved_gbs": achieved, "frac": achieved / peak, "alg_bytes": alg[k],
-                      "traffic": recorded_traffic(kname[k], sha)}
+                      "traffic": recorded_traffic(kname[k])}
+    ops = {k: {"ms": t_ops[k], "raw_gbs": raw_bytes / (t_ops[k] * 1e-3) / 1e9,
+               "achieved_gbs": alg_ops[k] / (t_ops[k] * 1e-3) / 1e9,
+               "frac": alg_ops[k] / (t_ops[k] * 1e-3) / 1e9 / peak, "alg_bytes": alg_ops[k]} for k in t_ops}
     dom = max(ms, key=ms.get)
     value = world * raw_bytes / (ms_step * 1e-3) / 1e9
     cpu = None
@@ -363,17 +385,17 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"{world} independent shards" if world > 1 else "single GPU"},
         "ratio": comp_total / raw_bytes, "compression": raw_bytes / comp_total,
         "n_esc": int(sum(m.n_esc for m in metas)),
-        "encode_gbs": kernels["encode"]["raw_gbs"], "decode_gbs": kernels["decode"]["raw_gbs"],
-        "calibrate_gbs": kernels["calibrate"]["raw_gbs"],
+        "encode_gbs": ops["encode"]["raw_gbs"], "decode_gbs": ops["decode"]["raw_gbs"],
+        "calibrate_gbs": ops["calibrate"]["raw_gbs"],
         "roofline": {"bound": "hbm", "kernel": kernels[dom]["kernel"], "achieved": kernels[dom]["achieved_gbs"],
                      "peak": peak, "unit": "GB/s", "frac": kernels[dom]["frac"],
                      "traffic": kernels[dom]["traffic"], "peak_source": peaks["source"]},
         "kernels": kernels,
+        "ops": ops,
         "clocks": clk,
         "gpu_launches": 7 * K,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "source_sha": sha,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
