@@ -5,31 +5,53 @@
 // Two launches per call (after a 256-byte header memset):
 //   cal_prepare  zeroes the per-item histograms and completion counters,
 //                validates the item table, writes the codebook of n == 0 items;
-//   cal_hist     streams every tile once into privatised shared-memory
-//                counters, flushes them with one global atomic per non-zero
-//                bin, and the CTA that flushes an item's last tiles ranks the
-//                256 bins and writes the codebook (ties by ascending exponent
-//                value).
-//
-// The histogram is bound by instruction issue, not by the atomics' conflicts,
-// so the counters are laid out to make an element as cheap as possible: one
-// 32-bit counter per (bin, thread), cnt[bin][tid] with 64 threads, so the
-// byte offset of an element's counter is its exponent byte times 256 -- a
-// shift and a mask of the BF16 pattern -- and the 32 lanes of a warp always
-// hit 32 different banks whatever their bins.  The adds are shared-memory
-// reductions without a return value.  Each thread keeps the next tile's
-// 16 x 16 bytes in flight (register double buffer) while it counts the
-// current one.
+//   cal_hist     persistent CTAs own contiguous runs of tiles.  A producer
+//                warp streams them (16 KiB tiles) through a 4-stage
+//                shared-memory ring with TMA bulk copies, so the counting
+//                warps never wait on global loads.  The 8 counting warps share
+//                one 32-bit counter per (bin, lane), cnt[bin][lane]: the byte
+//                offset of an element's counter is its exponent byte times
+//                128 -- a shift and a mask of the BF16 pattern -- and the 32
+//                lanes of a warp always hit 32 different banks whatever their
+//                bins.  The adds are shared-memory atomics without a return
+//                value; keying the columns by lane rather than by thread keeps
+//                the counters at 32 KiB, so 16 counting warps fit on an SM.  Counters are flushed with one global atomic
+//                per non-zero bin when the tensor changes; the CTA that
+//                flushes a tensor's last tiles ranks its 256 bins and writes
+//                the codebook (ties by ascending exponent value).
 #include "sz_internal.h"
 
 namespace sz {
 namespace {
 
-constexpr int kHistThreads = 64;
-constexpr int kHistCtasPerSm = 3;
-constexpr int kVecPerThread = kTile / 8 / kHistThreads;  // 16 x 16-byte vectors per tile
-constexpr size_t kHistSmem = size_t(256) * kHistThreads * 4;  // 64 KiB
+constexpr int kCountWarps = 8;
+constexpr int kCountThreads = kCountWarps * 32;
+constexpr int kCalThreads = kCountThreads + 32;  // + producer warp
+constexpr int kCalStages = 4;
+constexpr int kCalCtasPerSm = 2;
 constexpr uint32_t kItemInvalid = 0x80000000u;
+constexpr uint32_t kStageEnd = 1u, kStageInvalid = 2u;
+constexpr unsigned FULL = 0xFFFFFFFFu;
+
+struct __align__(128) CalStageBuf {
+  uint16_t x[kTile];
+};
+struct CalHdr {
+  uint32_t item, n, flags, pad;
+};
+struct CalShared {
+  uint32_t cnt[256 * 32];  // [bin][lane]
+  CalStageBuf st[kCalStages];
+  CalHdr hdr[kCalStages];
+  uint64_t full[kCalStages];
+  uint64_t empty[kCalStages];
+  uint32_t h[256];
+  unsigned long long s_top;
+  uint32_t s_nz;
+  int s_last;
+  uint8_t dl[16];
+};
+
 
 
 __device__ void write_empty_codebook(sz_codebook* cb) {
@@ -66,175 +88,188 @@ __global__ void cal_prepare(const __grid_constant__ Items items, CalWs ws) {
   }
 }
 
-// Ranks the 256 bins of item `ii` (count desc, value asc) and writes its
-// codebook.  Called by all kHistThreads threads of the CTA.
-__device__ void select_top16(const sz_item& it, const uint32_t* __restrict__ ghist, uint32_t* h,
-                             uint8_t* dl, unsigned long long* s_top, uint32_t* s_nz) {
-  const int tid = threadIdx.x;
+// Ranks the 256 bins of `it` (count desc, value asc) and writes its codebook.
+// Run by the kCountThreads counting threads (named barrier 1).
+__device__ void select_top16(const sz_item& it, const uint32_t* __restrict__ ghist, CalShared& sh) {
+  const uint32_t tid = threadIdx.x;
   __threadfence();
-  for (int b = tid; b < 256; b += kHistThreads) h[b] = __ldcg(ghist + b);
-  if (tid < 16) dl[tid] = 0;
+  for (uint32_t b = tid; b < 256; b += kCountThreads) sh.h[b] = __ldcg(ghist + b);
+  if (tid < 16) sh.dl[tid] = 0;
   if (tid == 0) {
-    *s_top = 0;
-    *s_nz = 0;
+    sh.s_top = 0;
+    sh.s_nz = 0;
   }
-  __syncthreads();
+  named_bar_sync(1, kCountThreads);
   sz_codebook* cb = it.codebook;
   unsigned long long top = 0;
   uint32_t nz = 0;
-  for (int b = tid; b < 256; b += kHistThreads) {
-    const uint32_t c = h[b];
+  for (uint32_t b = tid; b < 256; b += kCountThreads) {
+    const uint32_t c = sh.h[b];
     uint32_t rank = 0;
 #pragma unroll 8
-    for (int j = 0; j < 256; ++j) {
-      const uint32_t cj = h[j];
+    for (uint32_t j = 0; j < 256; ++j) {
+      const uint32_t cj = sh.h[j];
       rank += (cj > c) | ((cj == c) & (j < b));
     }
     uint32_t code = kEscape;
     if (c > 0 && rank < 16) {
       code = rank;
-      dl[rank] = uint8_t(b);
+      sh.dl[rank] = uint8_t(b);
       top += c;
     }
     nz += (c > 0);
     cb->enc_lut[b] = uint8_t(code);
   }
-  atomicAdd(s_top, top);
-  atomicAdd(s_nz, nz);
-  __syncthreads();
-  if (tid < 16) cb->dec_lut[tid] = dl[tid];
+  atomicAdd(&sh.s_top, top);
+  atomicAdd(&sh.s_nz, nz);
+  named_bar_sync(1, kCountThreads);
+  if (tid < 16) cb->dec_lut[tid] = sh.dl[tid];
   if (tid == 0) {
     const uint64_t n = it.n;
-    cb->n_top = *s_nz < 16 ? *s_nz : 16;
+    cb->n_top = sh.s_nz < 16 ? sh.s_nz : 16;
     cb->reserved0 = 0;
-    cb->top_count = *s_top;
+    cb->top_count = sh.s_top;
     cb->n = n;
-    cb->coverage = n ? double(*s_top) / double(n) : 1.0;
+    cb->coverage = n ? double(sh.s_top) / double(n) : 1.0;
   }
+  named_bar_sync(1, kCountThreads);  // h, dl and the sums are reused by the next select
 }
 
-__global__ void __launch_bounds__(kHistThreads, kHistCtasPerSm)
-    cal_hist(const __grid_constant__ Items items, CalWs ws) {
-  extern __shared__ __align__(16) uint32_t cnt[];  // [256 bins][kHistThreads]
-  __shared__ uint32_t h[256];
-  __shared__ uint8_t dl[16];
-  __shared__ unsigned long long s_top;
-  __shared__ uint32_t s_nz;
-  __shared__ int s_last;
-
-  const int tid = threadIdx.x;
+__global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __grid_constant__ Items items, CalWs ws) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  CalShared& sh = *reinterpret_cast<CalShared*>(smem_raw);
+  const uint32_t tid = threadIdx.x;
+  const uint32_t warp = tid >> 5, lane = tid & 31u;
   // an inconsistent item table (flagged by cal_prepare) is never walked
   if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
-  for (int b = 0; b < 256; ++b) cnt[b * kHistThreads + tid] = 0;
 
   const uint64_t T = items.total_tiles;
   const uint64_t per = (T + gridDim.x - 1) / gridDim.x;
   const uint64_t t0 = uint64_t(blockIdx.x) * per;
   const uint64_t t1 = (t0 + per < T) ? t0 + per : T;
-  __syncthreads();
   if (t0 >= t1) return;
 
-  uint32_t cur = find_item(items, t0);
-  uint64_t cur_begin = item_at(items, cur).tile_begin;
-  uint64_t cur_tiles = tiles_of(item_at(items, cur).n);
-  uint32_t run = 0;  // tiles counted since the last flush
+  for (uint32_t w = tid; w < 256 * 32; w += kCalThreads) sh.cnt[w] = 0;
+  if (tid == 0) {
+    for (int s = 0; s < kCalStages; ++s) {
+      mbar_init(&sh.full[s], 1 + 32);
+      mbar_init(&sh.empty[s], kCountWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
 
-  // this thread's counter column, as a byte address: counter of bin b is at
-  // col + 256 * b
-  char* const col = reinterpret_cast<char*>(cnt + tid);
-  auto count_lo = [&](uint32_t w) {  // element in bits 0..15
-    atomicAdd(reinterpret_cast<uint32_t*>(col + ((w << 1) & 0xFF00u)), 1u);
-  };
-  auto count_hi = [&](uint32_t w) {  // element in bits 16..31
-    atomicAdd(reinterpret_cast<uint32_t*>(col + ((w >> 15) & 0xFF00u)), 1u);
-  };
-  auto count_vec = [&](const uint4& v) {
-    count_lo(v.x);
-    count_hi(v.x);
-    count_lo(v.y);
-    count_hi(v.y);
-    count_lo(v.z);
-    count_hi(v.z);
-    count_lo(v.w);
-    count_hi(v.w);
-  };
-
-  auto flush = [&]() {
-    __syncthreads();
-    {
-      uint32_t* gh = ws.hist + uint64_t(cur) * 256;
-#pragma unroll
-      for (int q = 0; q < 256 / kHistThreads; ++q) {
-        const int b = tid * (256 / kHistThreads) + q;
-        uint32_t* row = cnt + b * kHistThreads;
-        uint32_t sum = 0;
-#pragma unroll 8
-        for (int j = 0; j < kHistThreads; ++j) {
-          const int c = (j + tid) & (kHistThreads - 1);  // lanes read 32 different banks
-          sum += row[c];
-          row[c] = 0;
-        }
-        if (sum) atomicAdd(gh + b, sum);
+  if (warp == kCountWarps) {
+    // ---------------------------------------------------------------- producer warp
+    uint32_t cur = 0;
+    uint64_t cur_begin = 0, cur_end = 0;
+    uint32_t it = 0;
+    for (uint64_t t = t0;; ++t, ++it) {
+      const int s = int(it % kCalStages);
+      if (it >= uint32_t(kCalStages) && !__all_sync(FULL, mbar_wait(&sh.empty[s], ((it / kCalStages) - 1) & 1))) {
+        if (lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+        return;
       }
+      CalHdr& hd = sh.hdr[s];
+      if (t >= t1) {
+        if (lane == 0) {
+          hd.flags = kStageEnd;
+          mbar_arrive(&sh.full[s]);
+        }
+        cp_async_mbar_arrive_noinc(&sh.full[s]);
+        return;
+      }
+      if (t >= cur_end) {
+        cur = find_item(items, t);
+        cur_begin = item_at(items, cur).tile_begin;
+        cur_end = cur_begin + tiles_of(item_at(items, cur).n);
+      }
+      const sz_item& itm = item_at(items, cur);
+      const uint64_t g = (t - cur_begin) * kTile;
+      const bool invalid = (ws.done[cur] & kItemInvalid) != 0 || t - cur_begin >= tiles_of(itm.n);
+      const uint32_t nh = (invalid || g >= itm.n) ? 0u : ((itm.n - g < kTile) ? uint32_t(itm.n - g) : kTile);
+      const uint32_t bulk = (nh * 2u) & ~15u;
+      const uint32_t tail = nh * 2u - bulk;
+      if (lane == 0) {
+        hd.item = cur;
+        hd.n = nh;
+        hd.flags = invalid ? kStageInvalid : 0u;
+        mbar_arrive_expect_tx(&sh.full[s], bulk);
+        if (bulk) bulk_g2s(sh.st[s].x, itm.x + g, bulk, &sh.full[s]);
+      } else if (lane == 1 && tail) {
+        cp_async16_zfill(reinterpret_cast<uint8_t*>(sh.st[s].x) + bulk,
+                         reinterpret_cast<const uint8_t*>(itm.x + g) + bulk, tail);
+      }
+      cp_async_mbar_arrive_noinc(&sh.full[s]);
+    }
+  }
+
+  // ------------------------------------------------------------------ counting warps
+  // this lane's counter column, as a byte address: bin b at col + 128 * b
+  char* const col = reinterpret_cast<char*>(sh.cnt + lane);
+  uint32_t cur = 0xFFFFFFFFu;
+  uint32_t run = 0;  // tiles of `cur` counted since the last flush
+  auto flush = [&]() {
+    named_bar_sync(1, kCountThreads);
+    uint32_t* gh = ws.hist + uint64_t(cur) * 256;
+    for (uint32_t b = tid; b < 256; b += kCountThreads) {
+      uint32_t* row = sh.cnt + b * 32;
+      uint32_t sum = 0;
+#pragma unroll 8
+      for (uint32_t j = 0; j < 32; ++j) {
+        const uint32_t c = (j + lane) & 31u;  // lanes read 32 different banks
+        sum += row[c];
+        row[c] = 0;
+      }
+      if (sum) atomicAdd(gh + b, sum);
     }
     __threadfence();
-    __syncthreads();
+    named_bar_sync(1, kCountThreads);
     if (tid == 0) {
       const uint32_t old = atomicAdd(ws.done + cur, run);
-      s_last = ((old & kItemInvalid) == 0) && (uint64_t(old) + run == cur_tiles);
+      sh.s_last = ((old & kItemInvalid) == 0) && (uint64_t(old) + run == tiles_of(item_at(items, cur).n));
     }
-    __syncthreads();
-    if (s_last) select_top16(item_at(items, cur), ws.hist + uint64_t(cur) * 256, h, dl, &s_top, &s_nz);
+    named_bar_sync(1, kCountThreads);
+    if (sh.s_last) select_top16(item_at(items, cur), ws.hist + uint64_t(cur) * 256, sh);
     run = 0;
   };
-
-  // r holds the current full tile once `have` is set: the next full tile of
-  // the same item is loaded before the current one is counted.
-  uint4 r[kVecPerThread];
-  bool have = false;
-  for (uint64_t t = t0; t < t1; ++t) {
-    if (t >= cur_begin + cur_tiles) {
+  for (uint32_t it = 0;; ++it) {
+    const int s = int(it % kCalStages);
+    const bool ok = mbar_wait(&sh.full[s], (it / kCalStages) & 1);
+    const CalHdr hd = sh.hdr[s];  // read before the vote: the stage may be released right after
+    if (named_bar_red_or(1, kCountThreads, !ok)) {
+      if (tid == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+      return;
+    }
+    if (hd.flags & kStageEnd) break;
+    if (hd.item != cur) {
       if (run) flush();
-      cur = find_item(items, t);
-      cur_begin = item_at(items, cur).tile_begin;
-      cur_tiles = tiles_of(item_at(items, cur).n);
-      have = false;
+      cur = hd.item;
     }
-    const sz_item& it = item_at(items, cur);
-    if ((ws.done[cur] & kItemInvalid) || t - cur_begin >= cur_tiles) {  // invalid item: nothing is read
-      have = false;
-      continue;
+    if (!(hd.flags & kStageInvalid)) {
+      const uint4* xs = reinterpret_cast<const uint4*>(sh.st[s].x);
+      if (hd.n == kTile) {
+        uint4 v[kTile / 8 / kCountThreads];
+#pragma unroll
+        for (int k = 0; k < kTile / 8 / kCountThreads; ++k) v[k] = xs[tid + k * kCountThreads];
+#pragma unroll
+        for (int k = 0; k < kTile / 8 / kCountThreads; ++k) {
+          const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            atomicAdd(reinterpret_cast<uint32_t*>(col + (w[q] & 0x7F80u)), 1u);
+            atomicAdd(reinterpret_cast<uint32_t*>(col + ((w[q] >> 16) & 0x7F80u)), 1u);
+          }
+        }
+      } else {
+        const uint16_t* xe = sh.st[s].x;
+        for (uint32_t e = tid; e < hd.n; e += kCountThreads)
+          atomicAdd(reinterpret_cast<uint32_t*>(col + (uint32_t(xe[e]) & 0x7F80u)), 1u);
+      }
+      ++run;
     }
-    const uint64_t base = (t - cur_begin) * kTile;
-    const uint64_t left = it.n - base;
-    const uint32_t nt = left < kTile ? uint32_t(left) : kTile;
-    const uint4* src = reinterpret_cast<const uint4*>(it.x + base);
-    if (nt == kTile) {
-      if (!have) {
-#pragma unroll
-        for (int k = 0; k < kVecPerThread; ++k) r[k] = __ldg(src + tid + k * kHistThreads);
-      }
-      const bool next_full = (t + 1 < t1) && (t + 1 < cur_begin + cur_tiles) && (left >= 2 * uint64_t(kTile));
-      uint4 q[kVecPerThread];
-      if (next_full) {
-#pragma unroll
-        for (int k = 0; k < kVecPerThread; ++k) q[k] = __ldg(src + kTile / 8 + tid + k * kHistThreads);
-      }
-#pragma unroll
-      for (int k = 0; k < kVecPerThread; ++k) count_vec(r[k]);
-      if (next_full) {
-#pragma unroll
-        for (int k = 0; k < kVecPerThread; ++k) r[k] = q[k];
-      }
-      have = next_full;
-    } else {
-      have = false;
-      const uint32_t nvec = nt >> 3;
-      for (uint32_t v = tid; v < nvec; v += kHistThreads) count_vec(__ldg(src + v));
-      const uint32_t rem = nt & 7u;
-      if (uint32_t(tid) < rem) count_lo(it.x[base + (nvec << 3) + tid]);
-    }
-    ++run;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty[s]);
   }
   if (run) flush();
 }
@@ -254,15 +289,16 @@ cudaError_t launch_calibrate(const Items& items, void* ws_base, cudaStream_t str
   }
   if (items.total_tiles == 0) return cudaSuccess;
   static thread_local int configured_device = -1;
+  const size_t smem = sizeof(CalShared);
   if (configured_device != dev.device) {
-    err = cudaFuncSetAttribute(cal_hist, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kHistSmem));
+    err = cudaFuncSetAttribute(cal_hist, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (err != cudaSuccess) return err;
     configured_device = dev.device;
   }
-  const uint64_t cap = uint64_t(dev.num_sms) * kHistCtasPerSm;
+  const uint64_t cap = uint64_t(dev.num_sms) * kCalCtasPerSm;
   const unsigned grid = unsigned(items.total_tiles < cap ? items.total_tiles : cap);
   if (g_timing.before) cudaEventRecord(g_timing.before, stream);
-  cal_hist<<<grid, kHistThreads, kHistSmem, stream>>>(items, ws);
+  cal_hist<<<grid, kCalThreads, smem, stream>>>(items, ws);
   err = cudaGetLastError();
   if (g_timing.after) cudaEventRecord(g_timing.after, stream);
   return err;
