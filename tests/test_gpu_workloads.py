@@ -1,0 +1,138 @@
+"""GPU parity at the full sizes of the five benchmark workloads.
+
+Every tensor is compared with the CPU oracle byte for byte (codebook, meta,
+payload) and its decode bit for bit, except the largest size-sweep points,
+where the oracle checks the exact codebook and escape count and a sample of
+1024-element chunks (pk, sm and escape entries), and the round trip is
+checked on the GPU.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import weight_compression_codec_gb300 as sz
+from weight_compression_codec_gb300 import inputs
+
+from gpu_util import DEV, check_codebook, roundtrip_single, to_dev, to_np_u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    sz.build()
+    torch.cuda.set_device(DEV)
+
+
+def _many_exact(arrays: list[np.ndarray]) -> list:
+    """Round trip of a tensor list through the *_many calls, every tensor exact."""
+    b = sz.Batch([to_dev(a) for a in arrays])
+    ws = sz.Workspace(DEV)
+    sz.sz_calibrate_many(b.table, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    sz.sz_encode_many(b.table, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    sz.sz_decode_many(b.table, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    torch.cuda.synchronize()
+    cbs = b.codebooks.cpu().numpy()
+    metas = b.metas.cpu().numpy()
+    out = []
+    for i, x in enumerate(arrays):
+        ocb = oracle.calibrate(x)
+        check_codebook(sz.codebook_from_bytes(cbs[i]), ocb, x.size)
+        opay, om = oracle.encode(x, ocb)
+        m = sz.meta_from_bytes(metas[i])
+        assert m.status == 0 and m.as_tuple() == om.as_tuple(), (i, m, om)
+        assert np.array_equal(b.payload_view(i, m.comp_bytes).cpu().numpy(), opay), f"payload of tensor {i}"
+        assert np.array_equal(to_np_u16(b.out_view(i)), x), f"decode of tensor {i}"
+        out.append((ocb, om))
+    return out
+
+
+def test_c1_weight_like_1m():
+    r = roundtrip_single(inputs.gaussian(1_048_576, 0.02))
+    assert abs(r["meta"].comp_bytes / (2 * 1_048_576) - 0.750) < 0.002
+
+
+def test_c2_kv_cache_full():
+    arrays = inputs.kv_cache()  # [32, 2, 4096, 8, 128], one codebook per (layer, K/V)
+    assert len(arrays) == 64 and all(a.size == 4096 * 8 * 128 for a in arrays)
+    res = _many_exact(arrays)
+    ratio = sum(om.comp_bytes for _, om in res) / sum(2 * a.size for a in arrays)
+    assert 0.75 < ratio < 0.80
+
+
+def test_c3_weight_pairs_full():
+    shapes = inputs.weight_shapes()
+    for start in range(0, 16, 4):  # 4 tensors (~1 GiB of BF16) per batch keeps host memory modest
+        arrays = [inputs.weight_tensor(i) for i in range(start, start + 4)]
+        res = _many_exact(arrays)
+        for (ocb, _), i in zip(res, range(start, start + 4)):
+            assert arrays[i - start].size == shapes[i][0] * shapes[i][1]
+            if i == 15:
+                assert ocb.coverage < 0.99  # the broad-exponent tensor still round-trips exactly
+
+
+def test_c4_edge_case_full():
+    r = roundtrip_single(inputs.edge_case(100_000_003))
+    m = r["meta"]
+    assert r["codebook"].coverage < 0.5 and m.comp_bytes > 2 * m.n  # escape-heavy: the payload expands
+
+
+def test_c5_paged_kv_8192_blocks():
+    arrays = inputs.paged_kv(8192)
+    _many_exact(arrays)
+
+
+def _sampled_check(x: np.ndarray, payload: torch.Tensor, m, cb_dev: torch.Tensor, samples: int = 64) -> None:
+    """Exact codebook and escape count from the oracle over the whole tensor;
+    pk, sm and escape entries of sampled 1024-element chunks against the
+    oracle run on each chunk with the same codebook."""
+    ocb = oracle.calibrate(x)
+    check_codebook(sz.read_codebook(cb_dev), ocb, x.size)
+    assert m.n_esc == oracle.count_escapes(x, ocb)
+    lay = oracle.layout(x.size, m.n_esc)
+    assert m.as_tuple() == lay.as_tuple()
+    cid = payload[m.off_cid:m.off_cid + 4 * m.n_esc].view(torch.int32)
+    rng = np.random.default_rng(x.size)
+    chunks = (x.size + 1023) // 1024
+    for c in sorted(set(rng.integers(0, chunks, size=samples).tolist()) | {0, chunks - 1}):
+        lo, hi = c * 1024, min(x.size, c * 1024 + 1024)
+        opay, om = oracle.encode(x[lo:hi], ocb)
+        n = hi - lo
+        pk = payload[m.off_pk + lo // 2:m.off_pk + lo // 2 + (n + 1) // 2].cpu().numpy()
+        assert np.array_equal(pk, opay[:(n + 1) // 2]), f"pk of chunk {c}"
+        smb = payload[m.off_sm + lo:m.off_sm + hi].cpu().numpy()
+        assert np.array_equal(smb, opay[om.off_sm:om.off_sm + n]), f"sm of chunk {c}"
+        k0 = int(torch.searchsorted(cid, torch.tensor([c], dtype=torch.int32, device=cid.device)).item())
+        e = om.n_esc
+        got_cid = cid[k0:k0 + e].cpu().numpy()
+        got_lp = payload[m.off_lpos + 2 * k0:m.off_lpos + 2 * (k0 + e)].cpu().numpy()
+        got_ev = payload[m.off_ev + k0:m.off_ev + k0 + e].cpu().numpy()
+        assert np.all(got_cid == c)
+        assert k0 + e == m.n_esc or int(cid[k0 + e].item()) > c, f"extra escapes in chunk {c}"
+        assert np.array_equal(got_lp, opay[om.off_lpos:om.off_lpos + 2 * e]), f"local_pos of chunk {c}"
+        assert np.array_equal(got_ev, opay[om.off_ev:om.off_ev + e]), f"esc_val of chunk {c}"
+
+
+@pytest.mark.parametrize("n", inputs.sweep_sizes())
+def test_c5_size_sweep(n):
+    x = inputs.sweep_tensor(n)
+    if n <= (1 << 26):
+        roundtrip_single(x)
+        return
+    xd = to_dev(x)
+    cb = sz.sz_calibrate(xd)
+    payload, meta = sz.sz_encode(xd, cb)
+    out = torch.empty_like(xd)
+    sz.sz_decode(payload, meta, cb, n, out=out)
+    m = sz.read_meta(meta)
+    assert m.status == 0
+    assert torch.equal(out, xd), "GPU round trip"
+    del out
+    _sampled_check(x, payload, m, cb)
