@@ -39,7 +39,7 @@ ROOT = Path(__file__).resolve().parent
 sys.path.insert(0, str(ROOT))
 
 METRIC = "encode/decode raw-BF16 GB/s on 1 GB300 and % of HBM roofline; compression ratio"
-WORKLOAD = "kv_cache_bf16_32x2x4096x8x128_64_codebooks"
+L2_BYTES = 126 << 20
 UNIT = "GB/s"
 CSRC = ROOT / "weight_compression_codec_gb300" / "csrc"
 TRAFFIC_FILE = ROOT / "profiles" / "ncu_traffic.json"
@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="kv_cache",
+                    help="kv_cache (the headline line), weights, edge_case, paged_kv, or sweep_<bytes>")
     ap.add_argument("--layers", type=int, default=32, help="KV-cache layers (64 tensors at 32)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -66,11 +68,70 @@ def dist_env():
     return world, rank, local
 
 
-def workload_arrays(layers: int, rank: int) -> list[np.ndarray]:
+# Each workload: (name in the JSON line, tensor count, generator of tensor i on
+# a rank).  Ranks hold disjoint data (weak scaling): seeds are offset by rank.
+def _kv(args, rank, i):
     from weight_compression_codec_gb300 import inputs
 
-    # each rank holds its own cache (weak scaling): layers are offset by rank
-    return [inputs.kv_cache_tensor(rank * layers + l, kv) for l in range(layers) for kv in range(2)]
+    return inputs.kv_cache_tensor(rank * args.layers + i // 2, i % 2)
+
+
+def _weight(args, rank, i):
+    from weight_compression_codec_gb300 import inputs
+
+    return inputs.weight_tensor(i)
+
+
+def _edge(args, rank, i):
+    from weight_compression_codec_gb300 import inputs
+
+    return inputs.edge_case(100_000_003, seed=rank)
+
+
+def _paged(args, rank, i):
+    from weight_compression_codec_gb300 import inputs
+
+    return inputs.paged_kv_block(rank * 8192 + i)
+
+
+def _sweep(n: int):
+    def gen(args, rank, i):
+        from weight_compression_codec_gb300 import inputs
+
+        return inputs.sweep_tensor(n)
+    return gen
+
+
+WORKLOADS = {
+    "kv_cache": ("kv_cache_bf16_32x2x4096x8x128_64_codebooks", lambda a: 2 * a.layers, _kv),
+    "weights": ("weights_bf16_8x(4096x14336,14336x4096)_16_codebooks", lambda a: 16, _weight),
+    "edge_case": ("edge_case_bf16_100000003_escape_heavy", lambda a: 1, _edge),
+    "paged_kv": ("paged_kv_bf16_8192x(16x8x128)_8192_codebooks", lambda a: 8192, _paged),
+}
+for _b in (256 << 20, 1 << 30, 4 << 30):
+    WORKLOADS[f"sweep_{_b}"] = (f"sweep_bf16_N(0,1)_{_b // 2}_elements", lambda a: 1, _sweep(_b // 2))
+
+
+def workload_name(args) -> str:
+    return WORKLOADS[args.workload][0]
+
+
+def workload_arrays(args, rank: int) -> list[np.ndarray]:
+    _, count, gen = WORKLOADS[args.workload]
+    return [gen(args, rank, i) for i in range(count(args))]
+
+
+def workload_sample(args, elements: int = 1 << 24) -> list[np.ndarray]:
+    """The workload's first tensors up to ``elements`` in total (the last one cut)."""
+    _, count, gen = WORKLOADS[args.workload]
+    out, have = [], 0
+    for i in range(count(args)):
+        x = gen(args, 0, i)[:elements - have]
+        out.append(x)
+        have += x.size
+        if have >= elements:
+            break
+    return out
 
 
 # ---------------------------------------------------------------------------- clocks
@@ -151,14 +212,14 @@ def cpu_oracle_sample(arrays: list[np.ndarray], budget_s: float) -> dict:
             break
     dt = time.perf_counter() - t0
     return {"value": done_bytes / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{k} KV-cache tensors of {arrays[0].size} elements (calibrate+encode+decode, "
+            "sample": f"{k} tensors of the workload, {done_bytes / 2**20:.0f} MiB (calibrate+encode+decode, "
                       f"single-threaded C), {dt:.1f} s"}
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return 0
-    arrays = workload_arrays(2, 0)  # 4 of the workload's tensors per step
+    arrays = workload_sample(args)  # the first 16M elements of the workload per step
     for _ in range(args.warmup):
         cpu_oracle_sample(arrays[:1], 0.0)
     times = []
@@ -174,11 +235,11 @@ def run_reference(args, world, rank):
     step = float(np.mean(times))
     raw = sum(2 * a.size for a in arrays)
     value = raw / step / 1e9
-    sample = f"{len(arrays)} of the 64 KV-cache tensors per step ({raw / 2**20:.0f} MiB raw)"
+    sample = f"first {len(arrays)} tensor(s) of the workload, {raw / 2**20:.0f} MiB raw per step"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "sample": sample},
+            "config": {"workload": workload_name(args), "sample": sample},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -211,13 +272,14 @@ def kernel_source_sha(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` at the full benchmark workload, from
-    the committed ncu summary, or None if the kernel changed since."""
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload`, from the committed ncu
+    summary, or None if it was recorded on another workload or the kernel
+    changed since."""
     if not TRAFFIC_FILE.exists():
         return None
     rec = json.loads(TRAFFIC_FILE.read_text()).get(kernel)
-    if not rec or rec.get("source_sha") != kernel_source_sha(kernel):
+    if not rec or rec.get("workload", "kv_cache") != workload or rec.get("source_sha") != kernel_source_sha(kernel):
         return None
     return rec.get("bytes_per_launch_full_workload")
 
@@ -235,7 +297,7 @@ def run_ours(args, world, rank, local):
         dist.init_process_group("nccl", device_id=dev)
     sz.build()
 
-    arrays = workload_arrays(args.layers, rank)
+    arrays = workload_arrays(args, rank)
     n_total = sum(a.size for a in arrays)
     raw_bytes = 2 * n_total
     xs = [torch.from_numpy(a.view(np.int16)).to(dev) for a in arrays]
@@ -424,7 +486,7 @@ def run_ours(args, world, rank, local):
         achieved = alg[k] / (ms[k] * 1e-3) / 1e9
         kernels[k] = {"kernel": kname[k], "ms": ms[k], "raw_gbs": raw_bytes / (ms[k] * 1e-3) / 1e9,
                       "achieved_gbs": achieved, "frac": achieved / peak, "alg_bytes": alg[k],
-                      "traffic": recorded_traffic(kname[k])}
+                      "traffic": recorded_traffic(kname[k], args.workload)}
     ops = {k: {"ms": t_ops[k], "raw_gbs": raw_bytes / (t_ops[k] * 1e-3) / 1e9,
                "achieved_gbs": alg_ops[k] / (t_ops[k] * 1e-3) / 1e9,
                "frac": alg_ops[k] / (t_ops[k] * 1e-3) / 1e9 / peak, "alg_bytes": alg_ops[k]} for k in t_ops}
@@ -432,13 +494,15 @@ def run_ours(args, world, rank, local):
     value = world * raw_bytes / (ms_step * 1e-3) / 1e9
     cpu = None
     if not args.no_cpu_baseline:
-        cpu = cpu_oracle_sample(arrays, args.cpu_seconds)
+        cpu = cpu_oracle_sample([a[:1 << 24] for a in arrays], args.cpu_seconds)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tensors": len(arrays), "elements": n_total, "raw_bytes": raw_bytes,
-                   "step": "calibrate+encode+decode", "l2": "inputs 512 MiB > L2, no flush",
+        "config": {"workload": workload_name(args), "tensors": len(arrays), "elements": n_total, "raw_bytes": raw_bytes,
+                   "step": "calibrate+encode+decode",
+                   "l2": f"inputs {raw_bytes / 2**20:.0f} MiB > L2, no flush" if raw_bytes > L2_BYTES
+                   else f"inputs {raw_bytes / 2**20:.0f} MiB fit in L2: L2-resident, no roofline claim",
                    "parallelism": f"{world} independent shards" if world > 1 else "single GPU"},
         "ratio": comp_total / raw_bytes, "compression": raw_bytes / comp_total,
         "n_esc": int(sum(m.n_esc for m in metas)),

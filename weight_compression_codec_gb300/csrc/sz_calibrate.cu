@@ -8,17 +8,22 @@
 //   cal_hist     persistent CTAs own contiguous runs of tiles.  A producer
 //                warp streams them (16 KiB tiles) through a 4-stage
 //                shared-memory ring with TMA bulk copies, so the counting
-//                warps never wait on global loads.  The 8 counting warps share
+//                warps never wait on global loads; it steps through the item
+//                table instead of searching it.  The 8 counting warps share
 //                one 32-bit counter per (bin, lane), cnt[bin][lane]: the byte
 //                offset of an element's counter is its exponent byte times
 //                128 -- a shift and a mask of the BF16 pattern -- and the 32
 //                lanes of a warp always hit 32 different banks whatever their
 //                bins.  The adds are shared-memory atomics without a return
 //                value; keying the columns by lane rather than by thread keeps
-//                the counters at 32 KiB, so 16 counting warps fit on an SM.  Counters are flushed with one global atomic
-//                per non-zero bin when the tensor changes; the CTA that
-//                flushes a tensor's last tiles ranks its 256 bins and writes
-//                the codebook (ties by ascending exponent value).
+//                the counters at 32 KiB, so 16 counting warps fit on an SM.
+//                When the tensor changes, thread b sums and clears bin b.  A
+//                tensor counted whole by one CTA goes straight to the CTA's
+//                select warp (two histogram buffers), which ranks it while the
+//                counting warps go on; otherwise the sums go to a global
+//                histogram (one atomic per non-zero bin) and the CTA that adds
+//                a tensor's last tiles hands it over.  The ranking (ties by
+//                ascending exponent value) compares only the non-zero bins.
 #include "sz_internal.h"
 
 namespace sz {
@@ -26,11 +31,14 @@ namespace {
 
 constexpr int kCountWarps = 8;
 constexpr int kCountThreads = kCountWarps * 32;
-constexpr int kCalThreads = kCountThreads + 32;  // + producer warp
+constexpr int kProducerWarp = kCountWarps;
+constexpr int kSelectWarp = kCountWarps + 1;
+constexpr int kCalThreads = kCountThreads + 64;  // + producer warp + select warp
 constexpr int kCalStages = 4;
 constexpr int kCalCtasPerSm = 2;
 constexpr uint32_t kItemInvalid = 0x80000000u;
 constexpr uint32_t kStageEnd = 1u, kStageInvalid = 2u;
+constexpr uint32_t kSelectEnd = 0xFFFFFFFFu;  // posted to the select warp when the CTA is done
 constexpr unsigned FULL = 0xFFFFFFFFu;
 
 struct __align__(128) CalStageBuf {
@@ -39,20 +47,25 @@ struct __align__(128) CalStageBuf {
 struct CalHdr {
   uint32_t item, n, flags, pad;
 };
+static_assert(kCountThreads == 256, "one counting thread per exponent bin");
+
 struct CalShared {
   uint32_t cnt[256 * 32];  // [bin][lane]
   CalStageBuf st[kCalStages];
   CalHdr hdr[kCalStages];
   uint64_t full[kCalStages];
   uint64_t empty[kCalStages];
-  uint32_t h[256];
-  unsigned long long s_top;
-  uint32_t s_nz;
-  int s_last;
+  // histograms handed from the counting warps to the select warp (double buffered)
+  alignas(16) uint32_t h[2][256];
+  uint32_t sel_item[2];
+  uint64_t sel_full[2];
+  uint64_t sel_empty[2];
+  // select warp scratch
+  unsigned long long key[256];  // non-zero bins in bin order: count << 8 | (255 - bin)
+  alignas(16) uint8_t lut[256];
   uint8_t dl[16];
+  int s_last;
 };
-
-
 
 __device__ void write_empty_codebook(sz_codebook* cb) {
   for (int v = 0; v < 256; ++v) cb->enc_lut[v] = kEscape;
@@ -88,51 +101,79 @@ __global__ void cal_prepare(const __grid_constant__ Items items, CalWs ws) {
   }
 }
 
-// Ranks the 256 bins of `it` (count desc, value asc) and writes its codebook.
-// Run by the kCountThreads counting threads (named barrier 1).
-__device__ void select_top16(const sz_item& it, const uint32_t* __restrict__ ghist, CalShared& sh) {
-  const uint32_t tid = threadIdx.x;
-  __threadfence();
-  for (uint32_t b = tid; b < 256; b += kCountThreads) sh.h[b] = __ldcg(ghist + b);
-  if (tid < 16) sh.dl[tid] = 0;
-  if (tid == 0) {
-    sh.s_top = 0;
-    sh.s_nz = 0;
-  }
-  named_bar_sync(1, kCountThreads);
-  sz_codebook* cb = it.codebook;
-  unsigned long long top = 0;
+// Ranks the 256 bins of histogram h (count desc, value asc) and writes the
+// codebook of `it`; run by one warp, lane l loading bins 8l .. 8l+7.  Only
+// non-zero bins take part: they are compacted in bin order as keys
+// count << 8 | (255 - bin) -- a larger key ranks first, which puts the
+// smaller bin first among equal counts -- and each counts the keys above its
+// own.
+__device__ void select_top16(const sz_item& it, const uint32_t* h, CalShared& sh, uint32_t lane) {
+  const uint4 lo = reinterpret_cast<const uint4*>(h)[2 * lane];
+  const uint4 hi = reinterpret_cast<const uint4*>(h)[2 * lane + 1];
+  const uint32_t c[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
   uint32_t nz = 0;
-  for (uint32_t b = tid; b < 256; b += kCountThreads) {
-    const uint32_t c = sh.h[b];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) nz += c[j] > 0;
+  uint32_t incl = nz;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t v = __shfl_up_sync(FULL, incl, d);
+    if (lane >= uint32_t(d)) incl += v;
+  }
+  const uint32_t total = __shfl_sync(FULL, incl, 31);
+  uint32_t pos = incl - nz;
+#pragma unroll
+  for (uint32_t j = 0; j < 8; ++j)
+    if (c[j]) sh.key[pos++] = (static_cast<unsigned long long>(c[j]) << 8) | (255u - (8u * lane + j));
+  reinterpret_cast<uint2*>(sh.lut)[lane] = make_uint2(0x10101010u, 0x10101010u);  // kEscape
+  if (lane < 16) sh.dl[lane] = 0;
+  __syncwarp();
+  for (uint32_t p = lane; p < total; p += 32) {
+    const unsigned long long key = sh.key[p];
     uint32_t rank = 0;
-#pragma unroll 8
-    for (uint32_t j = 0; j < 256; ++j) {
-      const uint32_t cj = sh.h[j];
-      rank += (cj > c) | ((cj == c) & (j < b));
+    for (uint32_t j = 0; j < total; ++j) rank += sh.key[j] > key;
+    if (rank < 16) {
+      const uint32_t bin = 255u - uint32_t(key & 0xFFu);
+      sh.lut[bin] = uint8_t(rank);
+      sh.dl[rank] = uint8_t(bin);
     }
-    uint32_t code = kEscape;
-    if (c > 0 && rank < 16) {
-      code = rank;
-      sh.dl[rank] = uint8_t(b);
-      top += c;
-    }
-    nz += (c > 0);
-    cb->enc_lut[b] = uint8_t(code);
   }
-  atomicAdd(&sh.s_top, top);
-  atomicAdd(&sh.s_nz, nz);
-  named_bar_sync(1, kCountThreads);
-  if (tid < 16) cb->dec_lut[tid] = sh.dl[tid];
-  if (tid == 0) {
+  __syncwarp();
+  sz_codebook* cb = it.codebook;
+  reinterpret_cast<uint2*>(cb->enc_lut)[lane] = reinterpret_cast<const uint2*>(sh.lut)[lane];
+  const uint32_t n_top = total < 16 ? total : 16u;
+  unsigned long long top = lane < n_top ? h[sh.dl[lane]] : 0ull;
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) top += __shfl_xor_sync(FULL, top, d);
+  if (lane < 16) cb->dec_lut[lane] = sh.dl[lane];
+  if (lane == 0) {
     const uint64_t n = it.n;
-    cb->n_top = sh.s_nz < 16 ? sh.s_nz : 16;
+    cb->n_top = n_top;
     cb->reserved0 = 0;
-    cb->top_count = sh.s_top;
+    cb->top_count = top;
     cb->n = n;
-    cb->coverage = n ? double(sh.s_top) / double(n) : 1.0;
+    cb->coverage = n ? double(top) / double(n) : 1.0;
   }
-  named_bar_sync(1, kCountThreads);  // h, dl and the sums are reused by the next select
+  __syncwarp();  // key, lut and dl are reused by the next select
+}
+
+// Index of the item holding global tile `tile` (the last item with
+// tile_begin <= tile; empty items share the next one's tile_begin), found by
+// the 32 lanes of a warp probing 32 entries per round: ceil(log32(count)) + 1
+// dependent loads.  Needs a table validated as consecutive.
+__device__ uint32_t find_item_warp(const Items& items, uint64_t tile, uint32_t lane) {
+  if (items.table == nullptr) return 0;
+  uint32_t lo = 0, hi = items.count;  // table[lo].tile_begin <= tile; the answer is in [lo, hi)
+  while (hi - lo > 32) {
+    const uint32_t step = (hi - lo + 31) / 32;
+    const uint32_t p = lo + lane * step;
+    const uint32_t m = __ballot_sync(FULL, p < hi && items.table[p].tile_begin <= tile);
+    if (m) lo += (31u - __clz(m)) * step;  // m has lane 0 unless the table is not consecutive
+    if (lo + step < hi) hi = lo + step;
+  }
+  const uint32_t p = lo + lane;
+  const uint32_t m = __ballot_sync(FULL, p < hi && items.table[p].tile_begin <= tile);
+  return m ? lo + (31u - __clz(m)) : lo;
 }
 
 __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __grid_constant__ Items items, CalWs ws) {
@@ -140,14 +181,14 @@ __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __g
   CalShared& sh = *reinterpret_cast<CalShared*>(smem_raw);
   const uint32_t tid = threadIdx.x;
   const uint32_t warp = tid >> 5, lane = tid & 31u;
-  // an inconsistent item table (flagged by cal_prepare) is never walked
-  if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
-
   const uint64_t T = items.total_tiles;
   const uint64_t per = (T + gridDim.x - 1) / gridDim.x;
   const uint64_t t0 = uint64_t(blockIdx.x) * per;
   const uint64_t t1 = (t0 + per < T) ? t0 + per : T;
   if (t0 >= t1) return;
+  // An inconsistent item table (flagged by cal_prepare) is never walked: every
+  // warp reads the flags, the producer after its first (bounds-safe) search.
+  const uint32_t hdr_flags = ws.hdr->flags;
 
   for (uint32_t w = tid; w < 256 * 32; w += kCalThreads) sh.cnt[w] = 0;
   if (tid == 0) {
@@ -155,14 +196,43 @@ __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __g
       mbar_init(&sh.full[s], 1 + 32);
       mbar_init(&sh.empty[s], kCountWarps);
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh.sel_full[b], 1);
+      mbar_init(&sh.sel_empty[b], 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kCountWarps) {
+  if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- producer warp
-    uint32_t cur = 0;
-    uint64_t cur_begin = 0, cur_end = 0;
+    // Lane l holds table entry wb + l (tile range, data pointer, invalid
+    // mark), loaded 32 at a time, so crossing into the next tensor costs
+    // shuffles rather than dependent global loads.
+    uint32_t cur = find_item_warp(items, t0, lane);
+    if (hdr_flags & SZ_FLAG_ITEMS) return;
+    uint32_t wb = 0;
+    uint64_t w_tb = 0, w_n = 0;
+    const uint16_t* w_x = nullptr;
+    uint32_t w_inv = 0;
+    auto load_window = [&](uint32_t base) {
+      wb = base;
+      const uint32_t i = base + lane;
+      if (i < items.count) {
+        const sz_item& e = item_at(items, i);
+        w_tb = e.tile_begin;
+        w_n = e.n;
+        w_x = e.x;
+        w_inv = ws.done[i] & kItemInvalid;
+      }
+    };
+    auto shfl64 = [&](uint64_t v, uint32_t src) {
+      return (uint64_t(__shfl_sync(FULL, uint32_t(v >> 32), src)) << 32) | __shfl_sync(FULL, uint32_t(v), src);
+    };
+    load_window(cur);
+    uint64_t cur_begin = 0, cur_end = 0, cur_n = 0;
+    const uint16_t* cur_x = nullptr;
+    bool cur_inv = false;
     uint32_t it = 0;
     for (uint64_t t = t0;; ++t, ++it) {
       const int s = int(it % kCalStages);
@@ -180,14 +250,28 @@ __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __g
         return;
       }
       if (t >= cur_end) {
-        cur = find_item(items, t);
-        cur_begin = item_at(items, cur).tile_begin;
-        cur_end = cur_begin + tiles_of(item_at(items, cur).n);
+        // the next tensor with a tile at t (the table is validated as consecutive)
+        if (t != t0) ++cur;
+        for (;;) {
+          if (cur >= items.count) {  // cannot happen for a consecutive table; ends the walk
+            cur_inv = true;
+            cur_end = t1;
+            break;
+          }
+          if (cur - wb >= 32) load_window(cur);
+          const uint32_t l = cur - wb;
+          cur_begin = shfl64(w_tb, l);
+          cur_n = shfl64(w_n, l);
+          cur_x = reinterpret_cast<const uint16_t*>(shfl64(reinterpret_cast<uint64_t>(w_x), l));
+          cur_inv = __shfl_sync(FULL, w_inv, l) != 0;
+          cur_end = cur_begin + tiles_of(cur_n);
+          if (t < cur_end) break;
+          ++cur;  // an empty tensor owns no tile
+        }
       }
-      const sz_item& itm = item_at(items, cur);
       const uint64_t g = (t - cur_begin) * kTile;
-      const bool invalid = (ws.done[cur] & kItemInvalid) != 0 || t - cur_begin >= tiles_of(itm.n);
-      const uint32_t nh = (invalid || g >= itm.n) ? 0u : ((itm.n - g < kTile) ? uint32_t(itm.n - g) : kTile);
+      const bool invalid = cur_inv || t < cur_begin || g >= cur_n;
+      const uint32_t nh = invalid ? 0u : ((cur_n - g < kTile) ? uint32_t(cur_n - g) : kTile);
       const uint32_t bulk = (nh * 2u) & ~15u;
       const uint32_t tail = nh * 2u - bulk;
       if (lane == 0) {
@@ -195,12 +279,30 @@ __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __g
         hd.n = nh;
         hd.flags = invalid ? kStageInvalid : 0u;
         mbar_arrive_expect_tx(&sh.full[s], bulk);
-        if (bulk) bulk_g2s(sh.st[s].x, itm.x + g, bulk, &sh.full[s]);
+        if (bulk) bulk_g2s(sh.st[s].x, cur_x + g, bulk, &sh.full[s]);
       } else if (lane == 1 && tail) {
         cp_async16_zfill(reinterpret_cast<uint8_t*>(sh.st[s].x) + bulk,
-                         reinterpret_cast<const uint8_t*>(itm.x + g) + bulk, tail);
+                         reinterpret_cast<const uint8_t*>(cur_x + g) + bulk, tail);
       }
       cp_async_mbar_arrive_noinc(&sh.full[s]);
+    }
+  }
+
+  if (hdr_flags & SZ_FLAG_ITEMS) return;
+
+  if (warp == kSelectWarp) {
+    // ---------------------------------------------------------------- select warp
+    // Ranks each histogram the counting warps hand over, while they count on.
+    for (uint32_t k = 0;; ++k) {
+      const uint32_t b = k & 1u;
+      if (!__all_sync(FULL, mbar_wait(&sh.sel_full[b], (k >> 1) & 1u))) {
+        if (lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+        return;
+      }
+      const uint32_t item = sh.sel_item[b];
+      if (item == kSelectEnd) return;
+      select_top16(item_at(items, item), sh.h[b], sh, lane);
+      if (lane == 0) mbar_arrive(&sh.sel_empty[b]);
     }
   }
 
@@ -208,38 +310,71 @@ __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __g
   // this lane's counter column, as a byte address: bin b at col + 128 * b
   char* const col = reinterpret_cast<char*>(sh.cnt + lane);
   uint32_t cur = 0xFFFFFFFFu;
-  uint32_t run = 0;  // tiles of `cur` counted since the last flush
-  auto flush = [&]() {
-    named_bar_sync(1, kCountThreads);
-    uint32_t* gh = ws.hist + uint64_t(cur) * 256;
-    for (uint32_t b = tid; b < 256; b += kCountThreads) {
-      uint32_t* row = sh.cnt + b * 32;
-      uint32_t sum = 0;
-#pragma unroll 8
-      for (uint32_t j = 0; j < 32; ++j) {
-        const uint32_t c = (j + lane) & 31u;  // lanes read 32 different banks
-        sum += row[c];
-        row[c] = 0;
-      }
-      if (sum) atomicAdd(gh + b, sum);
-    }
-    __threadfence();
-    named_bar_sync(1, kCountThreads);
+  uint32_t run = 0;    // tiles of `cur` counted since the last flush
+  uint32_t posts = 0;  // histograms handed to the select warp
+  // Waits until buffer posts & 1 is free again (its previous histogram ranked).
+  auto wait_buffer = [&]() {
+    if (posts >= 2 && !mbar_wait(&sh.sel_empty[posts & 1u], ((posts >> 1) - 1) & 1u) && lane == 0)
+      set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+  };
+  auto post = [&](uint32_t item) {  // after a named barrier over the counting threads
     if (tid == 0) {
-      const uint32_t old = atomicAdd(ws.done + cur, run);
-      sh.s_last = ((old & kItemInvalid) == 0) && (uint64_t(old) + run == tiles_of(item_at(items, cur).n));
+      sh.sel_item[posts & 1u] = item;
+      mbar_arrive(&sh.sel_full[posts & 1u]);
     }
-    named_bar_sync(1, kCountThreads);
-    if (sh.s_last) select_top16(item_at(items, cur), ws.hist + uint64_t(cur) * 256, sh);
+    ++posts;
+  };
+  auto flush = [&]() {
+    named_bar_sync(1, kCountThreads);  // every count of the tensor's tiles is in
+    // thread b sums and clears the 32 lane counters of bin b with 16-byte
+    // accesses, rotated so that the 8 threads of a quarter warp touch 8
+    // different bank groups
+    uint4* const row = reinterpret_cast<uint4*>(sh.cnt + tid * 32);
+    uint32_t sum = 0;
+#pragma unroll
+    for (uint32_t k = 0; k < 8; ++k) {
+      const uint32_t q = (k + tid) & 7u;
+      const uint4 v = row[q];
+      sum += v.x + v.y + v.z + v.w;
+      row[q] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    const uint64_t tiles = tiles_of(item_at(items, cur).n);
+    if (uint64_t(run) == tiles) {
+      // this CTA counted every tile of the tensor: hand the sums over directly
+      wait_buffer();
+      sh.h[posts & 1u][tid] = sum;
+      named_bar_sync(1, kCountThreads);  // sums written; counters clear for the next tensor
+      post(cur);
+    } else {
+      uint32_t* gh = ws.hist + uint64_t(cur) * 256;
+      if (sum) atomicAdd(gh + tid, sum);
+      __threadfence();
+      named_bar_sync(1, kCountThreads);
+      if (tid == 0) {
+        const uint32_t old = atomicAdd(ws.done + cur, run);
+        sh.s_last = ((old & kItemInvalid) == 0) && (uint64_t(old) + run == tiles);
+      }
+      named_bar_sync(1, kCountThreads);
+      if (sh.s_last) {
+        // the last CTA to add its counts ranks the tensor
+        __threadfence();
+        wait_buffer();
+        sh.h[posts & 1u][tid] = __ldcg(gh + tid);
+        named_bar_sync(1, kCountThreads);
+        post(cur);
+      }
+    }
     run = 0;
   };
+  bool timed_out = false;
   for (uint32_t it = 0;; ++it) {
     const int s = int(it % kCalStages);
     const bool ok = mbar_wait(&sh.full[s], (it / kCalStages) & 1);
     const CalHdr hd = sh.hdr[s];  // read before the vote: the stage may be released right after
     if (named_bar_red_or(1, kCountThreads, !ok)) {
       if (tid == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
-      return;
+      timed_out = true;
+      break;
     }
     if (hd.flags & kStageEnd) break;
     if (hd.item != cur) {
@@ -271,7 +406,11 @@ __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __g
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty[s]);
   }
-  if (run) flush();
+  if (run && !timed_out) flush();
+  // tell the select warp to stop once it has ranked everything posted
+  wait_buffer();
+  named_bar_sync(1, kCountThreads);
+  post(kSelectEnd);
 }
 
 }  // namespace

@@ -5,18 +5,23 @@
 //
 // Launches per call (after a 256-byte header memset):
 //   dec_prepare  validates each item's meta against the wire layout and the
-//                readable payload size, and finds each tile's escape range
-//                [k0, k1) by binary search of the sorted chunk_id stream
-//                (chunks 8*lt .. 8*lt+7 belong to tile lt);
+//                readable payload size, finds each tile's escape range
+//                [k0, k1) by searching the sorted chunk_id stream (chunks
+//                8*lt .. 8*lt+7 belong to tile lt), and (tables of several
+//                items) writes the tile -> item map; items of up to 32 tiles
+//                take one warp each;
 //   dec_main     persistent CTAs own a contiguous run of tiles.  A producer
-//                warp streams pk, sm and the tile's chunk_id/local_pos/esc_val
+//                warp (which resolves 32 tiles at a time, one per lane)
+//                streams pk, sm and the tile's chunk_id/local_pos/esc_val
 //                slices into a 4-stage shared-memory ring: TMA bulk copies for
 //                the 16-byte-aligned body of each slice and one zero-filling
 //                16-byte cp.async for its ragged end, so nothing outside the
-//                payload is read.  8 consumer warps decode 8 elements per
-//                thread step with the 16-entry dec_lut held in registers
-//                (byte permutes), apply the tile's escapes in shared memory and
-//                hand the finished 16 KiB tile to a TMA bulk store.
+//                payload is read.  A tile with more than 1024 escapes takes
+//                further stages carrying only its next escapes.  8 consumer
+//                warps decode 8 elements per thread step with the 16-entry
+//                dec_lut held in registers (byte permutes), patch the tile's
+//                escapes in shared memory and hand the finished 16 KiB tile
+//                to a TMA bulk store.
 #include "sz_internal.h"
 
 namespace sz {
@@ -27,9 +32,11 @@ constexpr int kDecConsumerWarps = 8;
 constexpr int kDecConsumers = kDecConsumerWarps * 32;
 constexpr int kDecThreads = kDecConsumers + 32;
 constexpr int kDecCtasPerSm = 2;
-constexpr uint32_t kEcap = 1024;  // escapes per tile staged in shared memory
+constexpr uint32_t kEcap = 1024;  // escapes per stage; a tile with more is sent as several stages
 constexpr uint32_t kRangeInvalid = 0xFFFFFFFFu;
-constexpr uint32_t kStageEnd = 1u, kStageInvalid = 2u, kStageSpill = 4u;
+// kStageCont: escapes only, continuing the previous stage's tile;
+// kStageMore: further escape stages of this tile follow.
+constexpr uint32_t kStageEnd = 1u, kStageInvalid = 2u, kStageCont = 4u, kStageMore = 8u;
 
 struct __align__(128) DecStage {
   uint8_t pk[kTile / 2 + 16];
@@ -39,9 +46,7 @@ struct __align__(128) DecStage {
   uint8_t ev[kEcap + 32];
   uint4 dec_lut;
   uint16_t* out;
-  const uint8_t* payload;  // for tiles whose escapes spill past kEcap
-  uint64_t off_cid, off_lpos, off_ev;
-  uint32_t k0, m, lt, n_tile, flags;
+  uint32_t m, lt, n_tile, flags;
   uint32_t sm_shift, cid_shift, lpos_shift, ev_shift;
 };
 
@@ -109,70 +114,136 @@ __device__ uint32_t lower_bound_cid16(const int32_t* cid, uint32_t e, uint32_t t
 }
 
 constexpr int kPrepWarps = 8;
+constexpr uint64_t kSmallTiles = 32;  // items of at most one 32-tile group are prepared by one warp
+constexpr uint32_t kDenseGroup = 4096;  // escapes in a 32-tile group above which tiles are searched, not counted
 
-// Escape ranges per tile.  blockIdx.y = item; each warp owns a group of 32
-// consecutive tiles of that item (lane l <-> tile ta + l).  The two half
-// warps bracket the group's escapes with 16-ary searches for the first
-// escape of tile ta and of tile ta + 32; the warp then reads the bracketed
-// chunk_id slice once, coalesced, counting escapes per tile in shared
-// memory, and a warp scan of the counts gives every tile's [k0, k1).
+// Escape ranges of the 32-tile group of item i starting at its tile ta (lane
+// l <-> tile ta + l), and the group's tile -> item map entries.  The two half
+// warps bracket the group's escapes with 16-ary searches for the first escape
+// of tile ta and of tile ta + 32; the warp then reads the bracketed chunk_id
+// slice once, coalesced, counting escapes per tile in shared memory, and a
+// warp scan of the counts gives every tile's [k0, k1).  A group with more
+// than kDenseGroup escapes is not read whole: each lane binary-searches its
+// own tile's first escape instead.  Writes outside the table's tiles are
+// dropped.
+__device__ void prepare_group(const Items& items, const DecWs& ws, uint32_t i, const sz_item& it, uint64_t tiles,
+                              bool bad, uint64_t ta, uint32_t lane, uint32_t* counts) {
+  const uint32_t ng = (tiles - ta < 32) ? uint32_t(tiles - ta) : 32u;
+  uint2 r = make_uint2(kRangeInvalid, 0);
+  if (!bad) {
+    const uint32_t e = uint32_t(it.meta->n_esc);
+    const int32_t* cid = reinterpret_cast<const int32_t*>(it.payload + it.meta->off_cid);
+    const uint32_t half_mask = lane < 16 ? 0x0000FFFFu : 0xFFFF0000u;
+    const uint32_t target = uint32_t(ta) * kChunksPerTile + (lane < 16 ? 0u : 32u * kChunksPerTile);
+    const uint32_t k = lower_bound_cid16(cid, e, target, lane & 15u, half_mask);
+    const uint32_t k_lo = __shfl_sync(0xFFFFFFFFu, k, 0);
+    const uint32_t k_hi = __shfl_sync(0xFFFFFFFFu, k, 16);
+    if (k_hi - k_lo > kDenseGroup) {
+      // many escapes: each lane finds the first escape of its own tile by a
+      // binary search of the group's slice (log2 of its length in loads)
+      const uint32_t target_l = (uint32_t(ta) + lane) * kChunksPerTile;
+      uint32_t lo = k_lo, len = k_hi - k_lo;
+      while (len > 0) {
+        const uint32_t half = len >> 1;
+        if (uint32_t(__ldg(cid + lo + half)) < target_l) {
+          lo += half + 1;
+          len -= half + 1;
+        } else {
+          len = half;
+        }
+      }
+      const uint32_t next = __shfl_down_sync(0xFFFFFFFFu, lo, 1);
+      r = make_uint2(lo, lane == 31 ? k_hi : next);
+    } else {
+      counts[lane] = 0;
+      __syncwarp();
+      // 8 independent loads per lane per round, then the shared-memory counts
+      for (uint32_t kb = k_lo; kb < k_hi; kb += 32 * 8) {
+        uint32_t c8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t kk = kb + lane + 32u * u;
+          c8[u] = kk < k_hi ? uint32_t(__ldg(cid + kk)) : 0xFFFFFFFFu;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t rel = (c8[u] >> 3) - uint32_t(ta);  // tile within the group
+          if (c8[u] != 0xFFFFFFFFu && rel < 32u) atomicAdd(&counts[rel], 1u);
+        }
+      }
+      __syncwarp();
+      const uint32_t c = counts[lane];
+      uint32_t incl = c;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= uint32_t(d)) incl += o;
+      }
+      r = make_uint2(k_lo + incl - c, k_lo + incl);
+      __syncwarp();  // counts is reused by the warp's next group
+    }
+  }
+  const uint64_t tt = it.tile_begin + ta + lane;
+  if (lane < ng && tt < items.total_tiles) {
+    ws.ranges[tt] = r;
+    if (ws.tile_item) ws.tile_item[tt] = i;
+  }
+}
+
+// Validation and escape ranges per item.  Rows of the grid (blockIdx.y) take
+// groups of kPrepWarps consecutive items: items of at most 32 tiles are
+// prepared by one warp of the row's first block, larger ones by the row's
+// blocks dealt round-robin over them (warp per 32-tile group).
 __global__ void __launch_bounds__(kPrepWarps * 32) dec_prepare(const __grid_constant__ Items items, DecWs ws) {
   __shared__ uint32_t s_bad;
   __shared__ uint32_t counts[kPrepWarps][32];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t warp = threadIdx.x >> 5;
-  for (uint32_t i = blockIdx.y; i < items.count; i += gridDim.y) {
-    const sz_item& it = item_at(items, i);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      s_bad = item_problems(items, i);
-      if (blockIdx.x == 0) {
-        ws.item_flags[i] = s_bad;
-        if (s_bad) set_flag(ws.hdr, s_bad);
+  const uint32_t groups = (items.count + kPrepWarps - 1) / kPrepWarps;
+  for (uint32_t grp = blockIdx.y; grp < groups; grp += gridDim.y) {
+    {
+      const uint32_t i = grp * kPrepWarps + warp;
+      if (blockIdx.x == 0 && i < items.count) {
+        const sz_item& it = item_at(items, i);
+        if (it.n <= kSmallTiles * kTile) {
+          uint32_t bad = 0;
+          if (lane == 0) {
+            bad = item_problems(items, i);
+            ws.item_flags[i] = bad;
+            if (bad) set_flag(ws.hdr, bad);
+          }
+          bad = __shfl_sync(0xFFFFFFFFu, bad, 0);
+          const uint64_t tiles = tiles_of(it.n);
+          if (!(bad & SZ_FLAG_ITEMS) && tiles > 0) prepare_group(items, ws, i, it, tiles, bad != 0, 0, lane, counts[warp]);
+        }
       }
     }
-    __syncthreads();
-    const bool bad = s_bad != 0;
-    const uint64_t tiles = (it.n > SZ_MAX_ELEMS) ? 0 : tiles_of(it.n);
-    const uint32_t e = bad ? 0u : uint32_t(it.meta->n_esc);
-    const int32_t* cid = bad ? nullptr : reinterpret_cast<const int32_t*>(it.payload + it.meta->off_cid);
-    const uint32_t half_mask = lane < 16 ? 0x0000FFFFu : 0xFFFF0000u;
-    for (uint64_t ta = (uint64_t(blockIdx.x) * kPrepWarps + warp) * 32; ta < tiles;
-         ta += uint64_t(gridDim.x) * kPrepWarps * 32) {
-      const uint32_t ng = (tiles - ta < 32) ? uint32_t(tiles - ta) : 32u;
-      uint2 r = make_uint2(kRangeInvalid, 0);
-      if (!bad) {
-        const uint32_t target = uint32_t(ta) * kChunksPerTile + (lane < 16 ? 0u : 32u * kChunksPerTile);
-        const uint32_t k = lower_bound_cid16(cid, e, target, lane & 15u, half_mask);
-        const uint32_t k_lo = __shfl_sync(0xFFFFFFFFu, k, 0);
-        const uint32_t k_hi = __shfl_sync(0xFFFFFFFFu, k, 16);
-        counts[warp][lane] = 0;
-        __syncwarp();
-        // 8 independent loads per lane per round, then the shared-memory counts
-        for (uint32_t kb = k_lo; kb < k_hi; kb += 32 * 8) {
-          uint32_t c8[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint32_t kk = kb + lane + 32u * u;
-            c8[u] = kk < k_hi ? uint32_t(__ldg(cid + kk)) : 0xFFFFFFFFu;
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint32_t rel = (c8[u] >> 3) - uint32_t(ta);  // tile within the group
-            if (c8[u] != 0xFFFFFFFFu && rel < 32u) atomicAdd(&counts[warp][rel], 1u);
-          }
+    // larger items: the row's blocks are dealt round-robin over its items,
+    // blocks_per_item of them to each
+    const uint32_t in_row = min(uint32_t(kPrepWarps), items.count - grp * kPrepWarps);
+    const uint32_t R = min(in_row, gridDim.x);
+    const uint32_t blocks_per_item = gridDim.x / R;
+    const uint32_t rank = blockIdx.x / R;
+    if (rank >= blocks_per_item) continue;
+    for (uint32_t q = blockIdx.x % R; q < in_row; q += R) {
+      const uint32_t i = grp * kPrepWarps + q;
+      const sz_item& it = item_at(items, i);
+      if (it.n <= kSmallTiles * kTile) continue;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        s_bad = item_problems(items, i);
+        if (rank == 0) {
+          ws.item_flags[i] = s_bad;
+          if (s_bad) set_flag(ws.hdr, s_bad);
         }
-        __syncwarp();
-        const uint32_t c = counts[warp][lane];
-        uint32_t incl = c;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-          const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-          if (lane >= uint32_t(d)) incl += o;
-        }
-        r = make_uint2(k_lo + incl - c, k_lo + incl);
       }
-      if (lane < ng) ws.ranges[it.tile_begin + ta + lane] = r;
+      __syncthreads();
+      const uint32_t bad = s_bad;
+      if (bad & SZ_FLAG_ITEMS) continue;
+      const uint64_t tiles = (it.n > SZ_MAX_ELEMS) ? 0 : tiles_of(it.n);
+      for (uint64_t ta = (uint64_t(rank) * kPrepWarps + warp) * 32; ta < tiles;
+           ta += uint64_t(blocks_per_item) * kPrepWarps * 32)
+        prepare_group(items, ws, i, it, tiles, bad != 0, ta, lane, counts[warp]);
     }
   }
 }
@@ -192,10 +263,6 @@ __device__ __forceinline__ uint2 decode4(uint32_t c16, uint32_t s4, uint32_t d0,
   r.x = ((y0 >> 1) & 0x7F807F80u) | (y0 & 0x007F007Fu) | ((y0 << 8) & 0x80008000u);
   r.y = ((y1 >> 1) & 0x7F807F80u) | (y1 & 0x007F007Fu) | ((y1 << 8) & 0x80008000u);
   return r;
-}
-
-__device__ __forceinline__ uint16_t merge_one(uint32_t sm, uint32_t exp) {
-  return uint16_t(((sm & 0x80u) << 8) | ((exp & 0xFFu) << 7) | (sm & 0x7Fu));
 }
 
 // One slice copy into shared memory: the aligned body by TMA (issued by the
@@ -239,116 +306,155 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
 
   if (warp == kDecConsumerWarps) {
     // ---------------------------------------------------------------- producer warp
-    uint32_t cur = 0xFFFFFFFFu;
-    uint64_t cur_begin = 0, cur_end = 0;
-    uint4 dlut = make_uint4(0, 0, 0, 0);
-    uint2 rec = make_uint2(0, 0);
-    for (uint64_t t = t0, it = 0;; ++t, ++it) {
-      const int s = int(it % kDecStages);
-      if (it >= uint64_t(kDecStages)) {
-        if (!mbar_wait(&sh.empty[s], uint32_t((it / kDecStages) - 1) & 1)) {
-          if (lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
-          return;
-        }
+    // Lane l holds what the producer needs of tile w0 + l of the current
+    // 32-tile window, resolved in parallel when the window starts: the escape
+    // range, the item (tile -> item map), its payload, output, dec_lut and
+    // section offsets.
+    bool w_ok = false;
+    uint2 w_rec = make_uint2(0, 0);
+    const uint8_t* w_base = nullptr;
+    uint16_t* w_out = nullptr;
+    uint64_t w_g = 0, w_off_sm = 0, w_off_cid = 0, w_off_lpos = 0, w_off_ev = 0;
+    uint4 w_dlut = make_uint4(0, 0, 0, 0);
+    uint32_t w_lt = 0, w_nt = 0;
+    uint64_t it = 0;  // stages handed out
+    // next free stage of the ring (bounded wait agreed by the warp)
+    auto acquire = [&](int& s) -> bool {
+      s = int(it % kDecStages);
+      if (it >= uint64_t(kDecStages) &&
+          !__all_sync(0xFFFFFFFFu, mbar_wait(&sh.empty[s], uint32_t((it / kDecStages) - 1) & 1))) {
+        if (lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+        return false;
       }
-      DecStage& st = sh.st[s];
+      return true;
+    };
+    for (uint64_t t = t0;; ++t) {
+      int s;
+      if (!acquire(s)) return;
       if (t >= t1) {
         if (lane == 0) {
-          st.flags = kStageEnd;
+          sh.st[s].flags = kStageEnd;
           mbar_arrive(&sh.full[s]);
         }
         cp_async_mbar_arrive_noinc(&sh.full[s]);
         return;
       }
-      // escape ranges of the next 32 tiles, one per lane
       if (((t - t0) & 31) == 0) {
         const uint64_t mine = t + lane;
-        rec = (mine < t1) ? ws.ranges[mine] : make_uint2(kRangeInvalid, 0);
+        w_ok = false;
+        if (mine < t1) {
+          w_rec = ws.ranges[mine];
+          const uint32_t idx = ws.tile_item ? ws.tile_item[mine] : 0u;
+          if (idx < items.count && w_rec.x != kRangeInvalid && ws.item_flags[idx] == 0) {
+            const sz_item& itm = item_at(items, idx);
+            const uint64_t tb = itm.tile_begin;
+            if (mine >= tb && mine - tb < tiles_of(itm.n)) {
+              w_lt = uint32_t(mine - tb);
+              w_g = uint64_t(w_lt) * kTile;
+              w_nt = (itm.n - w_g < kTile) ? uint32_t(itm.n - w_g) : kTile;
+              w_base = itm.payload;
+              w_out = itm.out + w_g;
+              const sz_meta* mp = itm.meta;
+              w_off_sm = mp->off_sm;
+              w_off_cid = mp->off_cid;
+              w_off_lpos = mp->off_lpos;
+              w_off_ev = mp->off_ev;
+              w_dlut = *reinterpret_cast<const uint4*>(itm.codebook->dec_lut);
+              w_ok = true;
+            }
+          }
+        }
       }
-      const uint32_t src_lane = uint32_t((t - t0) & 31);
-      const uint32_t k0 = __shfl_sync(0xFFFFFFFFu, rec.x, src_lane);
-      const uint32_t k1 = __shfl_sync(0xFFFFFFFFu, rec.y, src_lane);
-      if (t >= cur_end) {
-        cur = find_item(items, t);
-        cur_begin = item_at(items, cur).tile_begin;
-        cur_end = cur_begin + tiles_of(item_at(items, cur).n);
-        if (ws.item_flags[cur] == 0) dlut = *reinterpret_cast<const uint4*>(item_at(items, cur).codebook->dec_lut);
-      }
-      const sz_item& itm = item_at(items, cur);
-      const uint32_t lt = uint32_t(t - cur_begin);
-      const uint64_t g = uint64_t(lt) * kTile;
-      const bool invalid = (k0 == kRangeInvalid) || ws.item_flags[cur] != 0 || g >= itm.n;
-      const uint32_t nt = invalid ? 0u : ((itm.n - g < kTile) ? uint32_t(itm.n - g) : kTile);
-      if (invalid) {
+      const uint32_t src = uint32_t((t - t0) & 31);
+      if (!__shfl_sync(0xFFFFFFFFu, w_ok, src)) {
         if (lane == 0) {
-          st.flags = kStageInvalid;
+          sh.st[s].flags = kStageInvalid;
           mbar_arrive(&sh.full[s]);
         }
         cp_async_mbar_arrive_noinc(&sh.full[s]);
+        ++it;
         continue;
       }
-      const sz_meta* mp = itm.meta;
-      const uint64_t off_sm = mp->off_sm, off_cid = mp->off_cid, off_lpos = mp->off_lpos, off_ev = mp->off_ev;
-      const uint8_t* base = itm.payload;
+      auto shfl64 = [&](uint64_t v) {
+        return (uint64_t(__shfl_sync(0xFFFFFFFFu, uint32_t(v >> 32), src)) << 32) |
+               __shfl_sync(0xFFFFFFFFu, uint32_t(v), src);
+      };
+      const uint32_t k0 = __shfl_sync(0xFFFFFFFFu, w_rec.x, src);
+      const uint32_t k1 = __shfl_sync(0xFFFFFFFFu, w_rec.y, src);
+      const uint32_t lt = __shfl_sync(0xFFFFFFFFu, w_lt, src);
+      const uint32_t nt = __shfl_sync(0xFFFFFFFFu, w_nt, src);
+      const uint64_t g = shfl64(w_g);
+      const uint64_t off_sm = shfl64(w_off_sm), off_cid = shfl64(w_off_cid), off_lpos = shfl64(w_off_lpos),
+                     off_ev = shfl64(w_off_ev);
+      const uint8_t* base = reinterpret_cast<const uint8_t*>(shfl64(reinterpret_cast<uint64_t>(w_base)));
+      uint16_t* const out_t = reinterpret_cast<uint16_t*>(shfl64(reinterpret_cast<uint64_t>(w_out)));
+      uint4 dlut;
+      dlut.x = __shfl_sync(0xFFFFFFFFu, w_dlut.x, src);
+      dlut.y = __shfl_sync(0xFFFFFFFFu, w_dlut.y, src);
+      dlut.z = __shfl_sync(0xFFFFFFFFu, w_dlut.z, src);
+      dlut.w = __shfl_sync(0xFFFFFFFFu, w_dlut.w, src);
       const uint32_t m = (k1 > k0) ? k1 - k0 : 0u;
-      const bool spill = m > kEcap;
+      const uint32_t pieces = m ? (m + kEcap - 1) / kEcap : 1u;
       const Slice spk = slice_of(g >> 1, (nt + 1) >> 1);
       const Slice ssm = slice_of(off_sm + g, nt);
-      Slice scid = slice_of(off_cid + 4ull * k0, 4ull * m);
-      Slice slp = slice_of(off_lpos + 2ull * k0, 2ull * m);
-      Slice sev = slice_of(off_ev + k0, m);
-      const bool esc_smem = (m > 0) && !spill;
-      const uint32_t tx = uint32_t(spk.a1 - spk.a0) + uint32_t(ssm.a1 - ssm.a0) +
-                          (esc_smem ? uint32_t(scid.a1 - scid.a0) + uint32_t(slp.a1 - slp.a0) +
-                                          uint32_t(sev.a1 - sev.a0)
-                                    : 0u);
-      if (lane == 0) {
-        st.dec_lut = dlut;
-        st.out = itm.out + g;
-        st.payload = base;
-        st.off_cid = off_cid;
-        st.off_lpos = off_lpos;
-        st.off_ev = off_ev;
-        st.k0 = k0;
-        st.m = m;
-        st.lt = lt;
-        st.n_tile = nt;
-        st.flags = spill ? kStageSpill : 0u;
-        st.sm_shift = uint32_t(off_sm + g - ssm.a0);
-        st.cid_shift = uint32_t(off_cid + 4ull * k0 - scid.a0);
-        st.lpos_shift = uint32_t(off_lpos + 2ull * k0 - slp.a0);
-        st.ev_shift = uint32_t(off_ev + k0 - sev.a0);
-        mbar_arrive_expect_tx(&sh.full[s], tx);
-        if (spk.a1 > spk.a0) bulk_g2s(st.pk, base + spk.a0, uint32_t(spk.a1 - spk.a0), &sh.full[s]);
-        if (ssm.a1 > ssm.a0) bulk_g2s(st.sm, base + ssm.a0, uint32_t(ssm.a1 - ssm.a0), &sh.full[s]);
-        if (esc_smem) {
-          if (scid.a1 > scid.a0) bulk_g2s(st.cid, base + scid.a0, uint32_t(scid.a1 - scid.a0), &sh.full[s]);
-          if (slp.a1 > slp.a0) bulk_g2s(st.lpos, base + slp.a0, uint32_t(slp.a1 - slp.a0), &sh.full[s]);
-          if (sev.a1 > sev.a0) bulk_g2s(st.ev, base + sev.a0, uint32_t(sev.a1 - sev.a0), &sh.full[s]);
+      // the tile: pk, sm and its first kEcap escapes, then one stage per
+      // further kEcap escapes
+      for (uint32_t pc = 0; pc < pieces; ++pc) {
+        if (pc > 0 && !acquire(s)) return;
+        DecStage& st = sh.st[s];
+        const bool first = pc == 0;
+        const uint32_t pk0 = k0 + pc * kEcap;
+        const uint32_t pm = m ? ((m - pc * kEcap < kEcap) ? m - pc * kEcap : kEcap) : 0u;
+        const Slice scid = slice_of(off_cid + 4ull * pk0, 4ull * pm);
+        const Slice slp = slice_of(off_lpos + 2ull * pk0, 2ull * pm);
+        const Slice sev = slice_of(off_ev + pk0, pm);
+        const uint32_t tx = (first ? uint32_t(spk.a1 - spk.a0) + uint32_t(ssm.a1 - ssm.a0) : 0u) +
+                            (pm ? uint32_t(scid.a1 - scid.a0) + uint32_t(slp.a1 - slp.a0) + uint32_t(sev.a1 - sev.a0)
+                                : 0u);
+        if (lane == 0) {
+          st.dec_lut = dlut;
+          st.out = out_t;
+          st.m = pm;
+          st.lt = lt;
+          st.n_tile = nt;
+          st.flags = (first ? 0u : kStageCont) | (pc + 1 < pieces ? kStageMore : 0u);
+          st.sm_shift = uint32_t(off_sm + g - ssm.a0);
+          st.cid_shift = uint32_t(off_cid + 4ull * pk0 - scid.a0);
+          st.lpos_shift = uint32_t(off_lpos + 2ull * pk0 - slp.a0);
+          st.ev_shift = uint32_t(off_ev + pk0 - sev.a0);
+          mbar_arrive_expect_tx(&sh.full[s], tx);
+          if (first && spk.a1 > spk.a0) bulk_g2s(st.pk, base + spk.a0, uint32_t(spk.a1 - spk.a0), &sh.full[s]);
+          if (first && ssm.a1 > ssm.a0) bulk_g2s(st.sm, base + ssm.a0, uint32_t(ssm.a1 - ssm.a0), &sh.full[s]);
+          if (pm && scid.a1 > scid.a0) bulk_g2s(st.cid, base + scid.a0, uint32_t(scid.a1 - scid.a0), &sh.full[s]);
+          if (pm && slp.a1 > slp.a0) bulk_g2s(st.lpos, base + slp.a0, uint32_t(slp.a1 - slp.a0), &sh.full[s]);
+          if (pm && sev.a1 > sev.a0) bulk_g2s(st.ev, base + sev.a0, uint32_t(sev.a1 - sev.a0), &sh.full[s]);
+        } else if (first && lane == 1 && spk.end > spk.a1) {
+          cp_async16_zfill(st.pk + (spk.a1 - spk.a0), base + spk.a1, uint32_t(spk.end - spk.a1));
+        } else if (first && lane == 2 && ssm.end > ssm.a1) {
+          cp_async16_zfill(st.sm + (ssm.a1 - ssm.a0), base + ssm.a1, uint32_t(ssm.end - ssm.a1));
+        } else if (pm && lane == 3 && scid.end > scid.a1) {
+          cp_async16_zfill(reinterpret_cast<uint8_t*>(st.cid) + (scid.a1 - scid.a0), base + scid.a1,
+                           uint32_t(scid.end - scid.a1));
+        } else if (pm && lane == 4 && slp.end > slp.a1) {
+          cp_async16_zfill(reinterpret_cast<uint8_t*>(st.lpos) + (slp.a1 - slp.a0), base + slp.a1,
+                           uint32_t(slp.end - slp.a1));
+        } else if (pm && lane == 5 && sev.end > sev.a1) {
+          cp_async16_zfill(st.ev + (sev.a1 - sev.a0), base + sev.a1, uint32_t(sev.end - sev.a1));
         }
-      } else if (lane == 1 && spk.end > spk.a1) {
-        cp_async16_zfill(st.pk + (spk.a1 - spk.a0), base + spk.a1, uint32_t(spk.end - spk.a1));
-      } else if (lane == 2 && ssm.end > ssm.a1) {
-        cp_async16_zfill(st.sm + (ssm.a1 - ssm.a0), base + ssm.a1, uint32_t(ssm.end - ssm.a1));
-      } else if (esc_smem && lane == 3 && scid.end > scid.a1) {
-        cp_async16_zfill(reinterpret_cast<uint8_t*>(st.cid) + (scid.a1 - scid.a0), base + scid.a1,
-                         uint32_t(scid.end - scid.a1));
-      } else if (esc_smem && lane == 4 && slp.end > slp.a1) {
-        cp_async16_zfill(reinterpret_cast<uint8_t*>(st.lpos) + (slp.a1 - slp.a0), base + slp.a1,
-                         uint32_t(slp.end - slp.a1));
-      } else if (esc_smem && lane == 5 && sev.end > sev.a1) {
-        cp_async16_zfill(st.ev + (sev.a1 - sev.a0), base + sev.a1, uint32_t(sev.end - sev.a1));
+        cp_async_mbar_arrive_noinc(&sh.full[s]);
+        ++it;
       }
-      cp_async_mbar_arrive_noinc(&sh.full[s]);
     }
   }
 
   // ------------------------------------------------------------------ consumer warps
   uint32_t bad_escape = 0;
+  uint32_t tiles_done = 0;  // output buffer of the current tile: out[tiles_done & 1]
+  bool in_tile = false;     // the previous stage left its tile open (more escape stages)
   for (uint32_t it = 0;; ++it) {
     const int s = int(it % kDecStages);
-    const int ob = int(it & 1);
-    if (tid == 0) bulk_wait_read<1>();  // the store that last used out[ob] has read it
+    const int ob = int(tiles_done & 1u);
+    if (tid == 0 && !in_tile) bulk_wait_read<1>();  // the store that last used out[ob] has read it
     const bool ok = mbar_wait(&sh.full[s], (it / kDecStages) & 1);
     const DecStage& st = sh.st[s];
     // read before the vote: after it, an invalid tile's stage is released
@@ -364,7 +470,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     }
     const uint32_t nt = st.n_tile;
     uint16_t* const outs = sh.out[ob];
-    {
+    if (!(flags & kStageCont)) {
       const uint4 dl = st.dec_lut;
       const uint32_t shift = st.sm_shift;
 #pragma unroll
@@ -382,25 +488,18 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     }
     const uint32_t m = st.m;
     if (m) {
+      // an escape's code is 0, so its decoded value already holds the right
+      // sign and mantissa: the patch rewrites the exponent field only
       named_bar_sync(1, kDecConsumers);
-      const bool spill = flags & kStageSpill;
       const uint32_t chunk0 = st.lt * kChunksPerTile;
       for (uint32_t k = uint32_t(tid); k < m; k += kDecConsumers) {
-        uint32_t c, p, ev;
-        if (!spill) {
-          c = st.cid[(st.cid_shift >> 2) + k];
-          p = st.lpos[(st.lpos_shift >> 1) + k];
-          ev = st.ev[st.ev_shift + k];
-        } else {
-          const uint64_t kk = uint64_t(st.k0) + k;
-          c = *reinterpret_cast<const uint32_t*>(st.payload + st.off_cid + 4 * kk);
-          p = *reinterpret_cast<const uint16_t*>(st.payload + st.off_lpos + 2 * kk);
-          ev = st.payload[st.off_ev + kk];
-        }
+        const uint32_t c = st.cid[(st.cid_shift >> 2) + k];
+        const uint32_t p = st.lpos[(st.lpos_shift >> 1) + k];
+        const uint32_t ev = st.ev[st.ev_shift + k];
         const uint32_t rel = c - chunk0;
         const uint32_t pos = rel * kChunk + p;
         if (rel < kChunksPerTile && p < kChunk && pos < nt) {
-          outs[pos] = merge_one(st.sm[st.sm_shift + pos], ev);
+          outs[pos] = uint16_t((outs[pos] & 0x807Fu) | (ev << 7));
         } else {
           bad_escape = 1;
         }
@@ -408,14 +507,19 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     }
     fence_proxy_async_smem();
     named_bar_sync(1, kDecConsumers);
+    const bool more = (flags & kStageMore) != 0;
     if (tid == 0) {
       uint16_t* const outp = st.out;  // the stage may be refilled once released
       mbar_arrive(&sh.empty[s]);
-      const uint32_t body = (nt * 2u) & ~15u;
-      if (body) bulk_s2g(outp, outs, body);
-      bulk_commit();
-      for (uint32_t k = body / 2u; k < nt; ++k) outp[k] = outs[k];
+      if (!more) {
+        const uint32_t body = (nt * 2u) & ~15u;
+        if (body) bulk_s2g(outp, outs, body);
+        bulk_commit();
+        for (uint32_t k = body / 2u; k < nt; ++k) outp[k] = outs[k];
+      }
     }
+    in_tile = more;
+    if (!more) ++tiles_done;
   }
   if (bad_escape) set_flag(ws.hdr, SZ_FLAG_ESCAPE);
   if (tid == 0) bulk_wait_all<0>();
@@ -428,12 +532,16 @@ cudaError_t launch_decode(const Items& items, void* ws_base, cudaStream_t stream
   cudaError_t err = cudaMemsetAsync(ws_base, 0, sizeof(WsHeader), stream);
   if (err != cudaSuccess) return err;
   {
-    // blockIdx.y = item; x covers the average item's 32-tile groups (8 per block)
+    // blockIdx.y = group of kPrepWarps items; x covers the average item's
+    // 32-tile groups (8 per block) times the items a row takes in turn (1 when
+    // items are of one group or less: their warps need no other block)
     const uint64_t per_item = items.count ? (items.total_tiles + items.count - 1) / items.count : 0;
-    uint64_t gx = (per_item + 32 * kPrepWarps - 1) / (32 * kPrepWarps);
+    const uint64_t per_row = items.count < uint32_t(kPrepWarps) ? items.count : uint64_t(kPrepWarps);
+    uint64_t gx = per_item <= kSmallTiles ? 1 : (per_item + 32 * kPrepWarps - 1) / (32 * kPrepWarps) * per_row;
     if (gx < 1) gx = 1;
     if (gx > 1024) gx = 1024;
-    const unsigned gy = items.count < 65535u ? items.count : 65535u;
+    const uint64_t groups = (uint64_t(items.count) + kPrepWarps - 1) / kPrepWarps;
+    const unsigned gy = unsigned(groups < 65535u ? (groups ? groups : 1) : 65535u);
     dec_prepare<<<dim3(unsigned(gx), gy), kPrepWarps * 32, 0, stream>>>(items, ws);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }

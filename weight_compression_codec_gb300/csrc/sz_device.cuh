@@ -70,6 +70,18 @@ __device__ inline uint32_t find_item(const Items& it, uint64_t tile) {
   return lo;
 }
 
+// Tile -> item maps (filled by the prepare kernels) let a producer resolve any
+// tile with one load: in the decode workspace of every table of more than one
+// item, in the encode workspace of tables of more than kEncMapItems items
+// (smaller ones are searched directly, and only when a run of tiles leaves
+// the current item).
+constexpr uint32_t kEncMapItems = 256;
+__host__ __device__ inline bool dec_uses_tile_map(uint32_t count) { return count > 1; }
+__host__ __device__ inline bool enc_uses_tile_map(uint32_t count) { return count > kEncMapItems; }
+__host__ __device__ inline uint64_t tile_map_bytes(bool used, uint64_t tiles) {
+  return used ? ((tiles * 4 + 255u) & ~uint64_t(255)) : 0;
+}
+
 // ------------------------------------------------------------------ workspace
 // Every workspace starts with this header (256 bytes).
 struct WsHeader {
@@ -103,7 +115,8 @@ __host__ __device__ inline CalWs cal_ws(void* base, uint32_t count) {
 // encode: header | item_flags[count] u32 | item_esc[count] u32 (escape total) |
 //         seg_ticket[count] u32 | status[total_tiles] u64 (segment lookback words,
 //         at each segment's first tile) | chunk_cnt[total_tiles * 8] u16 |
-//         lpos staging[total_tiles * 8192] u16 | ev staging[total_tiles * 8192] u8
+//         lpos staging[total_tiles * 8192] u16 | ev staging[total_tiles * 8192] u8 |
+//         tile_item[total_tiles] u32 (tables of more than kEncMapItems items)
 // Staging slot of chunk c (global chunk index tile * 8 + chunk) starts at
 // entry c * 1024 and holds the chunk's escapes in element order.
 struct EncWs {
@@ -115,10 +128,11 @@ struct EncWs {
   uint16_t* chunk_cnt;
   uint16_t* lpos;
   uint8_t* ev;
+  uint32_t* tile_item;
 };
 __host__ __device__ inline uint64_t enc_ws_bytes(uint32_t count, uint64_t tiles) {
   return 256 + 3 * round_up256(uint64_t(count) * 4) + round_up256(tiles * 8) + round_up256(tiles * 16) +
-         round_up256(tiles * kTile * 2) + round_up256(tiles * kTile);
+         round_up256(tiles * kTile * 2) + round_up256(tiles * kTile) + tile_map_bytes(enc_uses_tile_map(count), tiles);
 }
 __host__ __device__ inline EncWs enc_ws(void* base, uint32_t count, uint64_t tiles) {
   char* p = static_cast<char*>(base);
@@ -138,17 +152,21 @@ __host__ __device__ inline EncWs enc_ws(void* base, uint32_t count, uint64_t til
   w.lpos = reinterpret_cast<uint16_t*>(p);
   p += round_up256(tiles * kTile * 2);
   w.ev = reinterpret_cast<uint8_t*>(p);
+  p += round_up256(tiles * kTile);
+  w.tile_item = enc_uses_tile_map(count) ? reinterpret_cast<uint32_t*>(p) : nullptr;
   return w;
 }
 
-// decode: header | item_flags[count] u32 | ranges[total_tiles] (k0, k1) u32x2
+// decode: header | item_flags[count] u32 | ranges[total_tiles] (k0, k1) u32x2 |
+//         tile_item[total_tiles] u32 (tables of more than one item)
 struct DecWs {
   WsHeader* hdr;
   uint32_t* item_flags;
   uint2* ranges;
+  uint32_t* tile_item;
 };
 __host__ __device__ inline uint64_t dec_ws_bytes(uint32_t count, uint64_t tiles) {
-  return 256 + round_up256(uint64_t(count) * 4) + round_up256(tiles * 8);
+  return 256 + round_up256(uint64_t(count) * 4) + round_up256(tiles * 8) + tile_map_bytes(dec_uses_tile_map(count), tiles);
 }
 __host__ __device__ inline DecWs dec_ws(void* base, uint32_t count, uint64_t tiles) {
   char* p = static_cast<char*>(base);
@@ -158,6 +176,8 @@ __host__ __device__ inline DecWs dec_ws(void* base, uint32_t count, uint64_t til
   w.item_flags = reinterpret_cast<uint32_t*>(p);
   p += round_up256(uint64_t(count) * 4);
   w.ranges = reinterpret_cast<uint2*>(p);
+  p += round_up256(tiles * 8);
+  w.tile_item = dec_uses_tile_map(count) ? reinterpret_cast<uint32_t*>(p) : nullptr;
   return w;
 }
 

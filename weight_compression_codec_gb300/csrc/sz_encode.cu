@@ -3,23 +3,26 @@
 //
 // Launches per call (after a 256-byte header memset):
 //   enc_prepare  validates the item table, zeroes per-tensor escape totals,
-//                segment tickets and segment status words;
-//   enc_main     persistent CTAs own contiguous runs of 8192-element tiles.
-//                A producer warp streams each tile (and the tensor's enc_lut)
-//                into a 4-stage shared-memory ring with TMA bulk copies; 8
-//                chunk warps -- warp w owns chunk w (1024 elements) -- split
-//                and pack with coalesced pk/sm stores, and compact the chunk's
-//                escapes with ballot/popc in element order into the chunk's
-//                staging slot.  The chunk counts and each tensor's escape
-//                total are recorded.  No warp ever waits on another CTA.
-//   enc_place    per tensor, segments of 256 chunks (claimed by ticket, so
-//                segments start in order): a block scan of the chunk counts
-//                and a decoupled lookback across the tensor's segments give
-//                each escape its global index; chunk_id, local_pos and
+//                segment tickets and segment status words, and (tables of
+//                more than 256 tensors) writes the tile -> tensor map;
+//   enc_main     persistent CTAs take runs of 4 tiles (8192 elements each)
+//                from a device-wide ticket.  A producer warp streams each
+//                tile (and the tensor's enc_lut) into a 4-stage shared-memory
+//                ring with TMA bulk copies; 8 chunk warps -- warp w owns chunk
+//                w (1024 elements) -- split and pack with coalesced pk/sm
+//                stores, and compact the chunk's escapes with ballot/popc in
+//                element order into the chunk's staging slot.  The chunk
+//                counts and each tensor's escape total are recorded.  No warp
+//                ever waits on another CTA.
+//   enc_place    writes each tensor's pads and meta and gives every escape its
+//                global index: tensors of at most 256 chunks by one warp (a
+//                warp scan of the chunk counts), larger ones by segments of
+//                256 chunks claimed by ticket (so segments start in order), a
+//                block scan of the chunk counts and a decoupled lookback
+//                across the tensor's segments.  chunk_id, local_pos and
 //                esc_val are then written once, in order, at their final
 //                offsets (the tensor's total is already known, so every
-//                offset is).  The segment holding chunk 0 also zeroes the pad
-//                bytes and writes the meta.
+//                offset is).
 // Every wait is bounded (kWaitTimeoutNs); on timeout SZ_FLAG_TIMEOUT is raised.
 #include "sz_internal.h"
 
@@ -48,10 +51,9 @@ struct __align__(128) EncStage {
 
 constexpr uint32_t kRun = 4;  // tiles per ticket
 
-// What the producer needs of an item; cached in shared memory for tables of
-// up to kCachedItems items, so mapping a ticket to its item costs no global
-// round trip.
-constexpr uint32_t kCachedItems = 128;
+// What the producer needs of an item.  When a ticket's run of tiles leaves
+// the current item, the producer's lanes resolve the run's tiles in parallel
+// (tile -> item map or table search, then the item) into shared memory.
 struct ItemLite {
   uint64_t tile_begin, n;
   const uint16_t* x;
@@ -74,8 +76,9 @@ __device__ __forceinline__ ItemLite item_lite(const Items& items, const EncWs& w
 }
 
 struct EncShared {
-  ItemLite item[kCachedItems];
   EncStage st[kEncStages];
+  ItemLite run_item[kRun];
+  uint32_t run_idx[kRun];
   uint64_t full[kEncStages];
   uint64_t empty[kEncStages];
 };
@@ -102,6 +105,17 @@ __global__ void enc_prepare(const __grid_constant__ Items items, EncWs ws) {
     ws.item_esc[i] = 0;
     ws.seg_ticket[i] = 0;
     if (bad) set_flag(ws.hdr, bad);
+  }
+  if (ws.tile_item != nullptr) {
+    // one warp per item writes the item's tile -> item map entries (clipped to the table's tiles)
+    const uint32_t lane = threadIdx.x & 31u;
+    const uint64_t nwarps = nthreads / 32;
+    for (uint64_t i = gtid / 32; i < items.count; i += nwarps) {
+      const sz_item& it = item_at(items, uint32_t(i));
+      const uint64_t tb = it.tile_begin;
+      const uint64_t te = (it.n > SZ_MAX_ELEMS) ? tb : tb + tiles_of(it.n);
+      for (uint64_t t = tb + lane; t < te && t < items.total_tiles; t += 32) ws.tile_item[t] = uint32_t(i);
+    }
   }
 }
 
@@ -323,8 +337,6 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
     }
     fence_mbar_init();
   }
-  if (items.count <= kCachedItems)
-    for (uint32_t i = tid; i < items.count; i += kEncThreads) sh.item[i] = item_lite(items, ws, i);
   __syncthreads();
 
   if (warp == kProducerWarp) {
@@ -335,6 +347,7 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
     uint32_t run_pos = kRun;
     uint32_t cur = 0xFFFFFFFFu;
     ItemLite itm{};
+    bool run_in_cur = false;
     for (uint32_t it = 0;; ++it) {
       const int s = int(it % kEncStages);
       if (it >= uint32_t(kEncStages) && !warp_wait(&sh.empty[s], ((it / kEncStages) - 1) & 1)) {
@@ -345,8 +358,21 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
         if (lane == 0) run_base = atomicAdd(&ws.hdr->ticket, 1ull * kRun);
         run_base = __shfl_sync(FULL, run_base, 0);
         run_pos = 0;
+        // a run inside the current item needs no lookup
+        run_in_cur = cur != 0xFFFFFFFFu && run_base >= itm.tile_begin &&
+                     run_base + kRun <= itm.tile_begin + tiles_of(itm.n);
+        if (!run_in_cur) {
+          if (lane < kRun && run_base + lane < T) {
+            const uint64_t tt = run_base + lane;
+            uint32_t idx = ws.tile_item ? ws.tile_item[tt] : find_item(items, tt);
+            if (idx >= items.count) idx = 0;  // never for a validated table; the range check below rejects it
+            sh.run_idx[lane] = idx;
+            sh.run_item[lane] = item_lite(items, ws, idx);
+          }
+          __syncwarp();
+        }
       }
-      const uint64_t t = run_base + run_pos++;
+      const uint64_t t = run_base + run_pos;
       EncStage& st = sh.st[s];
       if (t >= T) {
         if (lane == 0) {
@@ -356,25 +382,15 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
         cp_async_mbar_arrive_noinc(&sh.full[s]);
         return;
       }
-      if (cur == 0xFFFFFFFFu || t < itm.tile_begin || t >= itm.tile_begin + tiles_of(itm.n)) {
-        if (items.count <= kCachedItems) {
-          // last cached item with tile_begin <= t (empty items own no tile)
-          uint32_t lo = 0, hi = items.count;
-          while (hi - lo > 1) {
-            const uint32_t mid = (lo + hi) >> 1;
-            if (sh.item[mid].tile_begin <= t) lo = mid; else hi = mid;
-          }
-          cur = lo;
-          itm = sh.item[cur];
-        } else {
-          cur = find_item(items, t);
-          itm = item_lite(items, ws, cur);
-        }
+      if (!run_in_cur) {
+        cur = sh.run_idx[run_pos];
+        itm = sh.run_item[run_pos];
       }
-      const uint64_t cur_begin = itm.tile_begin;
-      const uint32_t lt = uint32_t(t - cur_begin);
+      ++run_pos;
+      const bool in_item = t >= itm.tile_begin && t - itm.tile_begin < tiles_of(itm.n);
+      const uint32_t lt = in_item ? uint32_t(t - itm.tile_begin) : 0u;
       const uint64_t g = uint64_t(lt) * kTile;
-      const bool invalid = itm.flags != 0 || g >= itm.n;
+      const bool invalid = itm.flags != 0 || !in_item;
       const uint32_t nt = invalid ? 0u : ((itm.n - g < kTile) ? uint32_t(itm.n - g) : kTile);
       const uint32_t bulk = (nt * 2u) & ~15u;
       const uint32_t tail = nt * 2u - bulk;
@@ -475,111 +491,215 @@ __device__ uint32_t segment_lookback(const unsigned long long* status, uint64_t 
 }
 
 constexpr int kPlaceThreads = kSegChunks;  // one thread per chunk of the segment
+constexpr uint32_t kPlaceWarps = kPlaceThreads / 32;
+constexpr uint64_t kSmallElems = uint64_t(kSegChunks) * kChunk;  // one segment: placed by one warp
+constexpr uint32_t kScatterUnroll = 8;  // escapes per thread per scatter round
 
+// Pad bytes (pk -> sm, sm -> chunk_id, local_pos -> esc_val: each < 4 bytes,
+// by threads r = 0..11 of the caller) and the meta (by r == 0) of item `it`.
+__device__ void finish_item(const EncWs& ws, const sz_item& it, const Layout& l, uint64_t n, uint32_t e,
+                            uint32_t flags, uint32_t r) {
+  if (!flags && r < 12) {
+    uint8_t* p = it.payload;
+    if (r < 4 && l.n_pairs + r < l.off_sm) p[l.n_pairs + r] = 0;
+    if (r >= 4 && r < 8 && l.off_sm + n + (r - 4) < l.off_cid) p[l.off_sm + n + (r - 4)] = 0;
+    if (r >= 8 && l.off_lpos + 2ull * e + (r - 8) < l.off_ev) p[l.off_lpos + 2ull * e + (r - 8)] = 0;
+  }
+  if (r == 0) {
+    if (flags) set_flag(ws.hdr, flags);
+    if (it.meta != nullptr && (reinterpret_cast<uintptr_t>(it.meta) & 15) == 0) {
+      sz_meta m;
+      m.n = n;
+      m.n_pairs = l.n_pairs;
+      m.n_esc = e;
+      m.comp_bytes = l.comp_bytes;
+      m.off_pk = 0;
+      m.off_sm = l.off_sm;
+      m.off_cid = l.off_cid;
+      m.off_lpos = l.off_lpos;
+      m.off_ev = l.off_ev;
+      m.chunk_size = kChunk;
+      m.status = flags;
+      m.coverage = (it.codebook && !(reinterpret_cast<uintptr_t>(it.codebook) & 15)) ? it.codebook->coverage : 0.0;
+      m.reserved1 = 0;
+      *it.meta = m;
+    }
+  }
+}
+
+// Writes the escapes of chunk `c` (cnt of them, the first at global index
+// o) from its staging slot.  Threads r = 0..stride-1 of the caller.
+__device__ __forceinline__ void scatter_chunk(const EncWs& ws, uint8_t* cid_p, uint8_t* lpos_p, uint8_t* ev_p,
+                                              uint64_t slot0, uint32_t c, uint32_t o, uint32_t cnt, uint32_t e,
+                                              uint32_t r, uint32_t stride) {
+  for (uint32_t k = r; k < cnt; k += stride) {
+    const uint64_t gidx = uint64_t(o) + k;
+    if (gidx >= e) break;
+    *reinterpret_cast<uint32_t*>(cid_p + 4 * gidx) = c;
+    *reinterpret_cast<uint16_t*>(lpos_p + 2 * gidx) = ws.lpos[slot0 + k] & uint16_t(kChunk - 1);
+    ev_p[gidx] = ws.ev[slot0 + k];
+  }
+}
+
+// Whole placement of an item of at most one segment by one warp: warp scan
+// of its chunk counts (lane l owns chunks 8l .. 8l+7), then the chunks'
+// escapes in order, each chunk's written by the 32 lanes together.
+__device__ void place_small(const Items& items, const EncWs& ws, uint32_t i, uint32_t lane, uint32_t* off) {
+  const sz_item& it = item_at(items, i);
+  uint32_t flags = ws.item_flags[i];
+  const uint64_t n = (flags & SZ_FLAG_SIZE) ? 0 : it.n;
+  const uint32_t e = ws.item_esc[i];
+  const Layout l = layout_of(n, e);
+  if (!flags && l.comp_bytes > it.capacity) flags |= SZ_FLAG_CAPACITY;
+  finish_item(ws, it, l, n, e, flags, lane);
+  if (flags) return;
+  const uint32_t chunks = uint32_t((n + kChunk - 1) / kChunk);
+  const uint64_t chunk_base = it.tile_begin * kChunksPerTile;
+  uint32_t c8[8], sum = 0;
+#pragma unroll
+  for (uint32_t j = 0; j < 8; ++j) {
+    const uint32_t c = lane * 8 + j;
+    c8[j] = c < chunks ? ws.chunk_cnt[chunk_base + c] : 0u;
+    sum += c8[j];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t v = __shfl_up_sync(FULL, incl, d);
+    if (lane >= uint32_t(d)) incl += v;
+  }
+  uint32_t run = incl - sum;
+#pragma unroll
+  for (uint32_t j = 0; j < 8; ++j) {
+    off[lane * 8 + j] = run;
+    run += c8[j];
+  }
+  if (lane == 31) off[kSegChunks] = run;
+  __syncwarp();
+  uint8_t* const cid_p = it.payload + l.off_cid;
+  uint8_t* const lpos_p = it.payload + l.off_lpos;
+  uint8_t* const ev_p = it.payload + l.off_ev;
+  for (uint32_t c = 0; c < chunks; ++c) {
+    const uint32_t o = off[c], cnt = off[c + 1] - o;
+    if (cnt) scatter_chunk(ws, cid_p, lpos_p, ev_p, (chunk_base + c) * kChunk, c, o, cnt, e, lane, 32);
+  }
+  __syncwarp();  // off is reused by this warp's next item
+}
+
+// Rows of the grid (blockIdx.y) take groups of kPlaceWarps consecutive items.
+// Items of at most one segment are placed by one warp of the row's first
+// block; larger ones by the row's blocks dealt round-robin over them: segments
+// of 256 chunks claimed by ticket (so they start in order), a block scan of
+// the chunk counts and a decoupled lookback across the item's segments.
 __global__ void __launch_bounds__(kPlaceThreads) enc_place(const __grid_constant__ Items items, EncWs ws) {
   __shared__ uint32_t off[kSegChunks + 1];  // exclusive offsets of the segment's chunks, then the total
+  __shared__ uint32_t woff[kPlaceWarps][kSegChunks + 1];
   __shared__ uint32_t wsum[kPlaceThreads / 32];
   __shared__ uint32_t s_seg, s_base;
   const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
   if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
-  for (uint32_t i = blockIdx.y; i < items.count; i += gridDim.y) {
-    const sz_item& it = item_at(items, i);
-    uint32_t flags = ws.item_flags[i];
-    const uint64_t n = (flags & SZ_FLAG_SIZE) ? 0 : it.n;
-    const uint32_t e = ws.item_esc[i];
-    const Layout l = layout_of(n, e);
-    if (!flags && l.comp_bytes > it.capacity) flags |= SZ_FLAG_CAPACITY;
-    if (blockIdx.x == 0) {
-      if (!flags && tid < 12) {
-        // pad bytes: pk -> sm, sm -> chunk_id, local_pos -> esc_val (each < 4 bytes)
-        uint8_t* p = it.payload;
-        if (tid < 4 && l.n_pairs + tid < l.off_sm) p[l.n_pairs + tid] = 0;
-        if (tid >= 4 && tid < 8 && l.off_sm + n + (tid - 4) < l.off_cid) p[l.off_sm + n + (tid - 4)] = 0;
-        if (tid >= 8 && l.off_lpos + 2ull * e + (tid - 8) < l.off_ev) p[l.off_lpos + 2ull * e + (tid - 8)] = 0;
-      }
-      if (tid == 0) {
-        if (flags) set_flag(ws.hdr, flags);
-        if (it.meta != nullptr && (reinterpret_cast<uintptr_t>(it.meta) & 15) == 0) {
-          sz_meta m;
-          m.n = n;
-          m.n_pairs = l.n_pairs;
-          m.n_esc = e;
-          m.comp_bytes = l.comp_bytes;
-          m.off_pk = 0;
-          m.off_sm = l.off_sm;
-          m.off_cid = l.off_cid;
-          m.off_lpos = l.off_lpos;
-          m.off_ev = l.off_ev;
-          m.chunk_size = kChunk;
-          m.status = flags;
-          m.coverage = (it.codebook && !(reinterpret_cast<uintptr_t>(it.codebook) & 15)) ? it.codebook->coverage : 0.0;
-          m.reserved1 = 0;
-          *it.meta = m;
-        }
+  const uint32_t groups = (items.count + kPlaceWarps - 1) / kPlaceWarps;
+  for (uint32_t grp = blockIdx.y; grp < groups; grp += gridDim.y) {
+    {
+      const uint32_t i = grp * kPlaceWarps + warp;
+      if (blockIdx.x == 0 && i < items.count) {
+        const uint64_t n = item_at(items, i).n;
+        if (n <= kSmallElems || (ws.item_flags[i] & SZ_FLAG_SIZE)) place_small(items, ws, i, lane, woff[warp]);
       }
     }
-    if (flags) continue;
-    const uint64_t chunks = (n + kChunk - 1) / kChunk;
-    const uint64_t segs = (chunks + kSegChunks - 1) / kSegChunks;
-    const uint64_t chunk_base = it.tile_begin * kChunksPerTile;
-    uint8_t* const cid_p = it.payload + l.off_cid;
-    uint8_t* const lpos_p = it.payload + l.off_lpos;
-    uint8_t* const ev_p = it.payload + l.off_ev;
-    for (;;) {
-      __syncthreads();  // the previous segment's s_seg / off are no longer read
-      if (tid == 0) s_seg = atomicAdd(ws.seg_ticket + i, 1u);
-      __syncthreads();
-      const uint64_t seg = s_seg;
-      if (seg >= segs) break;
-      // block exclusive scan of the segment's chunk counts
-      const uint64_t c = seg * kSegChunks + tid;
-      const uint32_t cnt = (c < chunks) ? ws.chunk_cnt[chunk_base + c] : 0u;
-      uint32_t incl = cnt;
+    // larger items: the row's blocks are dealt round-robin over its items
+    const uint32_t in_row = min(kPlaceWarps, items.count - grp * kPlaceWarps);
+    const uint32_t R = min(in_row, gridDim.x);
+    const uint32_t rank = blockIdx.x / R;
+    for (uint32_t q = blockIdx.x % R; q < in_row; q += R) {
+      const uint32_t i = grp * kPlaceWarps + q;
+      const sz_item& it = item_at(items, i);
+      uint32_t flags = ws.item_flags[i];
+      if (it.n <= kSmallElems || (flags & SZ_FLAG_SIZE)) continue;
+      const uint64_t n = it.n;
+      const uint32_t e = ws.item_esc[i];
+      const Layout l = layout_of(n, e);
+      if (!flags && l.comp_bytes > it.capacity) flags |= SZ_FLAG_CAPACITY;
+      if (rank == 0) finish_item(ws, it, l, n, e, flags, tid);
+      if (flags) continue;
+      const uint64_t chunks = (n + kChunk - 1) / kChunk;
+      const uint64_t segs = (chunks + kSegChunks - 1) / kSegChunks;
+      const uint64_t chunk_base = it.tile_begin * kChunksPerTile;
+      uint8_t* const cid_p = it.payload + l.off_cid;
+      uint8_t* const lpos_p = it.payload + l.off_lpos;
+      uint8_t* const ev_p = it.payload + l.off_ev;
+      for (;;) {
+        __syncthreads();  // the previous segment's s_seg / off are no longer read
+        if (tid == 0) s_seg = atomicAdd(ws.seg_ticket + i, 1u);
+        __syncthreads();
+        const uint64_t seg = s_seg;
+        if (seg >= segs) break;
+        // block exclusive scan of the segment's chunk counts
+        const uint64_t c = seg * kSegChunks + tid;
+        const uint32_t cnt = (c < chunks) ? ws.chunk_cnt[chunk_base + c] : 0u;
+        uint32_t incl = cnt;
 #pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t o = __shfl_up_sync(FULL, incl, d);
-        if (lane >= uint32_t(d)) incl += o;
-      }
-      if (lane == 31) wsum[warp] = incl;
-      __syncthreads();
-      uint32_t wbase = 0;
-      for (uint32_t w = 0; w < warp; ++w) wbase += wsum[w];
-      off[tid] = wbase + incl - cnt;
-      if (tid == kPlaceThreads - 1) off[kSegChunks] = wbase + incl;
-      __syncthreads();
-      const uint32_t agg = off[kSegChunks];
-      if (warp == 0) {
-        unsigned long long* st = ws.status + it.tile_begin + seg * kSegTiles;
-        uint32_t base = 0;
-        if (seg == 0) {
-          if (lane == 0) st_relaxed_u64(st, kIncl | agg);
-        } else {
-          if (lane == 0) st_relaxed_u64(st, kAgg | agg);
-          bool timed_out = false;
-          base = segment_lookback(ws.status, it.tile_begin, int64_t(seg) - 1, &timed_out);
-          if (lane == 0) {
-            if (timed_out) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
-            st_relaxed_u64(st, kIncl | (base + agg));
+        for (int d = 1; d < 32; d <<= 1) {
+          const uint32_t o = __shfl_up_sync(FULL, incl, d);
+          if (lane >= uint32_t(d)) incl += o;
+        }
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        uint32_t wbase = 0;
+        for (uint32_t w = 0; w < warp; ++w) wbase += wsum[w];
+        off[tid] = wbase + incl - cnt;
+        if (tid == kPlaceThreads - 1) off[kSegChunks] = wbase + incl;
+        __syncthreads();
+        const uint32_t agg = off[kSegChunks];
+        if (warp == 0) {
+          unsigned long long* st = ws.status + it.tile_begin + seg * kSegTiles;
+          uint32_t base = 0;
+          if (seg == 0) {
+            if (lane == 0) st_relaxed_u64(st, kIncl | agg);
+          } else {
+            if (lane == 0) st_relaxed_u64(st, kAgg | agg);
+            bool timed_out = false;
+            base = segment_lookback(ws.status, it.tile_begin, int64_t(seg) - 1, &timed_out);
+            if (lane == 0) {
+              if (timed_out) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+              st_relaxed_u64(st, kIncl | (base + agg));
+            }
           }
+          if (lane == 0) s_base = base;
         }
-        if (lane == 0) s_base = base;
-      }
-      __syncthreads();
-      const uint32_t base = s_base;
-      // scatter: escape j of the segment -> global index base + j
-      for (uint32_t j = tid; j < agg; j += kPlaceThreads) {
-        uint32_t lo = 0, hi = kSegChunks;  // last chunk q with off[q] <= j
-        while (hi - lo > 1) {
-          const uint32_t mid = (lo + hi) >> 1;
-          if (off[mid] <= j) lo = mid; else hi = mid;
-        }
-        const uint32_t k = j - off[lo];
-        const uint64_t slot = (chunk_base + seg * kSegChunks + lo) * kChunk + k;
-        const uint64_t gidx = uint64_t(base) + j;
-        if (gidx < e) {
-          *reinterpret_cast<uint32_t*>(cid_p + 4 * gidx) = uint32_t(seg * kSegChunks + lo);
-          *reinterpret_cast<uint16_t*>(lpos_p + 2 * gidx) = ws.lpos[slot] & uint16_t(kChunk - 1);
-          ev_p[gidx] = ws.ev[slot];
+        __syncthreads();
+        const uint32_t base = s_base;
+        // scatter: escape j of the segment -> global index base + j.  Each
+        // thread takes kScatterUnroll escapes per round and issues all their
+        // staging loads before any store, so a round costs one memory latency.
+        for (uint32_t j0 = 0; j0 < agg; j0 += kScatterUnroll * kPlaceThreads) {
+          uint32_t q[kScatterUnroll], jj[kScatterUnroll];
+          uint16_t lp[kScatterUnroll];
+          uint8_t ev[kScatterUnroll];
+#pragma unroll
+          for (uint32_t u = 0; u < kScatterUnroll; ++u) {
+            const uint32_t j = j0 + u * kPlaceThreads + tid;
+            jj[u] = j;
+            uint32_t lo = 0;  // last chunk lo with off[lo] <= j (off[kSegChunks] = agg > j)
+#pragma unroll
+            for (uint32_t b = kSegChunks / 2; b >= 1; b >>= 1)
+              if (off[lo + b] <= j) lo += b;
+            q[u] = lo;
+            if (j < agg) {
+              const uint64_t slot = (chunk_base + seg * kSegChunks + lo) * kChunk + (j - off[lo]);
+              lp[u] = ws.lpos[slot];
+              ev[u] = ws.ev[slot];
+            }
+          }
+#pragma unroll
+          for (uint32_t u = 0; u < kScatterUnroll; ++u) {
+            const uint64_t gidx = uint64_t(base) + jj[u];
+            if (jj[u] < agg && gidx < e) {
+              *reinterpret_cast<uint32_t*>(cid_p + 4 * gidx) = uint32_t(seg * kSegChunks + q[u]);
+              *reinterpret_cast<uint16_t*>(lpos_p + 2 * gidx) = lp[u] & uint16_t(kChunk - 1);
+              ev_p[gidx] = ev[u];
+            }
+          }
         }
       }
     }
@@ -593,7 +713,10 @@ cudaError_t launch_encode(const Items& items, void* ws_base, cudaStream_t stream
   cudaError_t err = cudaMemsetAsync(ws_base, 0, sizeof(WsHeader), stream);
   if (err != cudaSuccess) return err;
   {
-    const uint64_t work = items.total_tiles > items.count ? items.total_tiles : items.count;
+    // threads for the tiles, or a warp per item when the tile map is written per item
+    uint64_t work = items.total_tiles > items.count ? items.total_tiles : items.count;
+    if (enc_uses_tile_map(items.count) && uint64_t(items.count) * 32 > work)
+      work = uint64_t(items.count) * 32;
     const uint64_t blocks = (work + 255) / 256;
     const unsigned grid = unsigned(blocks < 2048 ? (blocks ? blocks : 1) : 2048);
     enc_prepare<<<grid, 256, 0, stream>>>(items, ws);
@@ -616,12 +739,16 @@ cudaError_t launch_encode(const Items& items, void* ws_base, cudaStream_t stream
     if (err != cudaSuccess) return err;
   }
   {
-    // blockIdx.y = tensor; x covers the average tensor's segments
+    // blockIdx.y = group of kPlaceWarps tensors; x covers the average tensor's
+    // segments times the tensors a row takes in turn (1 when tensors are of
+    // one segment or less: their warps need no other block)
     const uint64_t per_item = items.count ? (items.total_tiles + items.count - 1) / items.count : 0;
-    uint64_t gx = (per_item + kSegTiles - 1) / kSegTiles;
-    if (gx < 1) gx = 1;
+    const uint64_t seg_per_item = (per_item + kSegTiles - 1) / kSegTiles;
+    const uint64_t per_row = items.count < kPlaceWarps ? items.count : kPlaceWarps;
+    uint64_t gx = seg_per_item <= 1 ? 1 : seg_per_item * per_row;
     if (gx > 1024) gx = 1024;
-    const unsigned gy = items.count < 65535u ? items.count : 65535u;
+    const uint64_t groups = (uint64_t(items.count) + kPlaceWarps - 1) / kPlaceWarps;
+    const unsigned gy = unsigned(groups < 65535u ? (groups ? groups : 1) : 65535u);
     enc_place<<<dim3(unsigned(gx), gy), kPlaceThreads, 0, stream>>>(items, ws);
     err = cudaGetLastError();
   }
