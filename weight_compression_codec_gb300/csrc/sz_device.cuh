@@ -115,10 +115,10 @@ __host__ __device__ inline CalWs cal_ws(void* base, uint32_t count) {
 // encode: header | item_flags[count] u32 | item_esc[count] u32 (escape total) |
 //         seg_ticket[count] u32 | status[total_tiles] u64 (segment lookback words,
 //         at each segment's first tile) | chunk_cnt[total_tiles * 8] u16 |
-//         lpos staging[total_tiles * 8192] u16 | ev staging[total_tiles * 8192] u8 |
+//         escape staging[total_tiles * 8192] u32 (chunk-local position | esc_val << 16) |
 //         tile_item[total_tiles] u32 (tables of more than kEncMapItems items)
 // Staging slot of chunk c (global chunk index tile * 8 + chunk) starts at
-// entry c * 1024 and holds the chunk's escapes in element order.
+// entry c * 1024 and holds the chunk's escapes in element order, one word each.
 struct EncWs {
   WsHeader* hdr;
   uint32_t* item_flags;
@@ -126,13 +126,12 @@ struct EncWs {
   uint32_t* seg_ticket;
   unsigned long long* status;
   uint16_t* chunk_cnt;
-  uint16_t* lpos;
-  uint8_t* ev;
+  uint32_t* stage;
   uint32_t* tile_item;
 };
 __host__ __device__ inline uint64_t enc_ws_bytes(uint32_t count, uint64_t tiles) {
   return 256 + 3 * round_up256(uint64_t(count) * 4) + round_up256(tiles * 8) + round_up256(tiles * 16) +
-         round_up256(tiles * kTile * 2) + round_up256(tiles * kTile) + tile_map_bytes(enc_uses_tile_map(count), tiles);
+         round_up256(tiles * kTile * 4) + tile_map_bytes(enc_uses_tile_map(count), tiles);
 }
 __host__ __device__ inline EncWs enc_ws(void* base, uint32_t count, uint64_t tiles) {
   char* p = static_cast<char*>(base);
@@ -149,10 +148,8 @@ __host__ __device__ inline EncWs enc_ws(void* base, uint32_t count, uint64_t til
   p += round_up256(tiles * 8);
   w.chunk_cnt = reinterpret_cast<uint16_t*>(p);
   p += round_up256(tiles * 16);
-  w.lpos = reinterpret_cast<uint16_t*>(p);
-  p += round_up256(tiles * kTile * 2);
-  w.ev = reinterpret_cast<uint8_t*>(p);
-  p += round_up256(tiles * kTile);
+  w.stage = reinterpret_cast<uint32_t*>(p);
+  p += round_up256(tiles * kTile * 4);
   w.tile_item = enc_uses_tile_map(count) ? reinterpret_cast<uint32_t*>(p) : nullptr;
   return w;
 }

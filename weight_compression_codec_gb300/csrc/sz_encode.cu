@@ -142,13 +142,12 @@ __device__ __forceinline__ uint32_t codes4(const uint8_t* lut, uint2 v) {
 }
 
 // Split + pack of chunk `warp` of the tile in `st`, with its escapes compacted
-// in element order into (lslot, eslot).  Each lane handles 4 consecutive
+// in element order into the staging slot `slot`.  Each lane handles 4 consecutive
 // elements per row of 128.  Escape handling is byte-parallel: an enc_lut value
 // >= 16 (a non-zero high nibble) marks an escape, stored in pk as code 0.
 // Returns the chunk's escape count.  FULL_TILE: all 8192 elements exist.
 template <bool FULL_TILE>
-__device__ __forceinline__ uint32_t encode_chunk(const EncStage& st, uint32_t warp, uint32_t lane, uint16_t* lslot,
-                                                 uint8_t* eslot) {
+__device__ __forceinline__ uint32_t encode_chunk(const EncStage& st, uint32_t warp, uint32_t lane, uint32_t* slot) {
   const uint8_t* lut = st.enc_lut;
   const uint32_t nt = st.n_tile;
   const uint64_t g = uint64_t(st.lt) * kTile;
@@ -196,8 +195,7 @@ __device__ __forceinline__ uint32_t encode_chunk(const EncStage& st, uint32_t wa
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         if ((escm >> k) & 1u) {
-          lslot[pos] = uint16_t(row * 128 + lane * 4 + k);
-          eslot[pos] = uint8_t(ex[k]);
+          slot[pos] = uint32_t(row * 128 + lane * 4 + k) | (ex[k] << 16);
           ++pos;
         }
       }
@@ -236,9 +234,8 @@ __device__ __forceinline__ uint32_t warp_prefix(uint32_t c, uint32_t lane, uint3
 
 // Full tile, 8 elements per lane per row of 256 (4 rows per chunk).
 // Same output as encode_chunk<true>: pk/sm of the chunk, its escapes in
-// element order in (lslot, eslot); returns the escape count.
-__device__ __forceinline__ uint32_t encode_chunk8(const EncStage& st, uint32_t warp, uint32_t lane, uint16_t* lslot,
-                                                  uint8_t* eslot) {
+// element order in `slot`; returns the escape count.
+__device__ __forceinline__ uint32_t encode_chunk8(const EncStage& st, uint32_t warp, uint32_t lane, uint32_t* slot) {
   const uint8_t* lut = st.enc_lut;
   const uint64_t g = uint64_t(st.lt) * kTile;
   const uint32_t e0 = warp * kChunk + lane * 8u;
@@ -310,8 +307,7 @@ __device__ __forceinline__ uint32_t encode_chunk8(const EncStage& st, uint32_t w
     uint32_t pos = before[row];
     for (uint32_t m = (lane_esc >> (8 * row)) & 0xFFu; m; m &= m - 1) {
       const uint32_t elem = uint32_t(row) * 256u + lane * 8u + uint32_t(__ffs(m) - 1);  // chunk-local
-      lslot[pos] = uint16_t(elem);
-      eslot[pos] = uint8_t((xc[elem] >> 7) & 0xFFu);
+      slot[pos] = elem | ((uint32_t(xc[elem]) << 9) & 0x00FF0000u);  // position | exponent << 16
       ++pos;
     }
   }
@@ -433,11 +429,10 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
     if (flags & kStageEnd) break;
     if (!(flags & kStageInvalid)) {
       const uint64_t chunk = st.tile * kChunksPerTile + uint32_t(warp);  // global chunk index
-      uint16_t* lslot = ws.lpos + chunk * kChunk;
-      uint8_t* eslot = ws.ev + chunk * kChunk;
+      uint32_t* slot = ws.stage + chunk * kChunk;
       const uint32_t run = (st.n_tile == kTile)
-                               ? encode_chunk8(st, uint32_t(warp), uint32_t(lane), lslot, eslot)
-                               : encode_chunk<false>(st, uint32_t(warp), uint32_t(lane), lslot, eslot);
+                               ? encode_chunk8(st, uint32_t(warp), uint32_t(lane), slot)
+                               : encode_chunk<false>(st, uint32_t(warp), uint32_t(lane), slot);
       if (st.item != acc_item) {
         if (lane == 0 && acc) atomicAdd(ws.item_esc + acc_item, acc);
         acc_item = st.item;
@@ -494,6 +489,7 @@ constexpr int kPlaceThreads = kSegChunks;  // one thread per chunk of the segmen
 constexpr uint32_t kPlaceWarps = kPlaceThreads / 32;
 constexpr uint64_t kSmallElems = uint64_t(kSegChunks) * kChunk;  // one segment: placed by one warp
 constexpr uint32_t kScatterUnroll = 8;  // escapes per thread per scatter round
+constexpr int kPlaceBlocksPerSm = 4;
 
 // Pad bytes (pk -> sm, sm -> chunk_id, local_pos -> esc_val: each < 4 bytes,
 // by threads r = 0..11 of the caller) and the meta (by r == 0) of item `it`.
@@ -536,8 +532,9 @@ __device__ __forceinline__ void scatter_chunk(const EncWs& ws, uint8_t* cid_p, u
     const uint64_t gidx = uint64_t(o) + k;
     if (gidx >= e) break;
     *reinterpret_cast<uint32_t*>(cid_p + 4 * gidx) = c;
-    *reinterpret_cast<uint16_t*>(lpos_p + 2 * gidx) = ws.lpos[slot0 + k] & uint16_t(kChunk - 1);
-    ev_p[gidx] = ws.ev[slot0 + k];
+    const uint32_t v = ws.stage[slot0 + k];
+    *reinterpret_cast<uint16_t*>(lpos_p + 2 * gidx) = uint16_t(v & (kChunk - 1));
+    ev_p[gidx] = uint8_t(v >> 16);
   }
 }
 
@@ -591,7 +588,7 @@ __device__ void place_small(const Items& items, const EncWs& ws, uint32_t i, uin
 // block; larger ones by the row's blocks dealt round-robin over them: segments
 // of 256 chunks claimed by ticket (so they start in order), a block scan of
 // the chunk counts and a decoupled lookback across the item's segments.
-__global__ void __launch_bounds__(kPlaceThreads) enc_place(const __grid_constant__ Items items, EncWs ws) {
+__global__ void __launch_bounds__(kPlaceThreads, kPlaceBlocksPerSm) enc_place(const __grid_constant__ Items items, EncWs ws) {
   __shared__ uint32_t off[kSegChunks + 1];  // exclusive offsets of the segment's chunks, then the total
   __shared__ uint32_t woff[kPlaceWarps][kSegChunks + 1];
   __shared__ uint32_t wsum[kPlaceThreads / 32];
@@ -673,9 +670,7 @@ __global__ void __launch_bounds__(kPlaceThreads) enc_place(const __grid_constant
         // thread takes kScatterUnroll escapes per round and issues all their
         // staging loads before any store, so a round costs one memory latency.
         for (uint32_t j0 = 0; j0 < agg; j0 += kScatterUnroll * kPlaceThreads) {
-          uint32_t q[kScatterUnroll], jj[kScatterUnroll];
-          uint16_t lp[kScatterUnroll];
-          uint8_t ev[kScatterUnroll];
+          uint32_t q[kScatterUnroll], jj[kScatterUnroll], sv[kScatterUnroll];
 #pragma unroll
           for (uint32_t u = 0; u < kScatterUnroll; ++u) {
             const uint32_t j = j0 + u * kPlaceThreads + tid;
@@ -687,8 +682,7 @@ __global__ void __launch_bounds__(kPlaceThreads) enc_place(const __grid_constant
             q[u] = lo;
             if (j < agg) {
               const uint64_t slot = (chunk_base + seg * kSegChunks + lo) * kChunk + (j - off[lo]);
-              lp[u] = ws.lpos[slot];
-              ev[u] = ws.ev[slot];
+              sv[u] = ws.stage[slot];
             }
           }
 #pragma unroll
@@ -696,8 +690,8 @@ __global__ void __launch_bounds__(kPlaceThreads) enc_place(const __grid_constant
             const uint64_t gidx = uint64_t(base) + jj[u];
             if (jj[u] < agg && gidx < e) {
               *reinterpret_cast<uint32_t*>(cid_p + 4 * gidx) = uint32_t(seg * kSegChunks + q[u]);
-              *reinterpret_cast<uint16_t*>(lpos_p + 2 * gidx) = lp[u] & uint16_t(kChunk - 1);
-              ev_p[gidx] = ev[u];
+              *reinterpret_cast<uint16_t*>(lpos_p + 2 * gidx) = uint16_t(sv[u] & (kChunk - 1));
+              ev_p[gidx] = uint8_t(sv[u] >> 16);
             }
           }
         }
@@ -749,6 +743,9 @@ cudaError_t launch_encode(const Items& items, void* ws_base, cudaStream_t stream
     if (gx > 1024) gx = 1024;
     const uint64_t groups = (uint64_t(items.count) + kPlaceWarps - 1) / kPlaceWarps;
     const unsigned gy = unsigned(groups < 65535u ? (groups ? groups : 1) : 65535u);
+    // blocks take segments by ticket: about two waves of resident blocks suffice
+    const uint64_t cap = 2ull * kPlaceBlocksPerSm * uint64_t(dev.num_sms) / gy;
+    if (gx > cap) gx = cap > 0 ? cap : 1;
     enc_place<<<dim3(unsigned(gx), gy), kPlaceThreads, 0, stream>>>(items, ws);
     err = cudaGetLastError();
   }
