@@ -278,30 +278,35 @@ __device__ __forceinline__ uint32_t encode_chunk8(const EncStage& st, uint32_t w
   // Escapes of the chunk, in element order (row, lane, k): one pass per chunk.
   if (__ballot_sync(FULL, lane_esc != 0) == 0) return 0;
   const uint32_t lane_lt = (1u << lane) - 1u;
-  uint32_t c[4], before[4];
-  bool simple = true;  // at most one escape per lane and row: ballots give the prefixes
+  const uint16_t* xc = st.x + warp * kChunk;
+  uint32_t multi = 0;  // non-zero if this lane has two or more escapes in a row
 #pragma unroll
   for (int row = 0; row < 4; ++row) {
-    c[row] = __popc((lane_esc >> (8 * row)) & 0xFFu);
-    simple &= (c[row] <= 1);
+    const uint32_t b = (lane_esc >> (8 * row)) & 0xFFu;
+    multi |= b & (b - 1u);
   }
   uint32_t run = 0;
-  if (__all_sync(FULL, simple)) {
+  if (!__any_sync(FULL, multi != 0)) {
+    // at most one escape per lane and row: a ballot per row places them
 #pragma unroll
     for (int row = 0; row < 4; ++row) {
-      const uint32_t b = __ballot_sync(FULL, c[row] != 0);
-      before[row] = run + __popc(b & lane_lt);
+      const uint32_t byte = (lane_esc >> (8 * row)) & 0xFFu;
+      const uint32_t b = __ballot_sync(FULL, byte != 0);
+      if (byte) {
+        const uint32_t elem = uint32_t(row) * 256u + lane * 8u + uint32_t(__ffs(byte) - 1);  // chunk-local
+        slot[run + __popc(b & lane_lt)] = elem | ((uint32_t(xc[elem]) << 9) & 0x00FF0000u);
+      }
       run += __popc(b);
     }
-  } else {
-#pragma unroll
-    for (int row = 0; row < 4; ++row) {
-      uint32_t total;
-      before[row] = run + warp_prefix(c[row], lane, &total);
-      run += total;
-    }
+    return run;
   }
-  const uint16_t* xc = st.x + warp * kChunk;
+  uint32_t before[4];
+#pragma unroll
+  for (int row = 0; row < 4; ++row) {
+    uint32_t total;
+    before[row] = run + warp_prefix(__popc((lane_esc >> (8 * row)) & 0xFFu), lane, &total);
+    run += total;
+  }
 #pragma unroll
   for (int row = 0; row < 4; ++row) {
     uint32_t pos = before[row];
