@@ -205,11 +205,16 @@ __device__ __forceinline__ uint32_t encode_chunk(const EncStage& st, uint32_t wa
   return run;
 }
 
-// sm bytes of the two BF16 patterns of w at bytes 0 and 2 (bytes 1 and 3 are
-// don't-care): bit 7 of each comes from bit 15 of its pattern.
-__device__ __forceinline__ uint32_t sm_pair_lo(uint32_t w) {
-  const uint32_t s = w >> 8;
-  return (w & 0x007F007Fu) | (s & ~0x007F007Fu);  // one bit-select
+// sm bytes of the four BF16 patterns in (a, b) (element 2k in the low half of
+// a or b), element j in byte j: the low byte of each pattern with bit 7
+// replaced by the pattern's sign.  One permute gathers the low bytes, one
+// permute in sign-replicating mode (selector msb set) turns each pattern's
+// high byte into 0x00 or 0xFF, one bit-select merges them.
+__device__ __forceinline__ uint32_t sm_quad(uint32_t a, uint32_t b) {
+  uint32_t lows, signs;
+  asm("prmt.b32 %0, %1, %2, 0x6420;" : "=r"(lows) : "r"(a), "r"(b));
+  asm("prmt.b32 %0, %1, %2, 0xFDB9;" : "=r"(signs) : "r"(a), "r"(b));
+  return (lows & 0x7F7F7F7Fu) | (signs & 0x80808080u);
 }
 
 // Exclusive warp prefix of per-lane counts `c` (0..8) and the warp total.
@@ -266,8 +271,8 @@ __device__ __forceinline__ uint32_t encode_chunk8(const EncStage& st, uint32_t w
     }
     const uint32_t tlo = clo | (clo >> 4), thi = chi | (chi >> 4);
     *reinterpret_cast<uint32_t*>(pkw + row * 128) = __byte_perm(tlo, thi, 0x6420);
-    const uint32_t s01 = __byte_perm(sm_pair_lo(v.x), sm_pair_lo(v.y), 0x6420);
-    const uint32_t s23 = __byte_perm(sm_pair_lo(v.z), sm_pair_lo(v.w), 0x6420);
+    const uint32_t s01 = sm_quad(v.x, v.y);
+    const uint32_t s23 = sm_quad(v.z, v.w);
     if (sm8) {
       *reinterpret_cast<uint2*>(smw + row * 256) = make_uint2(s01, s23);
     } else {
