@@ -61,6 +61,19 @@ def parse_args():
     return ap.parse_args()
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of the ranks' values (every rank gets it); the job is as
+    slow as its slowest rank."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -369,11 +382,7 @@ def run_ours(args, world, rank, local):
     for w in (ws_cal, ws_enc, ws_dec):
         assert sz.sz_workspace_flags(w.buf) == 0
 
-    ms_step = total_ms / K
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(total_ms / K, world, dev)
 
     # e2e: the same step through the public API with host-resident input and output
     e2e = None
@@ -457,10 +466,7 @@ def run_ours(args, world, rank, local):
         e2e_ms = a.elapsed_time(b) / ke
         assert all(torch.equal(ho, hi) for ho, hi in zip(host_out, host_in)), "e2e round trip"
         meta_bytes = sum(m.numel() for m in host_meta)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, world, dev)
         e2e = {"value": world * raw_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                "h2d_bytes_per_step": raw_bytes, "d2h_bytes_per_step": raw_bytes + meta_bytes,
                "ms_per_step": e2e_ms, "groups": len(groups),
