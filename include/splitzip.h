@@ -159,6 +159,7 @@ SZ_API int sz_items_prepare(sz_item* h_items, uint32_t count, uint64_t* h_total_
 SZ_API size_t sz_calibrate_workspace_bytes(uint32_t count);
 SZ_API size_t sz_encode_workspace_bytes(uint32_t count, uint64_t total_tiles);
 SZ_API size_t sz_decode_workspace_bytes(uint32_t count, uint64_t total_tiles);
+SZ_API size_t sz_calibrate_encode_workspace_bytes(uint32_t count, uint64_t total_tiles);
 
 /* Copies the workspace's SZ_FLAG_* word to *h_flags after synchronising
  * `stream`.  Returns SZ_OK when no bit is set, SZ_ERR_DEVICE otherwise. */
@@ -206,6 +207,29 @@ SZ_API int sz_encode_many(const sz_item* d_items, uint32_t count, uint64_t total
                           void* d_workspace, size_t workspace_bytes, sz_stream stream);
 SZ_API int sz_decode_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles,
                           void* d_workspace, size_t workspace_bytes, sz_stream stream);
+
+/* ------------------------------------------------------------------ calibrate + encode in one pass */
+
+/* Calibration followed by encode ("splitzip_codec.py" calibrate_codebook,
+ * then encode_torch + assemble_payload with the codebook it returns) in one
+ * call that reads each input from its memory once: the tensors are taken in
+ * groups of about 32 MiB, each group counted and, two groups later, encoded
+ * while it is still in L2.  The codebooks, payloads, metas and flags are
+ * those of sz_calibrate (or sz_calibrate_many) followed by sz_encode
+ * (sz_encode_many), byte for byte; the table fields read and written are the
+ * union of the two calls'.  The main kernel is a cooperative launch (all its
+ * CTAs resident at once); SZ_ERR_CUDA if the device cannot run it.
+ * On a GB300 with the input in HBM the two separate calls are faster (the
+ * split-and-pack pass is bound by instruction issue, not by HBM, so the saved
+ * read does not shorten it, and the per-group codebook hand-off costs time);
+ * this call halves the input traffic, which matters where reading the input
+ * is the bottleneck.  The pages calibrate offline, one tensor at a time, and
+ * encode after a host round trip; this fusion has no counterpart there. */
+SZ_API int sz_calibrate_encode(const uint16_t* d_x, uint64_t n, sz_codebook* d_codebook,
+                               uint8_t* d_payload, uint64_t capacity, sz_meta* d_meta,
+                               void* d_workspace, size_t workspace_bytes, sz_stream stream);
+SZ_API int sz_calibrate_encode_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles,
+                                    void* d_workspace, size_t workspace_bytes, sz_stream stream);
 
 /* ------------------------------------------------------------------ decode without a caller workspace */
 

@@ -20,6 +20,8 @@ from .codec import (  # noqa: F401
     read_codebook,
     read_meta,
     sz_calibrate,
+    sz_calibrate_encode,
+    sz_calibrate_encode_many,
     sz_calibrate_many,
     sz_decode,
     sz_decode_many,

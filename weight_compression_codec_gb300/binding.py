@@ -93,6 +93,7 @@ SIGNATURES = {
     "sz_calibrate_workspace_bytes": (_SZ, [_U32]),
     "sz_encode_workspace_bytes": (_SZ, [_U32, _U64]),
     "sz_decode_workspace_bytes": (_SZ, [_U32, _U64]),
+    "sz_calibrate_encode_workspace_bytes": (_SZ, [_U32, _U64]),
     "sz_workspace_flags": (_INT, [_VP, ctypes.POINTER(_U32), _VP]),
     "sz_calibrate": (_INT, [_VP, _U64, _VP, _VP, _SZ, _VP]),
     "sz_encode": (_INT, [_VP, _U64, _VP, _VP, _U64, _VP, _VP, _SZ, _VP]),
@@ -100,6 +101,8 @@ SIGNATURES = {
     "sz_calibrate_many": (_INT, [_VP, _U32, _U64, _VP, _SZ, _VP]),
     "sz_encode_many": (_INT, [_VP, _U32, _U64, _VP, _SZ, _VP]),
     "sz_decode_many": (_INT, [_VP, _U32, _U64, _VP, _SZ, _VP]),
+    "sz_calibrate_encode": (_INT, [_VP, _U64, _VP, _VP, _U64, _VP, _VP, _SZ, _VP]),
+    "sz_calibrate_encode_many": (_INT, [_VP, _U32, _U64, _VP, _SZ, _VP]),
     "sz_set_timing_events": (_INT, [_VP, _VP]),
     "sz_decode_noalloc": (_INT, [_VP, _U64, _VP, _VP, _VP, _U64, _VP, _VP]),
 }

@@ -211,6 +211,29 @@ def sz_encode(x: torch.Tensor, codebook: torch.Tensor, payload: torch.Tensor | N
     return payload, meta
 
 
+def sz_calibrate_encode(x: torch.Tensor, codebook: torch.Tensor | None = None, payload: torch.Tensor | None = None,
+                        meta: torch.Tensor | None = None, workspace=None,
+                        stream=None) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """sz_calibrate then sz_encode in one pass over HBM.  Returns (codebook, payload, meta)."""
+    xb = _bits(x, "x")
+    dev = xb.device
+    n = xb.numel()
+    if codebook is None:
+        codebook = torch.empty(B.CODEBOOK_BYTES, dtype=torch.uint8, device=dev)
+    _u8(codebook, "codebook", B.CODEBOOK_BYTES)
+    if payload is None:
+        payload = torch.empty(max(sz_max_payload_bytes(n), 16), dtype=torch.uint8, device=dev)
+    _u8(payload, "payload")
+    if meta is None:
+        meta = torch.empty(B.META_BYTES, dtype=torch.uint8, device=dev)
+    _u8(meta, "meta", B.META_BYTES)
+    ws = _workspace(workspace, B.lib().sz_calibrate_encode_workspace_bytes(1, sz_tiles(n)), dev)
+    rc = B.lib().sz_calibrate_encode(xb.data_ptr(), n, codebook.data_ptr(), payload.data_ptr(), payload.numel(),
+                                     meta.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(stream))
+    B.check(rc, "sz_calibrate_encode")
+    return codebook, payload, meta
+
+
 def sz_decode(payload: torch.Tensor, meta: torch.Tensor, codebook: torch.Tensor, n: int,
               out: torch.Tensor | None = None, workspace=None, stream=None) -> torch.Tensor:
     """Decode a payload (device tensors) into ``out`` (BF16, n elements)."""
@@ -288,6 +311,15 @@ def sz_encode_many(table: ItemTable, workspace=None, stream=None) -> None:
     rc = B.lib().sz_encode_many(table.ptr(), table.count, table.total_tiles, ws.data_ptr(), ws.numel(),
                                 _stream_handle(stream))
     B.check(rc, "sz_encode_many")
+
+
+def sz_calibrate_encode_many(table: ItemTable, workspace=None, stream=None) -> None:
+    """sz_calibrate_many then sz_encode_many in one pass over HBM (same results)."""
+    dev = table.device.device
+    ws = _workspace(workspace, B.lib().sz_calibrate_encode_workspace_bytes(table.count, table.total_tiles), dev)
+    rc = B.lib().sz_calibrate_encode_many(table.ptr(), table.count, table.total_tiles, ws.data_ptr(), ws.numel(),
+                                          _stream_handle(stream))
+    B.check(rc, "sz_calibrate_encode_many")
 
 
 def sz_decode_many(table: ItemTable, workspace=None, stream=None) -> None:

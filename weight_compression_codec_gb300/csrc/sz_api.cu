@@ -132,6 +132,10 @@ SZ_API size_t sz_decode_workspace_bytes(uint32_t count, uint64_t total_tiles) {
   return size_t(dec_ws_bytes(count, total_tiles));
 }
 
+SZ_API size_t sz_calibrate_encode_workspace_bytes(uint32_t count, uint64_t total_tiles) {
+  return size_t(ce_ws_bytes(count, total_tiles));
+}
+
 SZ_API int sz_workspace_flags(const void* d_workspace, uint32_t* h_flags, sz_stream stream) {
   if (d_workspace == nullptr || h_flags == nullptr) return SZ_ERR_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -234,6 +238,41 @@ SZ_API int sz_decode_many(const sz_item* d_items, uint32_t count, uint64_t total
   if (device_info(&dev) != cudaSuccess) return SZ_ERR_CUDA;
   return from_cuda(launch_decode(table(d_items, count, total_tiles), d_workspace,
                                  reinterpret_cast<cudaStream_t>(stream), dev));
+}
+
+// ---------------------------------------------------------------- calibrate + encode
+
+SZ_API int sz_calibrate_encode(const uint16_t* d_x, uint64_t n, sz_codebook* d_codebook, uint8_t* d_payload,
+                               uint64_t capacity, sz_meta* d_meta, void* d_workspace, size_t workspace_bytes,
+                               sz_stream stream) {
+  if (n > SZ_MAX_ELEMS || d_codebook == nullptr || d_meta == nullptr) return SZ_ERR_ARG;
+  if (n > 0 && (d_x == nullptr || d_payload == nullptr)) return SZ_ERR_ARG;
+  if (!aligned(d_x, 16) || !aligned(d_payload, 16) || !aligned(d_codebook, 16) || !aligned(d_meta, 16))
+    return SZ_ERR_ALIGN;
+  if (layout_of(n, 0).off_cid > capacity) return SZ_ERR_CAPACITY;
+  if (int rc = check_ws(d_workspace, workspace_bytes, ce_ws_bytes(1, tiles_of(n)))) return rc;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return SZ_ERR_CUDA;
+  sz_item one;
+  std::memset(&one, 0, sizeof(one));
+  one.x = d_x;
+  one.payload = d_payload;
+  one.codebook = d_codebook;
+  one.meta = d_meta;
+  one.n = n;
+  one.capacity = capacity;
+  return from_cuda(
+      launch_calibrate_encode(single(one), d_workspace, reinterpret_cast<cudaStream_t>(stream), dev));
+}
+
+SZ_API int sz_calibrate_encode_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles,
+                                    void* d_workspace, size_t workspace_bytes, sz_stream stream) {
+  if (int rc = check_many(d_items, count, total_tiles)) return rc;
+  if (int rc = check_ws(d_workspace, workspace_bytes, ce_ws_bytes(count, total_tiles))) return rc;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return SZ_ERR_CUDA;
+  return from_cuda(launch_calibrate_encode(table(d_items, count, total_tiles), d_workspace,
+                                           reinterpret_cast<cudaStream_t>(stream), dev));
 }
 
 // Timing hook used by the benchmark: events recorded around the next main

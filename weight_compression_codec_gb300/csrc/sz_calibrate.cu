@@ -24,6 +24,7 @@
 //                histogram (one atomic per non-zero bin) and the CTA that adds
 //                a tensor's last tiles hands it over.  The ranking (ties by
 //                ascending exponent value) compares only the non-zero bins.
+#include "sz_count.cuh"
 #include "sz_internal.h"
 
 namespace sz {
@@ -36,7 +37,6 @@ constexpr int kSelectWarp = kCountWarps + 1;
 constexpr int kCalThreads = kCountThreads + 64;  // + producer warp + select warp
 constexpr int kCalStages = 4;
 constexpr int kCalCtasPerSm = 2;
-constexpr uint32_t kItemInvalid = 0x80000000u;
 constexpr uint32_t kStageEnd = 1u, kStageInvalid = 2u;
 constexpr uint32_t kSelectEnd = 0xFFFFFFFFu;  // posted to the select warp when the CTA is done
 constexpr unsigned FULL = 0xFFFFFFFFu;
@@ -60,22 +60,9 @@ struct CalShared {
   uint32_t sel_item[2];
   uint64_t sel_full[2];
   uint64_t sel_empty[2];
-  // select warp scratch
-  unsigned long long key[256];  // non-zero bins in bin order: count << 8 | (255 - bin)
-  alignas(16) uint8_t lut[256];
-  uint8_t dl[16];
+  SelectScratch sel;  // select warp scratch
   int s_last;
 };
-
-__device__ void write_empty_codebook(sz_codebook* cb) {
-  for (int v = 0; v < 256; ++v) cb->enc_lut[v] = kEscape;
-  for (int c = 0; c < 16; ++c) cb->dec_lut[c] = 0;
-  cb->n_top = 0;
-  cb->reserved0 = 0;
-  cb->top_count = 0;
-  cb->n = 0;
-  cb->coverage = 1.0;
-}
 
 __global__ void cal_prepare(const __grid_constant__ Items items, CalWs ws) {
   const uint64_t nthreads = uint64_t(gridDim.x) * blockDim.x;
@@ -99,81 +86,6 @@ __global__ void cal_prepare(const __grid_constant__ Items items, CalWs ws) {
       write_empty_codebook(it.codebook);
     }
   }
-}
-
-// Ranks the 256 bins of histogram h (count desc, value asc) and writes the
-// codebook of `it`; run by one warp, lane l loading bins 8l .. 8l+7.  Only
-// non-zero bins take part: they are compacted in bin order as keys
-// count << 8 | (255 - bin) -- a larger key ranks first, which puts the
-// smaller bin first among equal counts -- and each counts the keys above its
-// own.
-__device__ void select_top16(const sz_item& it, const uint32_t* h, CalShared& sh, uint32_t lane) {
-  const uint4 lo = reinterpret_cast<const uint4*>(h)[2 * lane];
-  const uint4 hi = reinterpret_cast<const uint4*>(h)[2 * lane + 1];
-  const uint32_t c[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-  uint32_t nz = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) nz += c[j] > 0;
-  uint32_t incl = nz;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const uint32_t v = __shfl_up_sync(FULL, incl, d);
-    if (lane >= uint32_t(d)) incl += v;
-  }
-  const uint32_t total = __shfl_sync(FULL, incl, 31);
-  uint32_t pos = incl - nz;
-#pragma unroll
-  for (uint32_t j = 0; j < 8; ++j)
-    if (c[j]) sh.key[pos++] = (static_cast<unsigned long long>(c[j]) << 8) | (255u - (8u * lane + j));
-  reinterpret_cast<uint2*>(sh.lut)[lane] = make_uint2(0x10101010u, 0x10101010u);  // kEscape
-  if (lane < 16) sh.dl[lane] = 0;
-  __syncwarp();
-  for (uint32_t p = lane; p < total; p += 32) {
-    const unsigned long long key = sh.key[p];
-    uint32_t rank = 0;
-    for (uint32_t j = 0; j < total; ++j) rank += sh.key[j] > key;
-    if (rank < 16) {
-      const uint32_t bin = 255u - uint32_t(key & 0xFFu);
-      sh.lut[bin] = uint8_t(rank);
-      sh.dl[rank] = uint8_t(bin);
-    }
-  }
-  __syncwarp();
-  sz_codebook* cb = it.codebook;
-  reinterpret_cast<uint2*>(cb->enc_lut)[lane] = reinterpret_cast<const uint2*>(sh.lut)[lane];
-  const uint32_t n_top = total < 16 ? total : 16u;
-  unsigned long long top = lane < n_top ? h[sh.dl[lane]] : 0ull;
-#pragma unroll
-  for (int d = 16; d > 0; d >>= 1) top += __shfl_xor_sync(FULL, top, d);
-  if (lane < 16) cb->dec_lut[lane] = sh.dl[lane];
-  if (lane == 0) {
-    const uint64_t n = it.n;
-    cb->n_top = n_top;
-    cb->reserved0 = 0;
-    cb->top_count = top;
-    cb->n = n;
-    cb->coverage = n ? double(top) / double(n) : 1.0;
-  }
-  __syncwarp();  // key, lut and dl are reused by the next select
-}
-
-// Index of the item holding global tile `tile` (the last item with
-// tile_begin <= tile; empty items share the next one's tile_begin), found by
-// the 32 lanes of a warp probing 32 entries per round: ceil(log32(count)) + 1
-// dependent loads.  Needs a table validated as consecutive.
-__device__ uint32_t find_item_warp(const Items& items, uint64_t tile, uint32_t lane) {
-  if (items.table == nullptr) return 0;
-  uint32_t lo = 0, hi = items.count;  // table[lo].tile_begin <= tile; the answer is in [lo, hi)
-  while (hi - lo > 32) {
-    const uint32_t step = (hi - lo + 31) / 32;
-    const uint32_t p = lo + lane * step;
-    const uint32_t m = __ballot_sync(FULL, p < hi && items.table[p].tile_begin <= tile);
-    if (m) lo += (31u - __clz(m)) * step;  // m has lane 0 unless the table is not consecutive
-    if (lo + step < hi) hi = lo + step;
-  }
-  const uint32_t p = lo + lane;
-  const uint32_t m = __ballot_sync(FULL, p < hi && items.table[p].tile_begin <= tile);
-  return m ? lo + (31u - __clz(m)) : lo;
 }
 
 __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __grid_constant__ Items items, CalWs ws) {
@@ -301,7 +213,7 @@ __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __g
       }
       const uint32_t item = sh.sel_item[b];
       if (item == kSelectEnd) return;
-      select_top16(item_at(items, item), sh.h[b], sh, lane);
+      select_top16(item_at(items, item), sh.h[b], sh.sel, lane);
       if (lane == 0) mbar_arrive(&sh.sel_empty[b]);
     }
   }
@@ -326,18 +238,7 @@ __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __g
   };
   auto flush = [&]() {
     named_bar_sync(1, kCountThreads);  // every count of the tensor's tiles is in
-    // thread b sums and clears the 32 lane counters of bin b with 16-byte
-    // accesses, rotated so that the 8 threads of a quarter warp touch 8
-    // different bank groups
-    uint4* const row = reinterpret_cast<uint4*>(sh.cnt + tid * 32);
-    uint32_t sum = 0;
-#pragma unroll
-    for (uint32_t k = 0; k < 8; ++k) {
-      const uint32_t q = (k + tid) & 7u;
-      const uint4 v = row[q];
-      sum += v.x + v.y + v.z + v.w;
-      row[q] = make_uint4(0u, 0u, 0u, 0u);
-    }
+    const uint32_t sum = take_bin(sh.cnt, tid);  // thread b sums and clears bin b
     const uint64_t tiles = tiles_of(item_at(items, cur).n);
     if (uint64_t(run) == tiles) {
       // this CTA counted every tile of the tensor: hand the sums over directly
@@ -382,25 +283,7 @@ __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __g
       cur = hd.item;
     }
     if (!(hd.flags & kStageInvalid)) {
-      const uint4* xs = reinterpret_cast<const uint4*>(sh.st[s].x);
-      if (hd.n == kTile) {
-        uint4 v[kTile / 8 / kCountThreads];
-#pragma unroll
-        for (int k = 0; k < kTile / 8 / kCountThreads; ++k) v[k] = xs[tid + k * kCountThreads];
-#pragma unroll
-        for (int k = 0; k < kTile / 8 / kCountThreads; ++k) {
-          const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            atomicAdd(reinterpret_cast<uint32_t*>(col + (w[q] & 0x7F80u)), 1u);
-            atomicAdd(reinterpret_cast<uint32_t*>(col + ((w[q] >> 16) & 0x7F80u)), 1u);
-          }
-        }
-      } else {
-        const uint16_t* xe = sh.st[s].x;
-        for (uint32_t e = tid; e < hd.n; e += kCountThreads)
-          atomicAdd(reinterpret_cast<uint32_t*>(col + (uint32_t(xe[e]) & 0x7F80u)), 1u);
-      }
+      count_tile(sh.st[s].x, hd.n, col, tid);
       ++run;
     }
     __syncwarp();

@@ -129,15 +129,20 @@ struct EncWs {
   uint32_t* stage;
   uint32_t* tile_item;
 };
-__host__ __device__ inline uint64_t enc_ws_bytes(uint32_t count, uint64_t tiles) {
-  return 256 + 3 * round_up256(uint64_t(count) * 4) + round_up256(tiles * 8) + round_up256(tiles * 16) +
-         round_up256(tiles * kTile * 4) + tile_map_bytes(enc_uses_tile_map(count), tiles);
+// Bytes of the encode workspace after its header (map excluded).
+__host__ __device__ inline uint64_t enc_body_bytes(uint32_t count, uint64_t tiles) {
+  return 3 * round_up256(uint64_t(count) * 4) + round_up256(tiles * 8) + round_up256(tiles * 16) +
+         round_up256(tiles * kTile * 4);
 }
-__host__ __device__ inline EncWs enc_ws(void* base, uint32_t count, uint64_t tiles) {
-  char* p = static_cast<char*>(base);
+__host__ __device__ inline uint64_t enc_ws_bytes(uint32_t count, uint64_t tiles) {
+  return 256 + enc_body_bytes(count, tiles) + tile_map_bytes(enc_uses_tile_map(count), tiles);
+}
+// The encode workspace with its header at hdr and its body at `body`.
+__host__ __device__ inline EncWs enc_ws_at(WsHeader* hdr, void* body, uint32_t count, uint64_t tiles,
+                                           uint32_t* tile_item) {
+  char* p = static_cast<char*>(body);
   EncWs w;
-  w.hdr = reinterpret_cast<WsHeader*>(p);
-  p += 256;
+  w.hdr = hdr;
   w.item_flags = reinterpret_cast<uint32_t*>(p);
   p += round_up256(uint64_t(count) * 4);
   w.item_esc = reinterpret_cast<uint32_t*>(p);
@@ -149,8 +154,50 @@ __host__ __device__ inline EncWs enc_ws(void* base, uint32_t count, uint64_t til
   w.chunk_cnt = reinterpret_cast<uint16_t*>(p);
   p += round_up256(tiles * 16);
   w.stage = reinterpret_cast<uint32_t*>(p);
-  p += round_up256(tiles * kTile * 4);
-  w.tile_item = enc_uses_tile_map(count) ? reinterpret_cast<uint32_t*>(p) : nullptr;
+  w.tile_item = tile_item;
+  return w;
+}
+__host__ __device__ inline EncWs enc_ws(void* base, uint32_t count, uint64_t tiles) {
+  char* p = static_cast<char*>(base);
+  uint32_t* map = enc_uses_tile_map(count)
+                      ? reinterpret_cast<uint32_t*>(p + 256 + enc_body_bytes(count, tiles))
+                      : nullptr;
+  return enc_ws_at(reinterpret_cast<WsHeader*>(p), p + 256, count, tiles, map);
+}
+
+// fused calibrate + encode: header | hist[count][256] u32 | done[count] u32 |
+//   ready[count] u32 (codebook written) | group_first[groups + 1] u64 |
+//   group_ticket[groups + 1] u32 | tile_item[tiles] u32 | encode body.
+//   Tensors are taken in groups by first tile, kGroupTiles tiles (32 MiB of
+//   BF16) per group.
+constexpr uint64_t kGroupTiles = 2048;
+__host__ __device__ inline uint64_t ce_groups(uint64_t tiles) { return (tiles + kGroupTiles - 1) / kGroupTiles; }
+struct CeWs {
+  CalWs cal;
+  EncWs enc;
+  uint32_t* ready;
+  uint64_t* group_first;
+  uint32_t* group_ticket;
+};
+__host__ __device__ inline uint64_t ce_ws_bytes(uint32_t count, uint64_t tiles) {
+  return 256 + round_up256(uint64_t(count) * 1024) + 2 * round_up256(uint64_t(count) * 4) +
+         round_up256((ce_groups(tiles) + 1) * 8) + round_up256((ce_groups(tiles) + 1) * 4) + round_up256(tiles * 4) +
+         enc_body_bytes(count, tiles);
+}
+__host__ __device__ inline CeWs ce_ws(void* base, uint32_t count, uint64_t tiles) {
+  char* p = static_cast<char*>(base);
+  CeWs w;
+  w.cal = cal_ws(base, count);  // header, hist, done
+  p += 256 + round_up256(uint64_t(count) * 1024) + round_up256(uint64_t(count) * 4);
+  w.ready = reinterpret_cast<uint32_t*>(p);
+  p += round_up256(uint64_t(count) * 4);
+  w.group_first = reinterpret_cast<uint64_t*>(p);
+  p += round_up256((ce_groups(tiles) + 1) * 8);
+  w.group_ticket = reinterpret_cast<uint32_t*>(p);
+  p += round_up256((ce_groups(tiles) + 1) * 4);
+  uint32_t* map = reinterpret_cast<uint32_t*>(p);
+  p += round_up256(tiles * 4);
+  w.enc = enc_ws_at(w.cal.hdr, p, count, tiles, map);
   return w;
 }
 
@@ -287,6 +334,16 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
 
 __device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Relaxed GPU-scope accesses: coherent single-copy-atomic 64-bit words with

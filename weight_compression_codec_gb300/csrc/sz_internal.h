@@ -20,6 +20,10 @@ cudaError_t device_info(DeviceInfo* info);
 cudaError_t launch_calibrate(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
 cudaError_t launch_encode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
 cudaError_t launch_decode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
+// calibrate + encode in one streaming pass (CeWs workspace), then placement
+cudaError_t launch_calibrate_encode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
+// escape placement, pads and metas after an encode pass (enc_place)
+cudaError_t launch_place(const Items& items, const EncWs& ws, cudaStream_t stream, const DeviceInfo& dev);
 
 // Optional timing hook: when set (non-null), launchers record `before` just
 // before and `after` just after their main kernel on the launch stream.
