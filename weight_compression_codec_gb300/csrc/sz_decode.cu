@@ -84,33 +84,31 @@ __device__ uint32_t item_problems(const Items& items, uint32_t i) {
   return bad;
 }
 
-// First k in [0, e) with cid[k] >= target (e if none), found by the 16 lanes
-// of a half warp (hl = lane within the half, half_mask = its lanes): each
-// round probes 16 evenly spaced positions, so the search takes
-// ceil(log16(e)) + 1 dependent loads instead of log2(e).
-__device__ uint32_t lower_bound_cid16(const int32_t* cid, uint32_t e, uint32_t target, uint32_t hl,
-                                      uint32_t half_mask) {
+// First k in [0, e) with cid[k] >= target (e if none), found by the 32 lanes
+// of a warp: each round probes 32 evenly spaced positions, so the search
+// takes ceil(log32(e)) + 1 dependent loads instead of log2(e).
+__device__ uint32_t lower_bound_cid32(const int32_t* cid, uint32_t e, uint32_t target, uint32_t lane) {
   uint32_t lo = 0, hi = e;  // the answer lies in [lo, hi]
-  while (hi - lo > 16) {
-    const uint32_t step = (hi - lo + 15) / 16;
-    uint32_t p = lo + (hl + 1) * step - 1;
+  while (hi - lo > 32) {
+    const uint32_t step = (hi - lo + 31) / 32;
+    uint32_t p = lo + (lane + 1) * step - 1;
     if (p > hi - 1) p = hi - 1;
-    const uint32_t c = __popc(__ballot_sync(half_mask, uint32_t(__ldg(cid + p)) < target));
+    const uint32_t c = __popc(__ballot_sync(0xFFFFFFFFu, uint32_t(__ldg(cid + p)) < target));
     if (c == 0) {
       hi = lo + step - 1;  // the first probe already holds cid >= target
     } else {
       uint32_t last_less = lo + c * step - 1;
       if (last_less > hi - 1) last_less = hi - 1;
-      if (c < 16) {
+      if (c < 32) {
         uint32_t first_ge = lo + (c + 1) * step - 1;
         if (first_ge < hi) hi = first_ge;
       }
       lo = last_less + 1;
     }
   }
-  const uint32_t p = lo + hl;
+  const uint32_t p = lo + lane;
   const bool less = (p < hi) && uint32_t(__ldg(cid + p)) < target;
-  return lo + __popc(__ballot_sync(half_mask, less));
+  return lo + __popc(__ballot_sync(0xFFFFFFFFu, less));
 }
 
 constexpr int kPrepWarps = 8;
@@ -118,14 +116,14 @@ constexpr uint64_t kSmallTiles = 32;  // items of at most one 32-tile group are 
 constexpr uint32_t kDenseGroup = 4096;  // escapes in a 32-tile group above which tiles are searched, not counted
 
 // Escape ranges of the 32-tile group of item i starting at its tile ta (lane
-// l <-> tile ta + l), and the group's tile -> item map entries.  The two half
-// warps bracket the group's escapes with 16-ary searches for the first escape
-// of tile ta and of tile ta + 32; the warp then reads the bracketed chunk_id
-// slice once, coalesced, counting escapes per tile in shared memory, and a
-// warp scan of the counts gives every tile's [k0, k1).  A group with more
-// than kDenseGroup escapes is not read whole: each lane binary-searches its
-// own tile's first escape instead.  Writes outside the table's tiles are
-// dropped.
+// l <-> tile ta + l), and the group's tile -> item map entries.  A 32-ary
+// warp search finds the group's first escape; then, unless the group holds
+// more than kDenseGroup escapes, the warp reads the chunk_id stream from
+// there, 512 entries per round, counting escapes per tile in shared memory
+// until it reaches the next group, and a warp scan of the counts gives every
+// tile's [k0, k1).  A denser group is not read whole: a second search finds
+// its end and each lane binary-searches its own tile's first escape.  Writes
+// outside the table's tiles are dropped.
 __device__ void prepare_group(const Items& items, const DecWs& ws, uint32_t i, const sz_item& it, uint64_t tiles,
                               bool bad, uint64_t ta, uint32_t lane, uint32_t* counts) {
   const uint32_t ng = (tiles - ta < 32) ? uint32_t(tiles - ta) : 32u;
@@ -133,15 +131,13 @@ __device__ void prepare_group(const Items& items, const DecWs& ws, uint32_t i, c
   if (!bad) {
     const uint32_t e = uint32_t(it.meta->n_esc);
     const int32_t* cid = reinterpret_cast<const int32_t*>(it.payload + it.meta->off_cid);
-    const uint32_t half_mask = lane < 16 ? 0x0000FFFFu : 0xFFFF0000u;
-    const uint32_t target = uint32_t(ta) * kChunksPerTile + (lane < 16 ? 0u : 32u * kChunksPerTile);
-    const uint32_t k = lower_bound_cid16(cid, e, target, lane & 15u, half_mask);
-    const uint32_t k_lo = __shfl_sync(0xFFFFFFFFu, k, 0);
-    const uint32_t k_hi = __shfl_sync(0xFFFFFFFFu, k, 16);
-    if (k_hi - k_lo > kDenseGroup) {
-      // many escapes: each lane finds the first escape of its own tile by a
-      // binary search of the group's slice (log2 of its length in loads)
-      const uint32_t target_l = (uint32_t(ta) + lane) * kChunksPerTile;
+    const uint32_t first = uint32_t(ta) * kChunksPerTile;   // first chunk of the group
+    const uint32_t limit = first + 32u * kChunksPerTile;    // first chunk of the next group
+    const uint32_t k_lo = lower_bound_cid32(cid, e, first, lane);
+    const bool dense = k_lo + kDenseGroup < e && uint32_t(__ldg(cid + k_lo + kDenseGroup)) < limit;
+    if (dense) {
+      const uint32_t k_hi = lower_bound_cid32(cid, e, limit, lane);
+      const uint32_t target_l = first + lane * kChunksPerTile;
       uint32_t lo = k_lo, len = k_hi - k_lo;
       while (len > 0) {
         const uint32_t half = len >> 1;
@@ -157,19 +153,21 @@ __device__ void prepare_group(const Items& items, const DecWs& ws, uint32_t i, c
     } else {
       counts[lane] = 0;
       __syncwarp();
-      // 8 independent loads per lane per round, then the shared-memory counts
-      for (uint32_t kb = k_lo; kb < k_hi; kb += 32 * 8) {
-        uint32_t c8[8];
+      for (uint32_t kb = k_lo; kb < e; kb += 32 * 16) {
+        uint32_t c16[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 16; ++u) {
           const uint32_t kk = kb + lane + 32u * u;
-          c8[u] = kk < k_hi ? uint32_t(__ldg(cid + kk)) : 0xFFFFFFFFu;
+          c16[u] = kk < e ? uint32_t(__ldg(cid + kk)) : 0xFFFFFFFFu;
         }
+        bool past = false;  // this lane read a chunk_id of a later group (or the stream's end)
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint32_t rel = (c8[u] >> 3) - uint32_t(ta);  // tile within the group
-          if (c8[u] != 0xFFFFFFFFu && rel < 32u) atomicAdd(&counts[rel], 1u);
+        for (int u = 0; u < 16; ++u) {
+          const uint32_t rel = (c16[u] >> 3) - uint32_t(ta);  // tile within the group
+          if (c16[u] != 0xFFFFFFFFu && rel < 32u) atomicAdd(&counts[rel], 1u);
+          past |= c16[u] >= limit;
         }
+        if (__any_sync(0xFFFFFFFFu, past)) break;
       }
       __syncwarp();
       const uint32_t c = counts[lane];
@@ -193,9 +191,9 @@ __device__ void prepare_group(const Items& items, const DecWs& ws, uint32_t i, c
 // Validation and escape ranges per item.  Rows of the grid (blockIdx.y) take
 // groups of kPrepWarps consecutive items: items of at most 32 tiles are
 // prepared by one warp of the row's first block, larger ones by the row's
-// blocks dealt round-robin over them (warp per 32-tile group).
+// blocks dealt round-robin over them (warp per 32-tile group, each warp
+// validating the item for itself).
 __global__ void __launch_bounds__(kPrepWarps * 32) dec_prepare(const __grid_constant__ Items items, DecWs ws) {
-  __shared__ uint32_t s_bad;
   __shared__ uint32_t counts[kPrepWarps][32];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t warp = threadIdx.x >> 5;
@@ -229,16 +227,17 @@ __global__ void __launch_bounds__(kPrepWarps * 32) dec_prepare(const __grid_cons
       const uint32_t i = grp * kPrepWarps + q;
       const sz_item& it = item_at(items, i);
       if (it.n <= kSmallTiles * kTile) continue;
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        s_bad = item_problems(items, i);
-        if (rank == 0) {
-          ws.item_flags[i] = s_bad;
-          if (s_bad) set_flag(ws.hdr, s_bad);
+      // every warp validates the item itself (no block barrier); the item's
+      // first block publishes the result
+      uint32_t bad = 0;
+      if (lane == 0) {
+        bad = item_problems(items, i);
+        if (rank == 0 && warp == 0) {
+          ws.item_flags[i] = bad;
+          if (bad) set_flag(ws.hdr, bad);
         }
       }
-      __syncthreads();
-      const uint32_t bad = s_bad;
+      bad = __shfl_sync(0xFFFFFFFFu, bad, 0);
       if (bad & SZ_FLAG_ITEMS) continue;
       const uint64_t tiles = (it.n > SZ_MAX_ELEMS) ? 0 : tiles_of(it.n);
       for (uint64_t ta = (uint64_t(rank) * kPrepWarps + warp) * 32; ta < tiles;
