@@ -96,6 +96,10 @@ typedef enum sz_status {
 #define SZ_FLAG_ITEMS 0x20u       /* item table: tile_begin chain inconsistent            */
 #define SZ_FLAG_SIZE 0x40u        /* an item's n is out of range for the call             */
 
+/* sz_meta.status bit that is not an error: the tensor was left uncompressed
+ * by the coverage gate of sz_encode_gated_many (its payload holds nothing). */
+#define SZ_META_GATED 0x100u
+
 /* Per-tensor codebook ("splitzip_codec.py" SplitZipCodebook and
  * calibrate_codebook).  304 bytes, 16-byte aligned in device memory. */
 typedef struct sz_codebook {
@@ -130,6 +134,20 @@ typedef struct sz_item {
   uint64_t capacity;       /* bytes available at payload                              */
   uint64_t tile_begin;     /* *_many only: sum of sz_tiles(n) of the items before it  */
 } sz_item;
+
+/* Build report of sz_encode_gated_many (the shard-cache builder's report of
+ * "docs/developer/splitzip.md": tensors encoded, tensors skipped for
+ * coverage, payload ratio).  64 bytes, in device memory. */
+typedef struct sz_gate_report {
+  uint64_t tensors_encoded;    /* coverage >= the gate, encoded                        */
+  uint64_t tensors_gated;      /* coverage below the gate, left uncompressed           */
+  uint64_t raw_bytes_encoded;  /* 2 n summed over the encoded tensors                  */
+  uint64_t payload_bytes;      /* comp_bytes summed over the encoded tensors           */
+  uint64_t raw_bytes_gated;    /* 2 n summed over the gated tensors                    */
+  uint64_t tensors_expanded;   /* encoded tensors whose payload exceeds 2 n            */
+  uint64_t escapes;            /* n_esc summed over the encoded tensors                */
+  uint64_t tensors_failed;     /* tensors with an error flag (neither encoded nor gated) */
+} sz_gate_report;
 
 /* ------------------------------------------------------------------ host-only queries */
 
@@ -186,7 +204,9 @@ SZ_API int sz_encode(const uint16_t* d_x, uint64_t n, const sz_codebook* d_codeb
  * *d_meta (payload_bytes readable bytes at d_payload) with d_codebook->dec_lut
  * into d_out[0..n).  n must equal d_meta->n; a meta that disagrees with the
  * layout or with payload_bytes sets SZ_FLAG_META and leaves d_out unwritten;
- * an escape outside the tensor sets SZ_FLAG_ESCAPE and is skipped. */
+ * an escape outside the tensor sets SZ_FLAG_ESCAPE and is skipped.  A meta
+ * with SZ_META_GATED describes a tensor kept raw: nothing is written for it
+ * and no flag is raised (the same holds in sz_decode_many). */
 SZ_API int sz_decode(const uint8_t* d_payload, uint64_t payload_bytes, const sz_meta* d_meta,
                      const sz_codebook* d_codebook, uint16_t* d_out, uint64_t n,
                      void* d_workspace, size_t workspace_bytes, sz_stream stream);
@@ -207,6 +227,21 @@ SZ_API int sz_encode_many(const sz_item* d_items, uint32_t count, uint64_t total
                           void* d_workspace, size_t workspace_bytes, sz_stream stream);
 SZ_API int sz_decode_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles,
                           void* d_workspace, size_t workspace_bytes, sz_stream stream);
+
+/* ------------------------------------------------------------------ coverage gate */
+
+/* sz_encode_many with the coverage gate of the pages' shard-cache builder
+ * ("docs/developer/splitzip.md": tensors whose Top-16 exponent coverage is
+ * below 0.99 are left uncompressed, so the worst case is parity; broad
+ * exponent distributions would expand).  A tensor whose codebook coverage is
+ * below min_coverage is not encoded: its meta gets status SZ_META_GATED, n,
+ * its coverage and zeros elsewhere, and no payload byte is written; the
+ * others are encoded exactly as by sz_encode_many.  *d_report (device, 16-byte
+ * aligned) receives the build report of the call.  min_coverage < 0 gates
+ * nothing.  Workspace: sz_encode_workspace_bytes. */
+SZ_API int sz_encode_gated_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles,
+                                double min_coverage, sz_gate_report* d_report,
+                                void* d_workspace, size_t workspace_bytes, sz_stream stream);
 
 /* ------------------------------------------------------------------ calibrate + encode in one pass */
 

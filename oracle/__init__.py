@@ -232,3 +232,35 @@ def to_p1_nibble_order(payload, meta: Meta, lib=None) -> np.ndarray:
         cm = _meta_to_c(meta)
         lib.szo_to_p1_nibble_order(_ptr(p, ctypes.c_uint8), ctypes.byref(cm))
     return p
+
+
+# ---------------------------------------------------------------------------- coverage gate
+# "docs/developer/splitzip.md" (the shard-cache builder): tensors whose Top-16
+# exponent coverage falls below 0.99 are left uncompressed, so the worst case
+# is parity; the builder reports the tensors encoded and skipped for coverage
+# and the payload ratio.  Reading: "below" is strict (coverage == gate is
+# encoded); a negative gate gates nothing; a tensor that still expands is
+# counted, not dropped.
+
+
+def gated(coverage: float, min_coverage: float) -> bool:
+    """True if the coverage gate leaves the tensor uncompressed."""
+    return min_coverage >= 0.0 and coverage < min_coverage
+
+
+def gate_report(ns, coverages, metas, min_coverage: float) -> dict:
+    """Build report over tensors of sizes ns, codebook coverages and the metas
+    their plain encode gives (meta i is used only when tensor i is encoded)."""
+    r = dict(tensors_encoded=0, tensors_gated=0, raw_bytes_encoded=0, payload_bytes=0, raw_bytes_gated=0,
+             tensors_expanded=0, escapes=0, tensors_failed=0)
+    for n, cov, m in zip(ns, coverages, metas):
+        if gated(cov, min_coverage):
+            r["tensors_gated"] += 1
+            r["raw_bytes_gated"] += 2 * n
+        else:
+            r["tensors_encoded"] += 1
+            r["raw_bytes_encoded"] += 2 * n
+            r["payload_bytes"] += m.comp_bytes
+            r["tensors_expanded"] += int(m.comp_bytes > 2 * n)
+            r["escapes"] += m.n_esc
+    return r

@@ -285,3 +285,31 @@ def test_decode_rejects_bad_meta(oracle):
     broken[m.off_lpos:m.off_lpos + 2] = np.frombuffer(np.uint16(1024).tobytes(), np.uint8)
     with pytest.raises(ValueError):
         oracle.decode(broken, m, cb.dec_lut)
+
+
+# ---------------------------------------------------------------------------- coverage gate
+
+
+def test_gate_is_strictly_below_and_negative_gates_nothing(oracle):
+    assert oracle.gated(0.98, 0.99) and not oracle.gated(0.99, 0.99) and not oracle.gated(1.0, 0.99)
+    assert not oracle.gated(0.0, -1.0) and oracle.gated(0.0, 0.5)
+
+
+def test_gate_report_by_hand(oracle):
+    # three tensors: a Gaussian one (coverage ~1), the all-bit-patterns tensor
+    # (coverage 1/16, payload 4.03 x raw) and an empty one (coverage 1.0)
+    from weight_compression_codec_gb300 import inputs
+
+    xs = [inputs.gaussian(10_000, 0.02, seed=3), inputs.all_bit_patterns(), np.zeros(0, np.uint16)]
+    cbs = [oracle.calibrate(x) for x in xs]
+    metas = [oracle.encode(x, cb)[1] for x, cb in zip(xs, cbs)]
+    assert cbs[1].coverage == 0.0625 and metas[1].comp_bytes == 528_384
+    r = oracle.gate_report([x.size for x in xs], [cb.coverage for cb in cbs], metas, 0.99)
+    assert r["tensors_gated"] == 1 and r["raw_bytes_gated"] == 2 * 65_536
+    assert r["tensors_encoded"] == 2 and r["raw_bytes_encoded"] == 20_000
+    assert r["payload_bytes"] == metas[0].comp_bytes + 0 and r["escapes"] == metas[0].n_esc
+    assert r["tensors_expanded"] == 0
+    # without the gate the all-bit-patterns tensor is encoded and expands
+    r = oracle.gate_report([x.size for x in xs], [cb.coverage for cb in cbs], metas, -1.0)
+    assert r["tensors_gated"] == 0 and r["tensors_expanded"] == 1 and r["escapes"] == metas[0].n_esc + 61_440
+    assert r["payload_bytes"] == metas[0].comp_bytes + 528_384

@@ -18,6 +18,7 @@ from .codec import (  # noqa: F401
     meta_from_bytes,
     meta_to_bytes,
     read_codebook,
+    read_gate_report,
     read_meta,
     sz_calibrate,
     sz_calibrate_encode,
@@ -26,6 +27,7 @@ from .codec import (  # noqa: F401
     sz_decode,
     sz_decode_many,
     sz_encode,
+    sz_encode_gated_many,
     sz_encode_many,
     sz_layout,
     sz_max_payload_bytes,

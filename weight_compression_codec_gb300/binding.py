@@ -27,6 +27,7 @@ SZ_FLAG_TIMEOUT = 0x08
 SZ_FLAG_ALIGN = 0x10
 SZ_FLAG_ITEMS = 0x20
 SZ_FLAG_SIZE = 0x40
+SZ_META_GATED = 0x100  # sz_meta.status: kept raw by the coverage gate (not an error)
 
 
 class SzCodebook(ctypes.Structure):
@@ -76,8 +77,15 @@ assert ctypes.sizeof(SzCodebook) == 304
 assert ctypes.sizeof(SzMeta) == 96
 assert ctypes.sizeof(SzItem) == 64
 
+class SzGateReport(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_uint64) for name in (
+        "tensors_encoded", "tensors_gated", "raw_bytes_encoded", "payload_bytes", "raw_bytes_gated",
+        "tensors_expanded", "escapes", "tensors_failed")]
+
+
 CODEBOOK_BYTES = 304
 META_BYTES = 96
+GATE_REPORT_BYTES = 64
 ITEM_BYTES = 64
 
 # Every symbol of include/splitzip.h with its ctypes signature.
@@ -103,6 +111,7 @@ SIGNATURES = {
     "sz_decode_many": (_INT, [_VP, _U32, _U64, _VP, _SZ, _VP]),
     "sz_calibrate_encode": (_INT, [_VP, _U64, _VP, _VP, _U64, _VP, _VP, _SZ, _VP]),
     "sz_calibrate_encode_many": (_INT, [_VP, _U32, _U64, _VP, _SZ, _VP]),
+    "sz_encode_gated_many": (_INT, [_VP, _U32, _U64, ctypes.c_double, _VP, _VP, _SZ, _VP]),
     "sz_set_timing_events": (_INT, [_VP, _VP]),
     "sz_decode_noalloc": (_INT, [_VP, _U64, _VP, _VP, _VP, _U64, _VP, _VP]),
 }

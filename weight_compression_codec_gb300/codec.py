@@ -313,6 +313,27 @@ def sz_encode_many(table: ItemTable, workspace=None, stream=None) -> None:
     B.check(rc, "sz_encode_many")
 
 
+def sz_encode_gated_many(table: ItemTable, min_coverage: float, report: torch.Tensor | None = None, workspace=None,
+                         stream=None) -> torch.Tensor:
+    """sz_encode_many with the coverage gate: tensors below min_coverage are left
+    uncompressed (meta status SZ_META_GATED).  Returns the build report (64-byte
+    device tensor; read_gate_report turns it into a dict)."""
+    dev = table.device.device
+    if report is None:
+        report = torch.empty(B.GATE_REPORT_BYTES, dtype=torch.uint8, device=dev)
+    _u8(report, "report", B.GATE_REPORT_BYTES)
+    ws = _workspace(workspace, B.lib().sz_encode_workspace_bytes(table.count, table.total_tiles), dev)
+    rc = B.lib().sz_encode_gated_many(table.ptr(), table.count, table.total_tiles, float(min_coverage),
+                                      report.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(stream))
+    B.check(rc, "sz_encode_gated_many")
+    return report
+
+
+def read_gate_report(report: torch.Tensor) -> dict:
+    r = B.SzGateReport.from_buffer_copy(bytes(report.reshape(-1)[:B.GATE_REPORT_BYTES].cpu().numpy().tobytes()))
+    return {name: int(getattr(r, name)) for name, _ in B.SzGateReport._fields_}
+
+
 def sz_calibrate_encode_many(table: ItemTable, workspace=None, stream=None) -> None:
     """sz_calibrate_many then sz_encode_many in one pass over HBM (same results)."""
     dev = table.device.device

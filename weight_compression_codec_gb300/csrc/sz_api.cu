@@ -240,6 +240,21 @@ SZ_API int sz_decode_many(const sz_item* d_items, uint32_t count, uint64_t total
                                  reinterpret_cast<cudaStream_t>(stream), dev));
 }
 
+// ---------------------------------------------------------------- coverage gate
+
+SZ_API int sz_encode_gated_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles, double min_coverage,
+                                sz_gate_report* d_report, void* d_workspace, size_t workspace_bytes,
+                                sz_stream stream) {
+  if (int rc = check_many(d_items, count, total_tiles)) return rc;
+  if (d_report == nullptr || min_coverage != min_coverage) return SZ_ERR_ARG;  // NaN gate
+  if (!aligned(d_report, 16)) return SZ_ERR_ALIGN;
+  if (int rc = check_ws(d_workspace, workspace_bytes, enc_ws_bytes(count, total_tiles))) return rc;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return SZ_ERR_CUDA;
+  return from_cuda(launch_encode(table(d_items, count, total_tiles), d_workspace,
+                                 reinterpret_cast<cudaStream_t>(stream), dev, min_coverage, d_report));
+}
+
 // ---------------------------------------------------------------- calibrate + encode
 
 SZ_API int sz_calibrate_encode(const uint16_t* d_x, uint64_t n, sz_codebook* d_codebook, uint8_t* d_payload,

@@ -68,19 +68,26 @@ __device__ bool meta_ok(const sz_item& it, uint64_t n_esc_limit) {
          l.comp_bytes <= it.capacity;
 }
 
+// Internal item flag (never in the header word): a tensor kept raw by the
+// coverage gate (meta status SZ_META_GATED), skipped without an error.
+constexpr uint32_t kItemGated = 0x80000000u;
+
 __device__ uint32_t item_problems(const Items& items, uint32_t i) {
   const sz_item& it = item_at(items, i);
   uint32_t bad = 0;
   if (it.n > SZ_MAX_ELEMS) return SZ_FLAG_SIZE;
-  if (it.codebook == nullptr || (reinterpret_cast<uintptr_t>(it.codebook) & 15)) bad |= SZ_FLAG_ALIGN;
-  if (it.n > 0 && (it.out == nullptr || (reinterpret_cast<uintptr_t>(it.out) & 15))) bad |= SZ_FLAG_ALIGN;
-  if (it.n > 0 && (it.payload == nullptr || (reinterpret_cast<uintptr_t>(it.payload) & 15))) bad |= SZ_FLAG_ALIGN;
-  if (!meta_ok(it, SZ_MAX_ELEMS)) bad |= SZ_FLAG_META;
   if (items.table) {
     const uint64_t expect = (i == 0) ? 0 : items.table[i - 1].tile_begin + tiles_of(items.table[i - 1].n);
     if (it.tile_begin != expect) bad |= SZ_FLAG_ITEMS;
     if (i + 1 == items.count && it.tile_begin + tiles_of(it.n) != items.total_tiles) bad |= SZ_FLAG_ITEMS;
   }
+  const sz_meta* mp = it.meta;
+  if (mp != nullptr && !(reinterpret_cast<uintptr_t>(mp) & 15) && (mp->status & SZ_META_GATED))
+    return bad | kItemGated;  // nothing stored, nothing to write
+  if (it.codebook == nullptr || (reinterpret_cast<uintptr_t>(it.codebook) & 15)) bad |= SZ_FLAG_ALIGN;
+  if (it.n > 0 && (it.out == nullptr || (reinterpret_cast<uintptr_t>(it.out) & 15))) bad |= SZ_FLAG_ALIGN;
+  if (it.n > 0 && (it.payload == nullptr || (reinterpret_cast<uintptr_t>(it.payload) & 15))) bad |= SZ_FLAG_ALIGN;
+  if (!meta_ok(it, SZ_MAX_ELEMS)) bad |= SZ_FLAG_META;
   return bad;
 }
 
@@ -208,7 +215,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32) dec_prepare(const __grid_cons
           if (lane == 0) {
             bad = item_problems(items, i);
             ws.item_flags[i] = bad;
-            if (bad) set_flag(ws.hdr, bad);
+            if (bad & ~kItemGated) set_flag(ws.hdr, bad & ~kItemGated);
           }
           bad = __shfl_sync(0xFFFFFFFFu, bad, 0);
           const uint64_t tiles = tiles_of(it.n);
@@ -234,7 +241,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32) dec_prepare(const __grid_cons
         bad = item_problems(items, i);
         if (rank == 0 && warp == 0) {
           ws.item_flags[i] = bad;
-          if (bad) set_flag(ws.hdr, bad);
+          if (bad & ~kItemGated) set_flag(ws.hdr, bad & ~kItemGated);
         }
       }
       bad = __shfl_sync(0xFFFFFFFFu, bad, 0);

@@ -128,6 +128,8 @@ struct EncWs {
   uint16_t* chunk_cnt;
   uint32_t* stage;
   uint32_t* tile_item;
+  double gate;              // coverage gate (< 0: none)
+  sz_gate_report* report;   // build report of a gated call, or nullptr
 };
 // Bytes of the encode workspace after its header (map excluded).
 __host__ __device__ inline uint64_t enc_body_bytes(uint32_t count, uint64_t tiles) {
@@ -155,6 +157,8 @@ __host__ __device__ inline EncWs enc_ws_at(WsHeader* hdr, void* body, uint32_t c
   p += round_up256(tiles * 16);
   w.stage = reinterpret_cast<uint32_t*>(p);
   w.tile_item = tile_item;
+  w.gate = -1.0;
+  w.report = nullptr;
   return w;
 }
 __host__ __device__ inline EncWs enc_ws(void* base, uint32_t count, uint64_t tiles) {

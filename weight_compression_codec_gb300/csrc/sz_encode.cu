@@ -102,11 +102,14 @@ __global__ void enc_prepare(const __grid_constant__ Items items, EncWs ws) {
       if (it.tile_begin != expect) bad |= SZ_FLAG_ITEMS;
       if (i + 1 == items.count && it.tile_begin + tiles_of(it.n) != items.total_tiles) bad |= SZ_FLAG_ITEMS;
     }
+    if (bad) set_flag(ws.hdr, bad);
+    // the coverage gate: a tensor below it is left uncompressed (not an error)
+    else if (ws.gate >= 0.0 && it.codebook->coverage < ws.gate) bad = SZ_META_GATED;
     ws.item_flags[i] = bad;
     ws.item_esc[i] = 0;
     ws.seg_ticket[i] = 0;
-    if (bad) set_flag(ws.hdr, bad);
   }
+  if (ws.report != nullptr && gtid == 0) *ws.report = sz_gate_report{};
   if (ws.tile_item != nullptr) {
     // one warp per item writes the item's tile -> item map entries (clipped to the table's tiles)
     const uint32_t lane = threadIdx.x & 31u;
@@ -298,7 +301,9 @@ constexpr uint32_t kScatterUnroll = 8;  // escapes per thread per scatter round
 constexpr int kPlaceBlocksPerSm = 4;
 
 // Pad bytes (pk -> sm, sm -> chunk_id, local_pos -> esc_val: each < 4 bytes,
-// by threads r = 0..11 of the caller) and the meta (by r == 0) of item `it`.
+// by threads r = 0..11 of the caller), the meta (by r == 0) of item `it`, and
+// its line of the build report of a gated call.  A gated item's meta holds n,
+// its coverage and status SZ_META_GATED only.
 __device__ void finish_item(const EncWs& ws, const sz_item& it, const Layout& l, uint64_t n, uint32_t e,
                             uint32_t flags, uint32_t r) {
   if (!flags && r < 12) {
@@ -308,23 +313,39 @@ __device__ void finish_item(const EncWs& ws, const sz_item& it, const Layout& l,
     if (r >= 8 && l.off_lpos + 2ull * e + (r - 8) < l.off_ev) p[l.off_lpos + 2ull * e + (r - 8)] = 0;
   }
   if (r == 0) {
-    if (flags) set_flag(ws.hdr, flags);
+    const bool gated = flags == SZ_META_GATED;
+    if (flags && !gated) set_flag(ws.hdr, flags);
     if (it.meta != nullptr && (reinterpret_cast<uintptr_t>(it.meta) & 15) == 0) {
       sz_meta m;
       m.n = n;
-      m.n_pairs = l.n_pairs;
-      m.n_esc = e;
-      m.comp_bytes = l.comp_bytes;
+      m.n_pairs = gated ? 0 : l.n_pairs;
+      m.n_esc = gated ? 0 : e;
+      m.comp_bytes = gated ? 0 : l.comp_bytes;
       m.off_pk = 0;
-      m.off_sm = l.off_sm;
-      m.off_cid = l.off_cid;
-      m.off_lpos = l.off_lpos;
-      m.off_ev = l.off_ev;
+      m.off_sm = gated ? 0 : l.off_sm;
+      m.off_cid = gated ? 0 : l.off_cid;
+      m.off_lpos = gated ? 0 : l.off_lpos;
+      m.off_ev = gated ? 0 : l.off_ev;
       m.chunk_size = kChunk;
       m.status = flags;
       m.coverage = (it.codebook && !(reinterpret_cast<uintptr_t>(it.codebook) & 15)) ? it.codebook->coverage : 0.0;
       m.reserved1 = 0;
       *it.meta = m;
+    }
+    if (ws.report != nullptr) {
+      sz_gate_report* rep = ws.report;
+      if (!flags) {
+        atomicAdd(reinterpret_cast<unsigned long long*>(&rep->tensors_encoded), 1ull);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&rep->raw_bytes_encoded), 2ull * n);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&rep->payload_bytes), l.comp_bytes);
+        if (l.comp_bytes > 2ull * n) atomicAdd(reinterpret_cast<unsigned long long*>(&rep->tensors_expanded), 1ull);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&rep->escapes), uint64_t(e));
+      } else if (gated) {
+        atomicAdd(reinterpret_cast<unsigned long long*>(&rep->tensors_gated), 1ull);
+        atomicAdd(reinterpret_cast<unsigned long long*>(&rep->raw_bytes_gated), 2ull * n);
+      } else {
+        atomicAdd(reinterpret_cast<unsigned long long*>(&rep->tensors_failed), 1ull);
+      }
     }
   }
 }
@@ -508,8 +529,11 @@ __global__ void __launch_bounds__(kPlaceThreads, kPlaceBlocksPerSm) enc_place(co
 
 }  // namespace
 
-cudaError_t launch_encode(const Items& items, void* ws_base, cudaStream_t stream, const DeviceInfo& dev) {
+cudaError_t launch_encode(const Items& items, void* ws_base, cudaStream_t stream, const DeviceInfo& dev, double gate,
+                          sz_gate_report* report) {
   EncWs ws = enc_ws(ws_base, items.count, items.total_tiles);
+  ws.gate = gate;
+  ws.report = report;
   cudaError_t err = cudaMemsetAsync(ws_base, 0, sizeof(WsHeader), stream);
   if (err != cudaSuccess) return err;
   {

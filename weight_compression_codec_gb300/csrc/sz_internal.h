@@ -18,7 +18,10 @@ struct DeviceInfo {
 cudaError_t device_info(DeviceInfo* info);
 
 cudaError_t launch_calibrate(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
-cudaError_t launch_encode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
+// gate >= 0: tensors whose codebook coverage is below it are left uncompressed
+// (meta status SZ_META_GATED); report (device) receives the build report
+cudaError_t launch_encode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev,
+                          double gate = -1.0, sz_gate_report* report = nullptr);
 cudaError_t launch_decode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
 // calibrate + encode in one streaming pass (CeWs workspace), then placement
 cudaError_t launch_calibrate_encode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
