@@ -228,6 +228,40 @@ SZ_API int sz_encode_many(const sz_item* d_items, uint32_t count, uint64_t total
 SZ_API int sz_decode_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles,
                           void* d_workspace, size_t workspace_bytes, sz_stream stream);
 
+/* ------------------------------------------------------------------ decode streamed from host memory */
+
+/* Decode of tensors whose payloads are in pinned host memory
+ * ("docs/developer/splitzip.md": a compressed fault is served by copying the
+ * payload from pinned host memory to the GPU and decoding it there, on the
+ * same stream).  h_items is a HOST array: payload = pinned host address
+ * (16-byte aligned, h_metas[i].comp_bytes bytes read), out and codebook =
+ * device addresses, n; meta, capacity and tile_begin are ignored.  h_metas
+ * (host) are the tensors' metas.  The tensors go in groups that fit in half
+ * of d_staging (device, 256-byte aligned, staging_bytes): copies of one group
+ * on copy_stream overlap the decode of the previous group on `stream`
+ * (the sz_decode_many kernels); payloads back to back in host memory (gaps
+ * under 256 bytes) go in one copy.  d_scratch (device, 256-byte aligned) holds
+ * the metas, the group tables and the decode workspace:
+ * sz_decode_many_host_scratch_bytes bytes.  Work on copy_stream follows the
+ * caller's earlier work on `stream`, and `stream` waits for all of it, so the
+ * call is ordered on `stream` like any other.  h_items and h_metas may be
+ * pageable and may be reused once the call returns: the library copies them
+ * into one of two pinned host buffers it keeps per device and thread, and so
+ * blocks the host until the upload of the call two back has completed.
+ * SZ_ERR_WORKSPACE if a payload does not fit in half the staging buffer;
+ * SZ_ERR_CUDA if a CUDA call fails.  Device-visible conditions (a meta
+ * that disagrees with the layout, an escape out of range) are reported as by
+ * sz_decode_many, through the workspace word at the start of the decode
+ * workspace (see sz_decode_many_host_flags_offset). */
+SZ_API size_t sz_decode_many_host_scratch_bytes(const sz_item* h_items, const sz_meta* h_metas, uint32_t count,
+                                                uint64_t staging_bytes);
+SZ_API int sz_decode_many_host(const sz_item* h_items, const sz_meta* h_metas, uint32_t count,
+                               void* d_staging, uint64_t staging_bytes, void* d_scratch, size_t scratch_bytes,
+                               sz_stream stream, sz_stream copy_stream);
+/* Offset (bytes) of the decode workspace, and so of its SZ_FLAG_* word, in the
+ * scratch of sz_decode_many_host: pass d_scratch + this to sz_workspace_flags. */
+SZ_API size_t sz_decode_many_host_flags_offset(uint32_t count);
+
 /* ------------------------------------------------------------------ coverage gate */
 
 /* sz_encode_many with the coverage gate of the pages' shard-cache builder

@@ -139,3 +139,34 @@ def test_meta_bytes_round_trip(lib, oracle):
     om = oracle.layout(12345, 67, 0.5)
     m = sz.meta_from_bytes(np.frombuffer(sz.meta_to_bytes(om), np.uint8))
     assert m.as_tuple() == om.as_tuple() and m.coverage == 0.5
+
+
+def test_host_decode_planner_on_the_host():
+    """sz_decode_many_host_scratch_bytes plans groups on the host only (the
+    addresses below are never dereferenced)."""
+    from weight_compression_codec_gb300 import binding as B
+
+    lib = B.lib()
+    n = 100_000
+    layout = B.SzMeta()
+    assert lib.sz_layout(n, 10, ctypes.byref(layout)) == 0
+    comp = layout.comp_bytes
+    count = 6
+    items = (B.SzItem * count)()
+    metas = (B.SzMeta * count)()
+    base = 1 << 32
+    for i in range(count):
+        items[i].payload = base + i * ((comp + 255) // 256 * 256)  # back to back, 256-byte steps
+        items[i].out = base
+        items[i].codebook = base
+        items[i].n = n
+        items[i].capacity = comp
+        metas[i] = layout
+    step = (comp + 255) // 256 * 256  # halves are whole multiples of 256 bytes
+    one = lib.sz_decode_many_host_scratch_bytes(items, metas, count, 2 * step)       # a tensor per group
+    all6 = lib.sz_decode_many_host_scratch_bytes(items, metas, count, 2 * 6 * step)  # all in one group
+    assert one > 0 and all6 > one  # a larger group needs a larger decode workspace
+    assert lib.sz_decode_many_host_scratch_bytes(items, metas, count, comp) == 0  # a payload exceeds half
+    metas[3].n = n + 1
+    assert lib.sz_decode_many_host_scratch_bytes(items, metas, count, 2 * step) == 0  # meta disagrees with n
+    assert lib.sz_decode_many_host_flags_offset(count) % 256 == 0

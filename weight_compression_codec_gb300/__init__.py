@@ -10,6 +10,7 @@ from .binding import SplitZipError, lib, library_path  # noqa: F401
 from .codec import (  # noqa: F401
     Batch,
     Codebook,
+    HostDecode,
     ItemTable,
     Meta,
     Workspace,

@@ -112,6 +112,9 @@ SIGNATURES = {
     "sz_calibrate_encode": (_INT, [_VP, _U64, _VP, _VP, _U64, _VP, _VP, _SZ, _VP]),
     "sz_calibrate_encode_many": (_INT, [_VP, _U32, _U64, _VP, _SZ, _VP]),
     "sz_encode_gated_many": (_INT, [_VP, _U32, _U64, ctypes.c_double, _VP, _VP, _SZ, _VP]),
+    "sz_decode_many_host_scratch_bytes": (_SZ, [_VP, _VP, _U32, _U64]),
+    "sz_decode_many_host": (_INT, [_VP, _VP, _U32, _VP, _U64, _VP, _SZ, _VP, _VP]),
+    "sz_decode_many_host_flags_offset": (_SZ, [_U32]),
     "sz_set_timing_events": (_INT, [_VP, _VP]),
     "sz_decode_noalloc": (_INT, [_VP, _U64, _VP, _VP, _VP, _U64, _VP, _VP]),
 }

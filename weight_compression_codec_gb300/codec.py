@@ -334,6 +334,48 @@ def read_gate_report(report: torch.Tensor) -> dict:
     return {name: int(getattr(r, name)) for name, _ in B.SzGateReport._fields_}
 
 
+class HostDecode:
+    """sz_decode_many_host over tensors whose payloads are in pinned host memory.
+
+    payloads[i]: pinned host uint8 tensor (or a view into one) holding the
+    payload; metas[i]: its Meta; codebooks[i] / outs[i]: device tensors.  The
+    staging buffer and scratch are allocated once and reused by run()."""
+
+    def __init__(self, payloads, metas, codebooks, outs, staging_bytes: int):
+        count = len(payloads)
+        dev = outs[0].device
+        self.items = (B.SzItem * count)()
+        self.metas = (B.SzMeta * count)()
+        for i in range(count):
+            if payloads[i].numel() and not (payloads[i].dtype == torch.uint8 and payloads[i].is_pinned()):
+                raise ValueError(f"payloads[{i}] must be a pinned host uint8 tensor")
+            it = self.items[i]
+            it.payload = payloads[i].data_ptr() if payloads[i].numel() else None
+            it.out = _bits(outs[i], f"out[{i}]").data_ptr() if outs[i].numel() else None
+            it.codebook = _u8(codebooks[i], f"codebook[{i}]", B.CODEBOOK_BYTES).data_ptr()
+            it.n = outs[i].numel()
+            it.capacity = payloads[i].numel()
+            self.metas[i] = B.SzMeta.from_buffer_copy(meta_to_bytes(metas[i]))
+        self.count = count
+        self.keep = (payloads, codebooks, outs)
+        self.staging = torch.empty(staging_bytes, dtype=torch.uint8, device=dev)
+        need = B.lib().sz_decode_many_host_scratch_bytes(self.items, self.metas, count, staging_bytes)
+        if need == 0:
+            raise B.SplitZipError(B.SZ_ERR_WORKSPACE, "sz_decode_many_host_scratch_bytes")
+        self.scratch = torch.empty(need, dtype=torch.uint8, device=dev)
+        self.copy_stream = torch.cuda.Stream(device=dev)
+
+    def run(self, stream=None) -> None:
+        rc = B.lib().sz_decode_many_host(self.items, self.metas, self.count, self.staging.data_ptr(),
+                                         self.staging.numel(), self.scratch.data_ptr(), self.scratch.numel(),
+                                         _stream_handle(stream), self.copy_stream.cuda_stream)
+        B.check(rc, "sz_decode_many_host")
+
+    def flags(self, stream=None) -> int:
+        off = B.lib().sz_decode_many_host_flags_offset(self.count)
+        return sz_workspace_flags(self.scratch[off:], stream)
+
+
 def sz_calibrate_encode_many(table: ItemTable, workspace=None, stream=None) -> None:
     """sz_calibrate_many then sz_encode_many in one pass over HBM (same results)."""
     dev = table.device.device
