@@ -264,3 +264,28 @@ def gate_report(ns, coverages, metas, min_coverage: float) -> dict:
             r["tensors_expanded"] += int(m.comp_bytes > 2 * n)
             r["escapes"] += m.n_esc
     return r
+
+
+# ---------------------------------------------------------------------------- slot decode
+# "splitzip_codec.py" GpuSplitZipDecoder.decode_slot_into and
+# "docs/developer/splitzip.md" (how a compressed fault is served; staging
+# invariants): the destination of a weight is a slot of its RAW size (2n
+# bytes); the compressed payload was copied into the slot's leading
+# comp_bytes; the decoder first copies those bytes aside (the slot is about to
+# be overwritten) and then decodes the full BF16 weight over the slot.  Bytes
+# of the slot past comp_bytes carry nothing.  Reading: a payload larger than
+# the slot cannot have been placed there and is rejected.
+
+
+def decode_slot(slot, meta: Meta, dec_lut, lib=None) -> np.ndarray:
+    """Decode the payload in slot[:meta.comp_bytes] over the slot (uint8, 2n
+    bytes).  Returns the slot, which then holds the BF16 bit patterns."""
+    s = np.asarray(slot)
+    if s.dtype != np.uint8 or s.ndim != 1 or s.size != 2 * meta.n:
+        raise ValueError("the slot must be a flat uint8 array of 2n bytes")
+    if meta.comp_bytes > s.size:
+        raise ValueError("payload larger than the slot")
+    stash = s[: meta.comp_bytes].copy()  # step 1: the payload copied aside
+    x = decode(stash, meta, dec_lut, lib=lib)  # step 2: decode over the slot
+    s[:] = x.view(np.uint8)
+    return s

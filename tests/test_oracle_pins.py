@@ -313,3 +313,56 @@ def test_gate_report_by_hand(oracle):
     r = oracle.gate_report([x.size for x in xs], [cb.coverage for cb in cbs], metas, -1.0)
     assert r["tensors_gated"] == 0 and r["tensors_expanded"] == 1 and r["escapes"] == metas[0].n_esc + 61_440
     assert r["payload_bytes"] == metas[0].comp_bytes + 528_384
+
+
+# ---------------------------------------------------------------------------- slot decode
+
+
+def test_decode_slot_golden_payload_with_garbage_after_it(oracle, golden):
+    # "splitzip_codec.py" GpuSplitZipDecoder: the payload sits in the slot's
+    # leading comp_bytes, the rest of the raw-size slot is arbitrary, and the
+    # weight is decoded over the whole slot
+    g = golden("three_chunk_escapes.json")
+    x = _three_chunk_input(g)
+    expect = np.zeros(g["meta"]["comp_bytes"], dtype=np.uint8)
+    for off, h in g["nonzero_runs_hex"]:
+        b = _bytes_hex(h)
+        expect[off:off + b.size] = b
+    m = oracle.layout(g["n"], g["meta"]["n_esc"], 1.0)
+    slot = np.random.default_rng(5).integers(0, 256, 2 * x.size, dtype=np.uint8)
+    slot[:expect.size] = expect
+    out = oracle.decode_slot(slot, m, np.array(g["dec_lut"], dtype=np.uint8))
+    assert out is slot and np.array_equal(slot.view(np.uint16), x)
+
+
+def test_decode_slot_needs_the_copy_aside(oracle):
+    # decoding element by element straight over the slot would overwrite pk,
+    # sm and escape bytes before they are read; the oracle's result must not
+    # depend on that (it equals the out-of-place decode)
+    x = inputs.gaussian(40_000, 0.02, seed=9)
+    x[::997] = 0x7F80  # a few escapes
+    cb = oracle.calibrate(x)
+    payload, m = oracle.encode(x, cb)
+    assert m.n_esc > 0 and m.comp_bytes <= 2 * x.size
+    slot = np.zeros(2 * x.size, dtype=np.uint8)
+    slot[:m.comp_bytes] = payload
+    naive = slot.copy()
+    nv = naive.view(np.uint16)
+    for i in range(x.size):  # no stash: element i is written before later elements are read
+        code = (naive[i // 2] >> (4 * (i % 2))) & 15
+        s = int(naive[m.off_sm + i])
+        nv[i] = ((s & 0x80) << 8) | (int(cb.dec_lut[code]) << 7) | (s & 0x7F)
+    assert not np.array_equal(nv, x)
+    oracle.decode_slot(slot, m, cb.dec_lut)
+    assert np.array_equal(slot.view(np.uint16), x)
+
+
+def test_decode_slot_rejects_a_payload_larger_than_the_slot(oracle):
+    x = np.array([0x3F80], dtype=np.uint16)  # n = 1: comp_bytes = 8 > 2
+    cb = oracle.calibrate(x)
+    payload, m = oracle.encode(x, cb)
+    assert m.comp_bytes == 8
+    with pytest.raises(ValueError):
+        oracle.decode_slot(np.zeros(2, np.uint8), m, cb.dec_lut)
+    with pytest.raises(ValueError):
+        oracle.decode_slot(np.zeros(8, np.uint8), m, cb.dec_lut)  # not a raw-size slot
