@@ -228,6 +228,48 @@ SZ_API int sz_encode_many(const sz_item* d_items, uint32_t count, uint64_t total
 SZ_API int sz_decode_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles,
                           void* d_workspace, size_t workspace_bytes, sz_stream stream);
 
+/* ------------------------------------------------------------------ in-place slot decode */
+
+/* Decode over the tensor's own buffer ("splitzip_codec.py"
+ * GpuSplitZipDecoder.decode_slot_into; "docs/developer/splitzip.md", how a
+ * compressed fault is served and the staging invariants): d_slot is the
+ * BF16 destination, 2n bytes, 16-byte aligned, whose leading comp_bytes hold
+ * the payload described by *d_meta (the bytes after it are ignored).  After
+ * the call the slot holds the n decoded values.  The pages' decoder copies
+ * the whole payload aside first; here only the bytes that a last-tile-first
+ * decode would overwrite before reading them (the sm bytes of elements below
+ * off_sm and the escape streams) are copied to the workspace, and each tile
+ * is stored once the tiles whose payload bytes lie under it have been read.
+ * A payload larger than 2n bytes cannot be in the slot: SZ_FLAG_META, slot
+ * untouched (as for a meta that disagrees with the layout).  A meta with
+ * SZ_META_GATED means the slot already holds the raw tensor: nothing is
+ * written.  Workspace: sz_decode_inplace_workspace_bytes(1, tiles(n))
+ * (decode workspace + 4 bytes and 12 KiB per tile + 256 bytes per tensor),
+ * 256-byte aligned. */
+SZ_API int sz_decode_inplace(uint16_t* d_slot, uint64_t n, const sz_meta* d_meta, const sz_codebook* d_codebook,
+                             void* d_workspace, size_t workspace_bytes, sz_stream stream);
+/* The same over an item table: item i's payload must equal its out (the
+ * slot) and its payload may use at most min(capacity, 2n) bytes. */
+SZ_API int sz_decode_inplace_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles,
+                                  void* d_workspace, size_t workspace_bytes, sz_stream stream);
+SZ_API size_t sz_decode_inplace_workspace_bytes(uint32_t count, uint64_t total_tiles);
+
+/* The in-place schedule of one tile, for inspection (host only): which
+ * payload bytes are copied to the stash and which tiles must have read their
+ * payload bytes before tile `tile` stores its output (local tile indices,
+ * inclusive ranges, empty when lo > hi).  SZ_ERR_ARG for n == 0, n out of
+ * range, n_esc > n or tile >= tiles(n); SZ_ERR_CAPACITY if the payload of
+ * (n, n_esc) is larger than 2n bytes. */
+typedef struct sz_inplace_tile {
+  uint64_t sm_stash_tiles;                /* tiles whose sm bytes are read from the stash   */
+  uint64_t stash_sm_from, stash_sm_to;    /* payload bytes stashed: sm part                 */
+  uint64_t stash_esc_from, stash_esc_to;  /* payload bytes stashed: escape streams          */
+  uint64_t stash_bytes, stash_budget;     /* stash bytes used / reserved for the tensor     */
+  uint64_t pk_lo, pk_hi;                  /* tiles whose pk bytes lie under this output     */
+  uint64_t sm_lo, sm_hi;                  /* tiles whose in-place sm bytes lie under it     */
+} sz_inplace_tile;
+SZ_API int sz_inplace_plan(uint64_t n, uint64_t n_esc, uint64_t tile, sz_inplace_tile* h_out);
+
 /* ------------------------------------------------------------------ decode streamed from host memory */
 
 /* Decode of tensors whose payloads are in pinned host memory

@@ -170,3 +170,81 @@ def test_host_decode_planner_on_the_host():
     metas[3].n = n + 1
     assert lib.sz_decode_many_host_scratch_bytes(items, metas, count, 2 * step) == 0  # meta disagrees with n
     assert lib.sz_decode_many_host_flags_offset(count) % 256 == 0
+
+
+# ---------------------------------------------------------------------------- in-place slot decode schedule
+
+
+def _inplace_cases():
+    # (n, n_esc): one tile, ragged tails, tile boundaries, an odd off_sm, escape
+    # counts up to the largest payload that still fits in the 2n-byte slot
+    cases = []
+    for n in (2, 3, 4, 7, 8191, 8192, 8193, 16384, 16385, 24577, 65536, 100_003, 262_144, 1_000_001, 2_097_152):
+        for frac in (0.0, 1e-4, 0.01, 0.0714):
+            e = int(n * frac)
+            cases.append((n, e))
+    return cases
+
+
+@pytest.mark.parametrize("n,e", _inplace_cases())
+def test_inplace_schedule_covers_every_payload_byte(lib, n, e):
+    """For the last-tile-first decode over the slot: every payload byte that
+    is read in place is overwritten (slot byte b belongs to output tile
+    b // 16384) only by its own reader's tile or by a tile that waits for its
+    reader; every other byte is in the stash; readers waited for are never
+    lower tiles (so the descending order cannot deadlock); the stash fits its
+    budget."""
+    m = sz.sz_layout(n, e)
+    if m.comp_bytes > 2 * n:
+        with pytest.raises(B.SplitZipError):
+            sz.inplace_plan(n, e, 0)
+        return
+    T = (n + 8191) // 8192
+    plans = [sz.inplace_plan(n, e, u) for u in range(T)]
+    p0 = plans[0]
+    assert all((p["sm_stash_tiles"], p["stash_sm_from"], p["stash_sm_to"], p["stash_esc_from"], p["stash_esc_to"])
+               == (p0["sm_stash_tiles"], p0["stash_sm_from"], p0["stash_sm_to"], p0["stash_esc_from"],
+                   p0["stash_esc_to"]) for p in plans)
+    assert p0["stash_bytes"] <= p0["stash_budget"]
+    for u, p in enumerate(plans):
+        for lo, hi in ((p["pk_lo"], p["pk_hi"]), (p["sm_lo"], p["sm_hi"])):
+            if lo <= hi:
+                assert u <= lo and hi < T
+    dep_lo = np.array([[p["pk_lo"], p["sm_lo"]] for p in plans], dtype=np.int64)
+    dep_hi = np.array([[p["pk_hi"], p["sm_hi"]] for p in plans], dtype=np.int64)
+
+    def check_in_place(b, r):
+        w = b // 16384
+        assert np.all(w < T)
+        assert np.all(w <= r), "a byte is overwritten by a tile decoded before its reader"
+        later = w < r
+        ww, rr = w[later], r[later]
+        ok = ((dep_lo[ww, 0] <= rr) & (rr <= dep_hi[ww, 0])) | ((dep_lo[ww, 1] <= rr) & (rr <= dep_hi[ww, 1]))
+        assert np.all(ok), "a tile stores over bytes whose reader it does not wait for"
+
+    # pk: element i's code is in byte i // 2, read by tile i // 8192
+    b = np.arange(m.n_pairs, dtype=np.int64)
+    check_in_place(b, b // 4096)
+    # sm: element i's byte at off_sm + i, read by tile i // 8192
+    i = np.arange(n, dtype=np.int64)
+    r = i // 8192
+    stashed = r < p0["sm_stash_tiles"]
+    sb = m.off_sm + i[stashed]
+    assert np.all((p0["stash_sm_from"] <= sb) & (sb < p0["stash_sm_to"]))
+    check_in_place(m.off_sm + i[~stashed], r[~stashed])
+    # escape streams: stashed whole
+    if e:
+        assert p0["stash_esc_from"] <= m.off_cid and p0["stash_esc_to"] >= m.off_ev + e
+    else:
+        assert p0["stash_esc_to"] == p0["stash_esc_from"]
+
+
+def test_inplace_plan_rejects_bad_arguments(lib):
+    t = B.SzInplaceTile()
+    assert lib.sz_inplace_plan(0, 0, 0, ctypes.byref(t)) == B.SZ_ERR_ARG
+    assert lib.sz_inplace_plan(8192, 0, 1, ctypes.byref(t)) == B.SZ_ERR_ARG  # one tile only
+    assert lib.sz_inplace_plan(100, 101, 0, ctypes.byref(t)) == B.SZ_ERR_ARG
+    assert lib.sz_inplace_plan(1, 0, 0, ctypes.byref(t)) == B.SZ_ERR_CAPACITY  # 8-byte payload, 2-byte slot
+    assert lib.sz_inplace_plan(8192, 0, 0, None) == B.SZ_ERR_ARG
+    assert lib.sz_decode_inplace_workspace_bytes(3, 10) == (lib.sz_decode_workspace_bytes(3, 10) + 256
+                                                            + 10 * 12288 + 3 * 256)

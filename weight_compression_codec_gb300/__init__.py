@@ -15,17 +15,21 @@ from .codec import (  # noqa: F401
     Meta,
     Workspace,
     codebook_from_bytes,
+    inplace_plan,
     make_items,
     meta_from_bytes,
     meta_to_bytes,
     read_codebook,
     read_gate_report,
     read_meta,
+    slot_table,
     sz_calibrate,
     sz_calibrate_encode,
     sz_calibrate_encode_many,
     sz_calibrate_many,
     sz_decode,
+    sz_decode_inplace,
+    sz_decode_inplace_many,
     sz_decode_many,
     sz_encode,
     sz_encode_gated_many,

@@ -83,6 +83,12 @@ class SzGateReport(ctypes.Structure):
         "tensors_expanded", "escapes", "tensors_failed")]
 
 
+class SzInplaceTile(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_uint64) for name in (
+        "sm_stash_tiles", "stash_sm_from", "stash_sm_to", "stash_esc_from", "stash_esc_to", "stash_bytes",
+        "stash_budget", "pk_lo", "pk_hi", "sm_lo", "sm_hi")]
+
+
 CODEBOOK_BYTES = 304
 META_BYTES = 96
 GATE_REPORT_BYTES = 64
@@ -112,6 +118,10 @@ SIGNATURES = {
     "sz_calibrate_encode": (_INT, [_VP, _U64, _VP, _VP, _U64, _VP, _VP, _SZ, _VP]),
     "sz_calibrate_encode_many": (_INT, [_VP, _U32, _U64, _VP, _SZ, _VP]),
     "sz_encode_gated_many": (_INT, [_VP, _U32, _U64, ctypes.c_double, _VP, _VP, _SZ, _VP]),
+    "sz_decode_inplace": (_INT, [_VP, _U64, _VP, _VP, _VP, _SZ, _VP]),
+    "sz_decode_inplace_many": (_INT, [_VP, _U32, _U64, _VP, _SZ, _VP]),
+    "sz_decode_inplace_workspace_bytes": (_SZ, [_U32, _U64]),
+    "sz_inplace_plan": (_INT, [_U64, _U64, _U64, ctypes.POINTER(SzInplaceTile)]),
     "sz_decode_many_host_scratch_bytes": (_SZ, [_VP, _VP, _U32, _U64]),
     "sz_decode_many_host": (_INT, [_VP, _VP, _U32, _VP, _U64, _VP, _SZ, _VP, _VP]),
     "sz_decode_many_host_flags_offset": (_SZ, [_U32]),

@@ -254,6 +254,28 @@ def sz_decode(payload: torch.Tensor, meta: torch.Tensor, codebook: torch.Tensor,
     return out
 
 
+def sz_decode_inplace(slot: torch.Tensor, meta: torch.Tensor, codebook: torch.Tensor, workspace=None,
+                      stream=None) -> torch.Tensor:
+    """Decode the payload held in the leading meta.comp_bytes of ``slot`` (the
+    BF16 destination, n elements) over the slot itself."""
+    sb = _bits(slot, "slot")
+    _u8(meta, "meta", B.META_BYTES)
+    _u8(codebook, "codebook", B.CODEBOOK_BYTES)
+    n = sb.numel()
+    ws = _workspace(workspace, B.lib().sz_decode_inplace_workspace_bytes(1, sz_tiles(n)), slot.device)
+    rc = B.lib().sz_decode_inplace(sb.data_ptr(), n, meta.data_ptr(), codebook.data_ptr(), ws.data_ptr(),
+                                   ws.numel(), _stream_handle(stream))
+    B.check(rc, "sz_decode_inplace")
+    return slot
+
+
+def inplace_plan(n: int, n_esc: int, tile: int) -> dict:
+    """The in-place decode's schedule of one tile (stash ranges, tiles waited for)."""
+    t = B.SzInplaceTile()
+    B.check(B.lib().sz_inplace_plan(int(n), int(n_esc), int(tile), ctypes.byref(t)), "sz_inplace_plan")
+    return {name: int(getattr(t, name)) for name, _ in B.SzInplaceTile._fields_}
+
+
 # ---------------------------------------------------------------------------- many tensors
 
 
@@ -327,6 +349,26 @@ def sz_encode_gated_many(table: ItemTable, min_coverage: float, report: torch.Te
                                       report.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(stream))
     B.check(rc, "sz_encode_gated_many")
     return report
+
+
+def slot_table(slots: list[torch.Tensor], codebooks, metas) -> ItemTable:
+    """Item table for sz_decode_inplace_many: item i decodes over slots[i]
+    (its payload in the slot's leading bytes); codebooks[i] / metas[i] are
+    device tensors or addresses."""
+    sb = [_bits(s, f"slot[{i}]") for i, s in enumerate(slots)]
+    n = [s.numel() for s in sb]
+    items = make_items(n, out=sb, payload=sb, capacity=[2 * k for k in n], codebook=codebooks, meta=metas)
+    t = ItemTable(items, sb[0].device)
+    t.keep = sb
+    return t
+
+
+def sz_decode_inplace_many(table: ItemTable, workspace=None, stream=None) -> None:
+    dev = table.device.device
+    ws = _workspace(workspace, B.lib().sz_decode_inplace_workspace_bytes(table.count, table.total_tiles), dev)
+    rc = B.lib().sz_decode_inplace_many(table.ptr(), table.count, table.total_tiles, ws.data_ptr(), ws.numel(),
+                                        _stream_handle(stream))
+    B.check(rc, "sz_decode_inplace_many")
 
 
 def read_gate_report(report: torch.Tensor) -> dict:

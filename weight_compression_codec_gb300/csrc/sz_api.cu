@@ -132,6 +132,30 @@ SZ_API size_t sz_decode_workspace_bytes(uint32_t count, uint64_t total_tiles) {
   return size_t(dec_ws_bytes(count, total_tiles));
 }
 
+SZ_API size_t sz_decode_inplace_workspace_bytes(uint32_t count, uint64_t total_tiles) {
+  return size_t(ip_ws_bytes(count, total_tiles));
+}
+
+SZ_API int sz_inplace_plan(uint64_t n, uint64_t n_esc, uint64_t tile, sz_inplace_tile* h_out) {
+  if (h_out == nullptr || n == 0 || n > SZ_MAX_ELEMS || n_esc > n || tile >= tiles_of(n)) return SZ_ERR_ARG;
+  const Layout l = layout_of(n, n_esc);
+  if (l.comp_bytes > 2 * n) return SZ_ERR_CAPACITY;
+  const IpStash st = ip_stash(n, n_esc, l.off_sm, l.off_cid, l.comp_bytes);
+  const IpDeps d = ip_deps(n, l.off_sm, tile);
+  h_out->sm_stash_tiles = st.sm_tiles;
+  h_out->stash_sm_from = st.sm_from;
+  h_out->stash_sm_to = st.sm_to;
+  h_out->stash_esc_from = st.esc_from;
+  h_out->stash_esc_to = st.esc_to;
+  h_out->stash_bytes = st.bytes;
+  h_out->stash_budget = tiles_of(n) * kIpStashPerTile + kIpStashPerItem;
+  h_out->pk_lo = d.pk_lo;
+  h_out->pk_hi = d.pk_hi;
+  h_out->sm_lo = d.sm_lo;
+  h_out->sm_hi = d.sm_hi;
+  return SZ_OK;
+}
+
 SZ_API size_t sz_calibrate_encode_workspace_bytes(uint32_t count, uint64_t total_tiles) {
   return size_t(ce_ws_bytes(count, total_tiles));
 }
@@ -208,6 +232,25 @@ SZ_API int sz_decode(const uint8_t* d_payload, uint64_t payload_bytes, const sz_
   return from_cuda(launch_decode(single(one), d_workspace, reinterpret_cast<cudaStream_t>(stream), dev));
 }
 
+SZ_API int sz_decode_inplace(uint16_t* d_slot, uint64_t n, const sz_meta* d_meta, const sz_codebook* d_codebook,
+                             void* d_workspace, size_t workspace_bytes, sz_stream stream) {
+  if (n > SZ_MAX_ELEMS || d_meta == nullptr || d_codebook == nullptr) return SZ_ERR_ARG;
+  if (n > 0 && d_slot == nullptr) return SZ_ERR_ARG;
+  if (!aligned(d_slot, 16) || !aligned(d_codebook, 16) || !aligned(d_meta, 16)) return SZ_ERR_ALIGN;
+  if (int rc = check_ws(d_workspace, workspace_bytes, ip_ws_bytes(1, tiles_of(n)))) return rc;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return SZ_ERR_CUDA;
+  sz_item one;
+  std::memset(&one, 0, sizeof(one));
+  one.out = d_slot;
+  one.payload = reinterpret_cast<uint8_t*>(d_slot);
+  one.codebook = const_cast<sz_codebook*>(d_codebook);
+  one.meta = const_cast<sz_meta*>(d_meta);
+  one.n = n;
+  one.capacity = 2 * n;
+  return from_cuda(launch_decode_inplace(single(one), d_workspace, reinterpret_cast<cudaStream_t>(stream), dev));
+}
+
 // ---------------------------------------------------------------- many tensors
 
 SZ_API int sz_calibrate_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles, void* d_workspace,
@@ -238,6 +281,16 @@ SZ_API int sz_decode_many(const sz_item* d_items, uint32_t count, uint64_t total
   if (device_info(&dev) != cudaSuccess) return SZ_ERR_CUDA;
   return from_cuda(launch_decode(table(d_items, count, total_tiles), d_workspace,
                                  reinterpret_cast<cudaStream_t>(stream), dev));
+}
+
+SZ_API int sz_decode_inplace_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles, void* d_workspace,
+                                  size_t workspace_bytes, sz_stream stream) {
+  if (int rc = check_many(d_items, count, total_tiles)) return rc;
+  if (int rc = check_ws(d_workspace, workspace_bytes, ip_ws_bytes(count, total_tiles))) return rc;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return SZ_ERR_CUDA;
+  return from_cuda(launch_decode_inplace(table(d_items, count, total_tiles), d_workspace,
+                                         reinterpret_cast<cudaStream_t>(stream), dev));
 }
 
 // ---------------------------------------------------------------- coverage gate

@@ -22,6 +22,14 @@
 //                dec_lut held in registers (byte permutes), patch the tile's
 //                escapes in shared memory and hand the finished 16 KiB tile
 //                to a TMA bulk store.
+//
+// In-place slot decode (the payload in the leading comp_bytes of the
+// tensor's own 2n-byte output, "splitzip_codec.py" GpuSplitZipDecoder): the
+// same prepare pass, then dip_stash copies aside only the bytes that a
+// last-tile-first decode would overwrite before reading them (the sm bytes
+// of elements below off_sm and the escape streams; the pages' decoder copies
+// the whole payload), then dec_main<true> decodes tiles in descending order,
+// each tile's store waiting for the tiles whose in-place bytes lie under it.
 #include "sz_internal.h"
 
 namespace sz {
@@ -48,6 +56,8 @@ struct __align__(128) DecStage {
   uint16_t* out;
   uint32_t m, lt, n_tile, flags;
   uint32_t sm_shift, cid_shift, lpos_shift, ev_shift;
+  uint64_t tile;  // flat tile index (in-place decode: its read_done word)
+  uint4 dep;      // in-place decode: tiles [tile + x, tile + y] and [tile + z, tile + w] to wait for
 };
 
 struct DecShared {
@@ -57,7 +67,7 @@ struct DecShared {
   uint64_t empty[kDecStages];
 };
 
-__device__ bool meta_ok(const sz_item& it, uint64_t n_esc_limit) {
+__device__ bool meta_ok(const sz_item& it, uint64_t n_esc_limit, uint64_t capacity) {
   const sz_meta* mp = it.meta;
   if (mp == nullptr || (reinterpret_cast<uintptr_t>(mp) & 15)) return false;
   const sz_meta m = *mp;
@@ -65,14 +75,17 @@ __device__ bool meta_ok(const sz_item& it, uint64_t n_esc_limit) {
   const Layout l = layout_of(m.n, m.n_esc);
   return m.n_pairs == l.n_pairs && m.off_pk == 0 && m.off_sm == l.off_sm && m.off_cid == l.off_cid &&
          m.off_lpos == l.off_lpos && m.off_ev == l.off_ev && m.comp_bytes == l.comp_bytes &&
-         l.comp_bytes <= it.capacity;
+         l.comp_bytes <= capacity;
 }
 
 // Internal item flag (never in the header word): a tensor kept raw by the
 // coverage gate (meta status SZ_META_GATED), skipped without an error.
 constexpr uint32_t kItemGated = 0x80000000u;
 
-__device__ uint32_t item_problems(const Items& items, uint32_t i) {
+// In-place decode (the payload in the leading bytes of the item's own output,
+// its 2n-byte slot): payload must equal out and the payload must fit in 2n
+// bytes (SZ_FLAG_META otherwise).
+__device__ uint32_t item_problems(const Items& items, uint32_t i, bool inplace) {
   const sz_item& it = item_at(items, i);
   uint32_t bad = 0;
   if (it.n > SZ_MAX_ELEMS) return SZ_FLAG_SIZE;
@@ -87,7 +100,12 @@ __device__ uint32_t item_problems(const Items& items, uint32_t i) {
   if (it.codebook == nullptr || (reinterpret_cast<uintptr_t>(it.codebook) & 15)) bad |= SZ_FLAG_ALIGN;
   if (it.n > 0 && (it.out == nullptr || (reinterpret_cast<uintptr_t>(it.out) & 15))) bad |= SZ_FLAG_ALIGN;
   if (it.n > 0 && (it.payload == nullptr || (reinterpret_cast<uintptr_t>(it.payload) & 15))) bad |= SZ_FLAG_ALIGN;
-  if (!meta_ok(it, SZ_MAX_ELEMS)) bad |= SZ_FLAG_META;
+  uint64_t capacity = it.capacity;
+  if (inplace) {
+    if (it.n > 0 && it.payload != reinterpret_cast<const uint8_t*>(it.out)) bad |= SZ_FLAG_META;
+    if (capacity > 2 * it.n) capacity = 2 * it.n;
+  }
+  if (!meta_ok(it, SZ_MAX_ELEMS, capacity)) bad |= SZ_FLAG_META;
   return bad;
 }
 
@@ -200,7 +218,8 @@ __device__ void prepare_group(const Items& items, const DecWs& ws, uint32_t i, c
 // prepared by one warp of the row's first block, larger ones by the row's
 // blocks dealt round-robin over them (warp per 32-tile group, each warp
 // validating the item for itself).
-__global__ void __launch_bounds__(kPrepWarps * 32) dec_prepare(const __grid_constant__ Items items, DecWs ws) {
+__global__ void __launch_bounds__(kPrepWarps * 32) dec_prepare(const __grid_constant__ Items items, DecWs ws,
+                                                                bool inplace) {
   __shared__ uint32_t counts[kPrepWarps][32];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t warp = threadIdx.x >> 5;
@@ -213,7 +232,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32) dec_prepare(const __grid_cons
         if (it.n <= kSmallTiles * kTile) {
           uint32_t bad = 0;
           if (lane == 0) {
-            bad = item_problems(items, i);
+            bad = item_problems(items, i, inplace);
             ws.item_flags[i] = bad;
             if (bad & ~kItemGated) set_flag(ws.hdr, bad & ~kItemGated);
           }
@@ -238,7 +257,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32) dec_prepare(const __grid_cons
       // first block publishes the result
       uint32_t bad = 0;
       if (lane == 0) {
-        bad = item_problems(items, i);
+        bad = item_problems(items, i, inplace);
         if (rank == 0 && warp == 0) {
           ws.item_flags[i] = bad;
           if (bad & ~kItemGated) set_flag(ws.hdr, bad & ~kItemGated);
@@ -251,6 +270,92 @@ __global__ void __launch_bounds__(kPrepWarps * 32) dec_prepare(const __grid_cons
            ta += uint64_t(blocks_per_item) * kPrepWarps * 32)
         prepare_group(items, ws, i, it, tiles, bad != 0, ta, lane, counts[warp]);
     }
+  }
+}
+
+// Copies payload bytes [a, b) to dst_v + a .. dst_v + b (dst_v: the stash
+// address of payload byte 0, congruent to src mod 16; b - a <= 16400) with
+// one warp: each lane issues 8 16-byte loads before its stores.
+__device__ __noinline__ void stash_copy_warp(uint64_t dst_v, const uint8_t* src, uint64_t a, uint64_t b, uint32_t lane) {
+  const uint64_t a16 = (a + 15) & ~uint64_t(15), b16 = b & ~uint64_t(15);
+  if (a16 >= b16) {
+    for (uint64_t x = a + lane; x < b; x += 32) *reinterpret_cast<uint8_t*>(dst_v + x) = __ldg(src + x);
+    return;
+  }
+  if (lane < a16 - a) *reinterpret_cast<uint8_t*>(dst_v + a + lane) = __ldg(src + a + lane);
+  if (lane < b - b16) *reinterpret_cast<uint8_t*>(dst_v + b16 + lane) = __ldg(src + b16 + lane);
+  const uint4* s4 = reinterpret_cast<const uint4*>(src) + a16 / 16;
+  uint4* d4 = reinterpret_cast<uint4*>(dst_v + a16);
+  const uint32_t nv = uint32_t((b16 - a16) / 16);  // at most 1025
+  for (uint32_t v0 = lane; v0 < nv; v0 += 8 * 32) {
+    uint4 r[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (v0 + 32u * j < nv) r[j] = __ldg(s4 + v0 + 32u * j);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (v0 + 32u * j < nv) d4[v0 + 32u * j] = r[j];
+  }
+}
+
+constexpr uint64_t kIpEscPiece = 16384;  // escape-stream bytes stashed per tile
+constexpr int kStashWarps = 8;
+
+// In-place decode, before the main pass: per tile (one warp each), clears
+// its read_done word and copies its share of the bytes that the descending
+// decode would overwrite before reading them: its own sm bytes when it is
+// one of the first ip_sm_stash_tiles tiles, and the escape streams' 16 KiB
+// piece with its index (the escape part is at most n / 2 + 15 bytes, so the
+// tiles cover it).
+__global__ void __launch_bounds__(kStashWarps * 32, 4) dip_stash(const __grid_constant__ Items items, DecWs ws) {
+  if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
+  const uint32_t lane = threadIdx.x & 31u;
+  for (uint64_t tt = uint64_t(blockIdx.x) * kStashWarps + (threadIdx.x >> 5); tt < items.total_tiles;
+       tt += uint64_t(gridDim.x) * kStashWarps) {
+    if (lane == 0) ws.read_done[tt] = 0;
+    const uint32_t idx = ws.tile_item ? ws.tile_item[tt] : 0u;
+    if (idx >= items.count || ws.item_flags[idx] != 0) continue;
+    const sz_item& it = item_at(items, idx);
+    const uint64_t tb = it.tile_begin;
+    if (tt < tb || tt - tb >= tiles_of(it.n)) continue;
+    const uint64_t lt = tt - tb;
+    const sz_meta* mp = it.meta;
+    const uint64_t off_sm = mp->off_sm;
+    const IpStash st = ip_stash(it.n, mp->n_esc, off_sm, mp->off_cid, mp->comp_bytes);
+    const uint64_t base = reinterpret_cast<uint64_t>(ws.stash) + ip_stash_at(tb, idx);
+    if (lt < st.sm_tiles) {
+      const uint64_t a = lt == 0 ? st.sm_from : off_sm + lt * kTile;
+      const uint64_t b = (off_sm + (lt + 1) * kTile < st.sm_to) ? off_sm + (lt + 1) * kTile : st.sm_to;
+      stash_copy_warp(base - st.sm_from, it.payload, a, b, lane);
+    }
+    const uint64_t ea = st.esc_from + lt * kIpEscPiece;
+    if (ea < st.esc_to)
+      stash_copy_warp(base + st.esc_off - st.esc_from, it.payload, ea,
+                      (ea + kIpEscPiece < st.esc_to) ? ea + kIpEscPiece : st.esc_to, lane);
+  }
+}
+
+// One warp waits (bounded) until read_done is set for every tile of
+// [tile + dep.x, tile + dep.y] and [tile + dep.z, tile + dep.w] other than
+// the tile itself: lane l polls one of them, so the check costs one round
+// trip however many tiles there are (at most 4 + 3).  Gives up after
+// kWaitTimeoutNs, or at once when another CTA has already given up
+// (SZ_FLAG_TIMEOUT), so a failed call ends within one timeout.
+__device__ bool wait_read_done_warp(const DecWs& ws, uint64_t tile, uint4 dep, uint32_t lane) {
+  const uint32_t lo0 = dep.x == 0 ? 1u : dep.x, lo1 = dep.z == 0 ? 1u : dep.z;  // skip the tile itself
+  const uint32_t n0 = dep.y >= lo0 ? dep.y - lo0 + 1 : 0, n1 = dep.w >= lo1 ? dep.w - lo1 + 1 : 0;
+  const uint32_t* p = nullptr;
+  if (lane < n0) p = ws.read_done + tile + lo0 + lane;
+  else if (lane < n0 + n1) p = ws.read_done + tile + lo1 + (lane - n0);
+  bool ok = p == nullptr || ld_acquire_u32(p) != 0;
+  if (__all_sync(0xFFFFFFFFu, ok)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (!ok) ok = ld_acquire_u32(p) != 0;
+    if (__all_sync(0xFFFFFFFFu, ok)) return true;
+    if ((i & 63) == 0 && __any_sync(0xFFFFFFFFu, lane == 0 && (global_timer_ns() - t0 > kWaitTimeoutNs ||
+                                                              (ld_acquire_u32(&ws.hdr->flags) & SZ_FLAG_TIMEOUT))))
+      return false;
   }
 }
 
@@ -286,6 +391,21 @@ __device__ __forceinline__ Slice slice_of(uint64_t start, uint64_t bytes) {
   return s;
 }
 
+// In-place decode schedule: ticket q is flat tile total_tiles - 1 - q
+// (descending) and CTA b of the R CTAs (a cooperative launch, so all are
+// resident) takes tickets b, b + R, b + 2R, ... in that order.  Every CTA
+// then meets its tickets in increasing order and a tile only waits for
+// tiles of smaller tickets, which are read before it by induction; and as
+// the CTAs advance together, a ticket is reached at about the time of its
+// neighbours, so waits are short.
+
+// INPLACE = false: sz_decode(_many); persistent CTAs own contiguous tile
+// ranges.  INPLACE = true: in-place slot decode; CTAs take tiles in the
+// cyclic descending order above, read the stashed sm and escape bytes from
+// the stash, mark each tile's read_done once its stage has landed and store
+// a tile only after the tiles whose in-place bytes lie under its output have
+// been read.
+template <bool INPLACE>
 __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     dec_main(const __grid_constant__ Items items, DecWs ws) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -297,9 +417,6 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
   if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
 
   const uint64_t T = items.total_tiles;
-  const uint64_t per = (T + gridDim.x - 1) / gridDim.x;
-  const uint64_t t0 = uint64_t(blockIdx.x) * per;
-  const uint64_t t1 = (t0 + per < T) ? t0 + per : T;
 
   if (tid == 0) {
     for (int s = 0; s < kDecStages; ++s) {
@@ -312,15 +429,18 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
 
   if (warp == kDecConsumerWarps) {
     // ---------------------------------------------------------------- producer warp
-    // Lane l holds what the producer needs of tile w0 + l of the current
-    // 32-tile window, resolved in parallel when the window starts: the escape
-    // range, the item (tile -> item map), its payload, output, dec_lut and
-    // section offsets.
+    // Lane l holds what the producer needs of tile l of the current window,
+    // resolved in parallel when the window starts: the escape range, the
+    // item (tile -> item map), its payload, output, dec_lut and section
+    // offsets (in-place: also the sm and escape sources and the tiles to
+    // wait for).
     bool w_ok = false;
     uint2 w_rec = make_uint2(0, 0);
     const uint8_t* w_base = nullptr;
     uint16_t* w_out = nullptr;
     uint64_t w_g = 0, w_off_sm = 0, w_off_cid = 0, w_off_lpos = 0, w_off_ev = 0;
+    uint64_t w_smv = 0, w_escv = 0;  // in-place: address of payload byte 0 in the sm / escape source
+    uint4 w_dep = make_uint4(1, 0, 1, 0);
     uint4 w_dlut = make_uint4(0, 0, 0, 0);
     uint32_t w_lt = 0, w_nt = 0;
     uint64_t it = 0;  // stages handed out
@@ -334,21 +454,43 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
       }
       return true;
     };
-    for (uint64_t t = t0;; ++t) {
+    auto shfl64 = [&](uint64_t v, uint32_t from) {
+      return (uint64_t(__shfl_sync(0xFFFFFFFFu, uint32_t(v >> 32), from)) << 32) |
+             __shfl_sync(0xFFFFFFFFu, uint32_t(v), from);
+    };
+    // next / t1: the CTA's range of tiles, or (in place) of its tickets' ranks
+    // (rank r <-> ticket blockIdx.x + r R)
+    uint64_t next = 0, t1 = 0;
+    const uint64_t R = gridDim.x;
+    if constexpr (INPLACE) {
+      t1 = blockIdx.x < T ? (T - blockIdx.x + R - 1) / R : 0;
+    } else {
+      const uint64_t per = (T + R - 1) / R;
+      next = uint64_t(blockIdx.x) * per;
+      t1 = (next + per < T) ? next + per : T;
+    }
+    uint64_t win_first = 0;  // tile, or (in place) rank, of the window's first entry
+    uint32_t win_len = 0, win_pos = 0;
+    for (;;) {
       int s;
       if (!acquire(s)) return;
-      if (t >= t1) {
-        if (lane == 0) {
-          sh.st[s].flags = kStageEnd;
-          mbar_arrive(&sh.full[s]);
+      if (win_pos == win_len) {
+        const uint64_t first = next;
+        win_len = next < t1 ? uint32_t((t1 - next < 32) ? t1 - next : 32) : 0u;
+        next += win_len;
+        win_first = first;
+        win_pos = 0;
+        if (win_len == 0) {
+          if (lane == 0) {
+            sh.st[s].flags = kStageEnd;
+            mbar_arrive(&sh.full[s]);
+          }
+          cp_async_mbar_arrive_noinc(&sh.full[s]);
+          return;
         }
-        cp_async_mbar_arrive_noinc(&sh.full[s]);
-        return;
-      }
-      if (((t - t0) & 31) == 0) {
-        const uint64_t mine = t + lane;
+        const uint64_t mine = INPLACE ? T - 1 - (blockIdx.x + (first + lane) * R) : first + lane;
         w_ok = false;
-        if (mine < t1) {
+        if (uint32_t(lane) < win_len) {
           w_rec = ws.ranges[mine];
           const uint32_t idx = ws.tile_item ? ws.tile_item[mine] : 0u;
           if (idx < items.count && w_rec.x != kRangeInvalid && ws.item_flags[idx] == 0) {
@@ -366,34 +508,53 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
               w_off_lpos = mp->off_lpos;
               w_off_ev = mp->off_ev;
               w_dlut = *reinterpret_cast<const uint4*>(itm.codebook->dec_lut);
+              if constexpr (INPLACE) {
+                const IpStash sv = ip_stash(itm.n, mp->n_esc, w_off_sm, w_off_cid, mp->comp_bytes);
+                const uint64_t sb = reinterpret_cast<uint64_t>(ws.stash) + ip_stash_at(tb, idx);
+                w_smv = (w_lt < sv.sm_tiles) ? sb - sv.sm_from : reinterpret_cast<uint64_t>(itm.payload);
+                w_escv = sb + sv.esc_off - sv.esc_from;
+                const IpDeps d = ip_deps(itm.n, w_off_sm, w_lt);
+                w_dep = make_uint4(1, 0, 1, 0);
+                if (d.pk_lo <= d.pk_hi) w_dep.x = uint32_t(d.pk_lo - w_lt), w_dep.y = uint32_t(d.pk_hi - w_lt);
+                if (d.sm_lo <= d.sm_hi) w_dep.z = uint32_t(d.sm_lo - w_lt), w_dep.w = uint32_t(d.sm_hi - w_lt);
+              }
               w_ok = true;
             }
           }
         }
       }
-      const uint32_t src = uint32_t((t - t0) & 31);
+      const uint32_t src = win_pos++;
+      const uint64_t tile = INPLACE ? T - 1 - (blockIdx.x + (win_first + src) * R) : win_first + src;
       if (!__shfl_sync(0xFFFFFFFFu, w_ok, src)) {
         if (lane == 0) {
           sh.st[s].flags = kStageInvalid;
+          sh.st[s].tile = tile;
           mbar_arrive(&sh.full[s]);
         }
         cp_async_mbar_arrive_noinc(&sh.full[s]);
         ++it;
         continue;
       }
-      auto shfl64 = [&](uint64_t v) {
-        return (uint64_t(__shfl_sync(0xFFFFFFFFu, uint32_t(v >> 32), src)) << 32) |
-               __shfl_sync(0xFFFFFFFFu, uint32_t(v), src);
-      };
       const uint32_t k0 = __shfl_sync(0xFFFFFFFFu, w_rec.x, src);
       const uint32_t k1 = __shfl_sync(0xFFFFFFFFu, w_rec.y, src);
       const uint32_t lt = __shfl_sync(0xFFFFFFFFu, w_lt, src);
       const uint32_t nt = __shfl_sync(0xFFFFFFFFu, w_nt, src);
-      const uint64_t g = shfl64(w_g);
-      const uint64_t off_sm = shfl64(w_off_sm), off_cid = shfl64(w_off_cid), off_lpos = shfl64(w_off_lpos),
-                     off_ev = shfl64(w_off_ev);
-      const uint8_t* base = reinterpret_cast<const uint8_t*>(shfl64(reinterpret_cast<uint64_t>(w_base)));
-      uint16_t* const out_t = reinterpret_cast<uint16_t*>(shfl64(reinterpret_cast<uint64_t>(w_out)));
+      const uint64_t g = shfl64(w_g, src);
+      const uint64_t off_sm = shfl64(w_off_sm, src), off_cid = shfl64(w_off_cid, src),
+                     off_lpos = shfl64(w_off_lpos, src), off_ev = shfl64(w_off_ev, src);
+      const uint8_t* base = reinterpret_cast<const uint8_t*>(shfl64(reinterpret_cast<uint64_t>(w_base), src));
+      const uint8_t* sm_src = base;   // where payload byte 0 of the sm section's source is
+      const uint8_t* esc_src = base;  // ... of the escape streams' source
+      uint4 dep = make_uint4(1, 0, 1, 0);
+      if constexpr (INPLACE) {
+        sm_src = reinterpret_cast<const uint8_t*>(shfl64(w_smv, src));
+        esc_src = reinterpret_cast<const uint8_t*>(shfl64(w_escv, src));
+        dep.x = __shfl_sync(0xFFFFFFFFu, w_dep.x, src);
+        dep.y = __shfl_sync(0xFFFFFFFFu, w_dep.y, src);
+        dep.z = __shfl_sync(0xFFFFFFFFu, w_dep.z, src);
+        dep.w = __shfl_sync(0xFFFFFFFFu, w_dep.w, src);
+      }
+      uint16_t* const out_t = reinterpret_cast<uint16_t*>(shfl64(reinterpret_cast<uint64_t>(w_out), src));
       uint4 dlut;
       dlut.x = __shfl_sync(0xFFFFFFFFu, w_dlut.x, src);
       dlut.y = __shfl_sync(0xFFFFFFFFu, w_dlut.y, src);
@@ -424,28 +585,30 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
           st.lt = lt;
           st.n_tile = nt;
           st.flags = (first ? 0u : kStageCont) | (pc + 1 < pieces ? kStageMore : 0u);
+          st.tile = tile;
+          st.dep = dep;
           st.sm_shift = uint32_t(off_sm + g - ssm.a0);
           st.cid_shift = uint32_t(off_cid + 4ull * pk0 - scid.a0);
           st.lpos_shift = uint32_t(off_lpos + 2ull * pk0 - slp.a0);
           st.ev_shift = uint32_t(off_ev + pk0 - sev.a0);
           mbar_arrive_expect_tx(&sh.full[s], tx);
           if (first && spk.a1 > spk.a0) bulk_g2s(st.pk, base + spk.a0, uint32_t(spk.a1 - spk.a0), &sh.full[s]);
-          if (first && ssm.a1 > ssm.a0) bulk_g2s(st.sm, base + ssm.a0, uint32_t(ssm.a1 - ssm.a0), &sh.full[s]);
-          if (pm && scid.a1 > scid.a0) bulk_g2s(st.cid, base + scid.a0, uint32_t(scid.a1 - scid.a0), &sh.full[s]);
-          if (pm && slp.a1 > slp.a0) bulk_g2s(st.lpos, base + slp.a0, uint32_t(slp.a1 - slp.a0), &sh.full[s]);
-          if (pm && sev.a1 > sev.a0) bulk_g2s(st.ev, base + sev.a0, uint32_t(sev.a1 - sev.a0), &sh.full[s]);
+          if (first && ssm.a1 > ssm.a0) bulk_g2s(st.sm, sm_src + ssm.a0, uint32_t(ssm.a1 - ssm.a0), &sh.full[s]);
+          if (pm && scid.a1 > scid.a0) bulk_g2s(st.cid, esc_src + scid.a0, uint32_t(scid.a1 - scid.a0), &sh.full[s]);
+          if (pm && slp.a1 > slp.a0) bulk_g2s(st.lpos, esc_src + slp.a0, uint32_t(slp.a1 - slp.a0), &sh.full[s]);
+          if (pm && sev.a1 > sev.a0) bulk_g2s(st.ev, esc_src + sev.a0, uint32_t(sev.a1 - sev.a0), &sh.full[s]);
         } else if (first && lane == 1 && spk.end > spk.a1) {
           cp_async16_zfill(st.pk + (spk.a1 - spk.a0), base + spk.a1, uint32_t(spk.end - spk.a1));
         } else if (first && lane == 2 && ssm.end > ssm.a1) {
-          cp_async16_zfill(st.sm + (ssm.a1 - ssm.a0), base + ssm.a1, uint32_t(ssm.end - ssm.a1));
+          cp_async16_zfill(st.sm + (ssm.a1 - ssm.a0), sm_src + ssm.a1, uint32_t(ssm.end - ssm.a1));
         } else if (pm && lane == 3 && scid.end > scid.a1) {
-          cp_async16_zfill(reinterpret_cast<uint8_t*>(st.cid) + (scid.a1 - scid.a0), base + scid.a1,
+          cp_async16_zfill(reinterpret_cast<uint8_t*>(st.cid) + (scid.a1 - scid.a0), esc_src + scid.a1,
                            uint32_t(scid.end - scid.a1));
         } else if (pm && lane == 4 && slp.end > slp.a1) {
-          cp_async16_zfill(reinterpret_cast<uint8_t*>(st.lpos) + (slp.a1 - slp.a0), base + slp.a1,
+          cp_async16_zfill(reinterpret_cast<uint8_t*>(st.lpos) + (slp.a1 - slp.a0), esc_src + slp.a1,
                            uint32_t(slp.end - slp.a1));
         } else if (pm && lane == 5 && sev.end > sev.a1) {
-          cp_async16_zfill(st.ev + (sev.a1 - sev.a0), base + sev.a1, uint32_t(sev.end - sev.a1));
+          cp_async16_zfill(st.ev + (sev.a1 - sev.a0), esc_src + sev.a1, uint32_t(sev.end - sev.a1));
         }
         cp_async_mbar_arrive_noinc(&sh.full[s]);
         ++it;
@@ -465,6 +628,14 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     const DecStage& st = sh.st[s];
     // read before the vote: after it, an invalid tile's stage is released
     const uint32_t flags = ok ? st.flags : 0u;
+    if constexpr (INPLACE) {
+      // The tile's payload bytes are in shared memory now (or it reads
+      // none): the phase completes only after the copies' reads of global
+      // memory have returned, so no store issued after this flag is seen can
+      // change what they read.  A relaxed store suffices (a release fence
+      // here, on every tile, cost a quarter of the kernel's time).
+      if (tid == 0 && ok && !(flags & (kStageCont | kStageEnd))) st_relaxed_u32(ws.read_done + st.tile, 1u);
+    }
     if (named_bar_red_or(1, kDecConsumers, !ok)) {
       if (tid == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
       break;
@@ -514,14 +685,33 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     fence_proxy_async_smem();
     named_bar_sync(1, kDecConsumers);
     const bool more = (flags & kStageMore) != 0;
-    if (tid == 0) {
-      uint16_t* const outp = st.out;  // the stage may be refilled once released
-      mbar_arrive(&sh.empty[s]);
+    if (warp == 0) {
+      // the stage may be refilled once released: read what the store needs first
+      uint16_t* const outp = st.out;
+      const uint64_t tile = st.tile;
+      const uint4 dep = st.dep;
+      __syncwarp();
+      if (tid == 0) mbar_arrive(&sh.empty[s]);
       if (!more) {
-        const uint32_t body = (nt * 2u) & ~15u;
-        if (body) bulk_s2g(outp, outs, body);
-        bulk_commit();
-        for (uint32_t k = body / 2u; k < nt; ++k) outp[k] = outs[k];
+        bool go = true;
+        if constexpr (INPLACE) {
+          // the tiles whose in-place bytes lie under this output have read them
+          go = wait_read_done_warp(ws, tile, dep, uint32_t(lane));
+          if (tid == 0) {
+            if (go) {
+              fence_proxy_async_global();
+            } else {
+              set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+            }
+          }
+        }
+        if (tid == 0) {
+          const uint32_t body = (nt * 2u) & ~15u;
+          if (go && body) bulk_s2g(outp, outs, body);
+          bulk_commit();
+          if (go)
+            for (uint32_t k = body / 2u; k < nt; ++k) outp[k] = outs[k];
+        }
       }
     }
     in_tile = more;
@@ -533,39 +723,77 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
 
 }  // namespace
 
-cudaError_t launch_decode(const Items& items, void* ws_base, cudaStream_t stream, const DeviceInfo& dev) {
-  DecWs ws = dec_ws(ws_base, items.count, items.total_tiles);
-  cudaError_t err = cudaMemsetAsync(ws_base, 0, sizeof(WsHeader), stream);
-  if (err != cudaSuccess) return err;
-  {
-    // blockIdx.y = group of kPrepWarps items; x covers the average item's
-    // 32-tile groups (8 per block) times the items a row takes in turn (1 when
-    // items are of one group or less: their warps need no other block)
-    const uint64_t per_item = items.count ? (items.total_tiles + items.count - 1) / items.count : 0;
-    const uint64_t per_row = items.count < uint32_t(kPrepWarps) ? items.count : uint64_t(kPrepWarps);
-    uint64_t gx = per_item <= kSmallTiles ? 1 : (per_item + 32 * kPrepWarps - 1) / (32 * kPrepWarps) * per_row;
-    if (gx < 1) gx = 1;
-    if (gx > 1024) gx = 1024;
-    const uint64_t groups = (uint64_t(items.count) + kPrepWarps - 1) / kPrepWarps;
-    const unsigned gy = unsigned(groups < 65535u ? (groups ? groups : 1) : 65535u);
-    dec_prepare<<<dim3(unsigned(gx), gy), kPrepWarps * 32, 0, stream>>>(items, ws);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  }
-  if (items.total_tiles == 0) return cudaSuccess;
+namespace {
+
+cudaError_t launch_prepare(const Items& items, const DecWs& ws, cudaStream_t stream, bool inplace) {
+  // blockIdx.y = group of kPrepWarps items; x covers the average item's
+  // 32-tile groups (8 per block) times the items a row takes in turn (1 when
+  // items are of one group or less: their warps need no other block)
+  const uint64_t per_item = items.count ? (items.total_tiles + items.count - 1) / items.count : 0;
+  const uint64_t per_row = items.count < uint32_t(kPrepWarps) ? items.count : uint64_t(kPrepWarps);
+  uint64_t gx = per_item <= kSmallTiles ? 1 : (per_item + 32 * kPrepWarps - 1) / (32 * kPrepWarps) * per_row;
+  if (gx < 1) gx = 1;
+  if (gx > 1024) gx = 1024;
+  const uint64_t groups = (uint64_t(items.count) + kPrepWarps - 1) / kPrepWarps;
+  const unsigned gy = unsigned(groups < 65535u ? (groups ? groups : 1) : 65535u);
+  dec_prepare<<<dim3(unsigned(gx), gy), kPrepWarps * 32, 0, stream>>>(items, ws, inplace);
+  return cudaGetLastError();
+}
+
+template <bool INPLACE>
+cudaError_t launch_main(const Items& items, const DecWs& ws, cudaStream_t stream, const DeviceInfo& dev) {
   static thread_local int configured_device = -1;
+  static thread_local int ctas_per_sm = kDecCtasPerSm;
   const size_t smem = sizeof(DecShared);
+  cudaError_t err;
   if (configured_device != dev.device) {
-    err = cudaFuncSetAttribute(dec_main, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    err = cudaFuncSetAttribute(dec_main<INPLACE>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (err != cudaSuccess) return err;
+    int nb = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, dec_main<INPLACE>, kDecThreads, smem);
+    if (err != cudaSuccess) return err;
+    if (nb < 1) return cudaErrorInvalidConfiguration;
+    ctas_per_sm = nb < kDecCtasPerSm ? nb : kDecCtasPerSm;
     configured_device = dev.device;
   }
-  const uint64_t cap = uint64_t(dev.num_sms) * kDecCtasPerSm;
+  const uint64_t cap = uint64_t(dev.num_sms) * ctas_per_sm;
   const unsigned grid = unsigned(items.total_tiles < cap ? items.total_tiles : cap);
   if (g_timing.before) cudaEventRecord(g_timing.before, stream);
-  dec_main<<<grid, kDecThreads, smem, stream>>>(items, ws);
-  err = cudaGetLastError();
+  if constexpr (INPLACE) {
+    // tiles wait for tiles of other CTAs' runs: every CTA must be resident
+    Items it = items;
+    DecWs w = ws;
+    void* args[] = {&it, &w};
+    err = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(dec_main<true>), dim3(grid), dim3(kDecThreads),
+                                      args, smem, stream);
+  } else {
+    dec_main<false><<<grid, kDecThreads, smem, stream>>>(items, ws);
+    err = cudaGetLastError();
+  }
   if (g_timing.after) cudaEventRecord(g_timing.after, stream);
   return err;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const Items& items, void* ws_base, cudaStream_t stream, const DeviceInfo& dev) {
+  const DecWs ws = dec_ws(ws_base, items.count, items.total_tiles);
+  cudaError_t err = cudaMemsetAsync(ws_base, 0, sizeof(WsHeader), stream);
+  if (err != cudaSuccess || (err = launch_prepare(items, ws, stream, false)) != cudaSuccess) return err;
+  if (items.total_tiles == 0) return cudaSuccess;
+  return launch_main<false>(items, ws, stream, dev);
+}
+
+cudaError_t launch_decode_inplace(const Items& items, void* ws_base, cudaStream_t stream, const DeviceInfo& dev) {
+  const DecWs ws = ip_ws(ws_base, items.count, items.total_tiles);
+  cudaError_t err = cudaMemsetAsync(ws_base, 0, sizeof(WsHeader), stream);
+  if (err != cudaSuccess || (err = launch_prepare(items, ws, stream, true)) != cudaSuccess) return err;
+  if (items.total_tiles == 0) return cudaSuccess;
+  const uint64_t blocks = (items.total_tiles + kStashWarps - 1) / kStashWarps;
+  const uint64_t cap = uint64_t(dev.num_sms) * 32;  // four waves of 8 blocks per SM, then grid-stride
+  dip_stash<<<unsigned(blocks < cap ? blocks : cap), kStashWarps * 32, 0, stream>>>(items, ws);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  return launch_main<true>(items, ws, stream, dev);
 }
 
 }  // namespace sz

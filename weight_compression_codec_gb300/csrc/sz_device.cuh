@@ -212,6 +212,8 @@ struct DecWs {
   uint32_t* item_flags;
   uint2* ranges;
   uint32_t* tile_item;
+  uint32_t* read_done;  // in-place decode: per tile, its in-place input has been read
+  uint8_t* stash;       // in-place decode: the bytes copied aside
 };
 __host__ __device__ inline uint64_t dec_ws_bytes(uint32_t count, uint64_t tiles) {
   return 256 + round_up256(uint64_t(count) * 4) + round_up256(tiles * 8) + tile_map_bytes(dec_uses_tile_map(count), tiles);
@@ -226,6 +228,97 @@ __host__ __device__ inline DecWs dec_ws(void* base, uint32_t count, uint64_t til
   w.ranges = reinterpret_cast<uint2*>(p);
   p += round_up256(tiles * 8);
   w.tile_item = dec_uses_tile_map(count) ? reinterpret_cast<uint32_t*>(p) : nullptr;
+  w.read_done = nullptr;
+  w.stash = nullptr;
+  return w;
+}
+
+// ------------------------------------------------------------------ in-place slot decode
+// The payload occupies the leading comp_bytes of the tensor's own 2n-byte
+// output (its slot) and the weight is decoded over it.  Tiles of a tensor
+// are decoded from the last to the first.  Output tile u covers slot bytes
+// [16384 u, 16384 u + 2 nt); a payload byte read by tile r and overwritten by
+// tile w = byte / 16384 is safe in place when w <= r (the reader comes first,
+// or is the writer itself).  pk bytes of tile t start at 4096 t, so they
+// always are; sm bytes of element i lie at off_sm + i, safe whenever
+// i >= off_sm; the escape streams are not.  So, before the decode, the sm
+// bytes of the first ip_sm_stash_tiles tiles (every element below off_sm)
+// and the whole escape streams are copied to a stash; everything else is
+// read in place, and a tile stores its output only after the tiles whose
+// in-place bytes lie under it have read them (ip_deps).
+
+// tiles whose sm bytes are read from the stash
+__host__ __device__ inline uint64_t ip_sm_stash_tiles(uint64_t n, uint64_t off_sm) {
+  const uint64_t m = n < off_sm ? n : off_sm;
+  return (m + kTile - 1) / kTile;
+}
+
+// Stash of one tensor: payload bytes [floor16(off_sm), off_sm + S) (S = the
+// stashed sm elements) at offset 0 and [floor16(off_cid), comp_bytes) at
+// esc_off; both keep their payload offsets mod 16.
+struct IpStash {
+  uint64_t sm_tiles;  // tiles whose sm bytes come from the stash
+  uint64_t sm_from, sm_to;    // payload byte range of the sm part
+  uint64_t esc_from, esc_to;  // payload byte range of the escape part (empty without escapes)
+  uint64_t esc_off;           // stash offset of the escape part (16-byte multiple)
+  uint64_t bytes;             // stash bytes used
+};
+__host__ __device__ inline IpStash ip_stash(uint64_t n, uint64_t n_esc, uint64_t off_sm, uint64_t off_cid,
+                                            uint64_t comp_bytes) {
+  IpStash s;
+  s.sm_tiles = ip_sm_stash_tiles(n, off_sm);
+  const uint64_t S = (s.sm_tiles * kTile < n) ? s.sm_tiles * kTile : n;
+  s.sm_from = off_sm & ~uint64_t(15);
+  s.sm_to = S ? off_sm + S : s.sm_from;
+  s.esc_from = off_cid & ~uint64_t(15);
+  s.esc_to = n_esc ? comp_bytes : s.esc_from;
+  s.esc_off = (s.sm_to - s.sm_from + 15) & ~uint64_t(15);
+  s.bytes = s.esc_off + (s.esc_to - s.esc_from);
+  return s;
+}
+
+// Stash budget of a tensor of `tiles` tiles: enough for any payload of at
+// most 2n bytes (sm part <= n + 30, escape part <= n - off_sm + 15, with
+// off_sm >= n / 2 and n <= 8192 tiles).
+constexpr uint64_t kIpStashPerTile = 12288;
+constexpr uint64_t kIpStashPerItem = 256;
+__host__ __device__ inline uint64_t ip_stash_at(uint64_t tile_begin, uint32_t item) {
+  return tile_begin * kIpStashPerTile + uint64_t(item) * kIpStashPerItem;
+}
+
+// Tiles (local indices, inclusive ranges, empty when lo > hi) whose in-place
+// bytes lie under output tile u: pk of tiles 4u .. 4u + 3, and in-place sm
+// (tiles >= sm_tiles) of the tiles whose sm bytes meet [16384 u, 16384 u +
+// 16384).  Every such tile is >= u, so it is decoded first.
+struct IpDeps {
+  uint64_t pk_lo, pk_hi, sm_lo, sm_hi;
+};
+__host__ __device__ inline IpDeps ip_deps(uint64_t n, uint64_t off_sm, uint64_t u) {
+  IpDeps d;
+  const uint64_t T = (n + kTile - 1) / kTile;
+  d.pk_lo = 4 * u;
+  d.pk_hi = (4 * u + 3 < T) ? 4 * u + 3 : T - 1;
+  const uint64_t sm_tiles = ip_sm_stash_tiles(n, off_sm);
+  const uint64_t w0 = 2 * kTile * u, w1 = w0 + 2 * kTile;  // the output bytes of tile u (at most)
+  // tile t's sm bytes [off_sm + 8192 t, off_sm + 8192 t + 8192) meet [w0, w1)
+  d.sm_lo = (w0 >= off_sm + kTile) ? (w0 - off_sm - kTile) / kTile + 1 : 0;
+  d.sm_hi = (w1 > off_sm) ? (w1 - off_sm - 1) / kTile : 0;
+  if (w1 <= off_sm) d.sm_lo = 1, d.sm_hi = 0;
+  if (d.sm_lo < sm_tiles) d.sm_lo = sm_tiles;
+  if (d.sm_hi >= T) d.sm_hi = T - 1;
+  return d;
+}
+
+// in-place decode workspace: the decode workspace | read_done[tiles] u32 | stash
+__host__ __device__ inline uint64_t ip_ws_bytes(uint32_t count, uint64_t tiles) {
+  return dec_ws_bytes(count, tiles) + round_up256(tiles * 4) + tiles * kIpStashPerTile +
+         uint64_t(count) * kIpStashPerItem;
+}
+__host__ __device__ inline DecWs ip_ws(void* base, uint32_t count, uint64_t tiles) {
+  DecWs w = dec_ws(base, count, tiles);
+  char* p = static_cast<char*>(base) + dec_ws_bytes(count, tiles);
+  w.read_done = reinterpret_cast<uint32_t*>(p);
+  w.stash = reinterpret_cast<uint8_t*>(p + round_up256(tiles * 4));
   return w;
 }
 
@@ -317,6 +410,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's earlier generic-proxy global accesses (e.g. an
+// acquire that saw another CTA's flag) before its later async-proxy global
+// accesses (a bulk store).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // 16-byte cp.async that reads only `src_bytes` (0..16) bytes and zero-fills
 // the rest of the destination; nothing beyond src + src_bytes is read.
 __device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, uint32_t src_bytes) {
@@ -348,6 +448,10 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
 
 __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Relaxed GPU-scope accesses: coherent single-copy-atomic 64-bit words with
