@@ -88,7 +88,8 @@ struct WsHeader {
   uint32_t flags;        // SZ_FLAG_* bits
   uint32_t pad0;
   unsigned long long ticket;  // dynamic tile counter (encode)
-  uint32_t reserved[60];
+  uint32_t tiles_differ;      // in-place decode: set when the tensors' tile counts are not all equal
+  uint32_t reserved[59];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
@@ -448,6 +449,12 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
 
 __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
