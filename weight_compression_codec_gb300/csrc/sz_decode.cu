@@ -60,9 +60,26 @@ struct __align__(128) DecStage {
   uint4 dep;      // in-place decode: tiles [tile + x, tile + y] and [tile + z, tile + w] to wait for
 };
 
+// What the producer needs of one tile, resolved by one lane of the producer
+// warp when a window of tiles starts (kept in shared memory, not registers,
+// so the producer's loop stays light on registers).
+constexpr uint32_t kWin = 16;
+struct WinEntry {
+  const uint8_t* base;  // payload
+  uint16_t* out;        // the tile's first output element
+  uint64_t off_sm, off_cid, off_lpos, off_ev;
+  uint64_t smv, escv;   // in place: address of payload byte 0 in the sm / escape source
+  uint64_t tile;        // flat tile index (in place: kNoTile for a hole past a tensor's end)
+  uint4 dec_lut;
+  uint4 dep;            // in place: tiles to wait for (as DecStage::dep)
+  uint32_t k0, k1, lt, nt;
+  uint32_t ok, pad[3];
+};
+
 struct DecShared {
   DecStage st[kDecStages];
   alignas(128) uint16_t out[2][kTile];
+  WinEntry win[kWin];
   uint64_t full[kDecStages];
   uint64_t empty[kDecStages];
 };
@@ -474,20 +491,11 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
 
   if (warp == kDecConsumerWarps) {
     // ---------------------------------------------------------------- producer warp
-    // Lane l holds what the producer needs of tile l of the current window,
-    // resolved in parallel when the window starts: the escape range, the
-    // item (tile -> item map), its payload, output, dec_lut and section
-    // offsets (in-place: also the sm and escape sources and the tiles to
-    // wait for).
-    bool w_ok = false;
-    uint2 w_rec = make_uint2(0, 0);
-    const uint8_t* w_base = nullptr;
-    uint16_t* w_out = nullptr;
-    uint64_t w_g = 0, w_off_sm = 0, w_off_cid = 0, w_off_lpos = 0, w_off_ev = 0;
-    uint64_t w_smv = 0, w_escv = 0;  // in-place: address of payload byte 0 in the sm / escape source
-    uint4 w_dep = make_uint4(1, 0, 1, 0);
-    uint4 w_dlut = make_uint4(0, 0, 0, 0);
-    uint32_t w_lt = 0, w_nt = 0;
+    // When a window of kWin tiles starts, lane l resolves tile l of it in
+    // parallel (escape range, item through the tile -> item map, payload,
+    // output, dec_lut, section offsets; in place also the sm and escape
+    // sources and the tiles to wait for) into sh.win[l]; then the tiles are
+    // issued one by one from that table.
     uint64_t it = 0;  // stages handed out
     // next free stage of the ring (bounded wait agreed by the warp)
     auto acquire = [&](int& s) -> bool {
@@ -499,12 +507,6 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
       }
       return true;
     };
-    auto shfl64 = [&](uint64_t v, uint32_t from) {
-      return (uint64_t(__shfl_sync(0xFFFFFFFFu, uint32_t(v >> 32), from)) << 32) |
-             __shfl_sync(0xFFFFFFFFu, uint32_t(v), from);
-    };
-    // next / t1: the CTA's range of tiles, or (in place) of its tickets' ranks
-    // (rank r <-> ticket blockIdx.x + r R)
     // next / t1: the CTA's range of tiles, or (in place) of its positions k
     // (k <-> position k % C of chunk ticket blockIdx.x + (k / C) R)
     uint64_t next = 0, t1 = 0;
@@ -521,11 +523,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
       t1 = (next + per < T) ? next + per : T;
     }
     uint32_t win_len = 0, win_pos = 0;
-    uint64_t w_tile = 0;  // lane l: the tile of window entry l (in place: kNoTile for a hole)
     for (;;) {
       if (win_pos == win_len) {
         const uint64_t first = next;
-        win_len = next < t1 ? uint32_t((t1 - next < 32) ? t1 - next : 32) : 0u;
+        win_len = next < t1 ? uint32_t((t1 - next < kWin) ? t1 - next : kWin) : 0u;
         next += win_len;
         win_pos = 0;
         if (win_len == 0) {
@@ -538,50 +539,62 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
           cp_async_mbar_arrive_noinc(&sh.full[s]);
           return;
         }
-        const uint64_t k = first + lane;
-        const uint64_t mine =
-            INPLACE ? ip_tile_of(blockIdx.x + (k / C) * R, k % C, T, items.count, Tu, C) : k;
-        w_tile = mine;
-        w_ok = false;
-        if (uint32_t(lane) < win_len && mine != kNoTile) {
-          w_rec = ws.ranges[mine];
-          const uint32_t idx = ws.tile_item ? ws.tile_item[mine] : 0u;
-          if (idx < items.count && w_rec.x != kRangeInvalid && ws.item_flags[idx] == 0) {
-            const sz_item& itm = item_at(items, idx);
-            const uint64_t tb = itm.tile_begin;
-            if (mine >= tb && mine - tb < tiles_of(itm.n)) {
-              w_lt = uint32_t(mine - tb);
-              w_g = uint64_t(w_lt) * kTile;
-              w_nt = (itm.n - w_g < kTile) ? uint32_t(itm.n - w_g) : kTile;
-              w_base = itm.payload;
-              w_out = itm.out + w_g;
-              const sz_meta* mp = itm.meta;
-              w_off_sm = mp->off_sm;
-              w_off_cid = mp->off_cid;
-              w_off_lpos = mp->off_lpos;
-              w_off_ev = mp->off_ev;
-              w_dlut = *reinterpret_cast<const uint4*>(itm.codebook->dec_lut);
-              if constexpr (INPLACE) {
-                const IpStash sv = ip_stash(itm.n, mp->n_esc, w_off_sm, w_off_cid, mp->comp_bytes);
-                const uint64_t sb = reinterpret_cast<uint64_t>(ws.stash) + ip_stash_at(tb, idx);
-                w_smv = (w_lt < sv.sm_tiles) ? sb - sv.sm_from : reinterpret_cast<uint64_t>(itm.payload);
-                w_escv = sb + sv.esc_off - sv.esc_from;
-                const IpDeps d = ip_deps(itm.n, w_off_sm, w_lt);
-                w_dep = make_uint4(1, 0, 1, 0);
-                if (d.pk_lo <= d.pk_hi) w_dep.x = uint32_t(d.pk_lo - w_lt), w_dep.y = uint32_t(d.pk_hi - w_lt);
-                if (d.sm_lo <= d.sm_hi) w_dep.z = uint32_t(d.sm_lo - w_lt), w_dep.w = uint32_t(d.sm_hi - w_lt);
+        __syncwarp();  // every lane is done with the previous window's entries
+        if (uint32_t(lane) < win_len) {
+          const uint64_t k = first + lane;
+          const uint64_t mine =
+              INPLACE ? ip_tile_of(blockIdx.x + (k / C) * R, k % C, T, items.count, Tu, C) : k;
+          WinEntry& w = sh.win[lane];
+          w.tile = mine;
+          uint32_t ok = 0;
+          if (mine != kNoTile) {
+            const uint2 rec = ws.ranges[mine];
+            const uint32_t idx = ws.tile_item ? ws.tile_item[mine] : 0u;
+            if (idx < items.count && rec.x != kRangeInvalid && ws.item_flags[idx] == 0) {
+              const sz_item& itm = item_at(items, idx);
+              const uint64_t tb = itm.tile_begin;
+              if (mine >= tb && mine - tb < tiles_of(itm.n)) {
+                const uint32_t lt = uint32_t(mine - tb);
+                const uint64_t g = uint64_t(lt) * kTile;
+                const sz_meta* mp = itm.meta;
+                w.k0 = rec.x;
+                w.k1 = rec.y;
+                w.lt = lt;
+                w.nt = (itm.n - g < kTile) ? uint32_t(itm.n - g) : kTile;
+                w.base = itm.payload;
+                w.out = itm.out + g;
+                w.off_sm = mp->off_sm;
+                w.off_cid = mp->off_cid;
+                w.off_lpos = mp->off_lpos;
+                w.off_ev = mp->off_ev;
+                w.dec_lut = *reinterpret_cast<const uint4*>(itm.codebook->dec_lut);
+                if constexpr (INPLACE) {
+                  const IpStash sv = ip_stash(itm.n, mp->n_esc, w.off_sm, w.off_cid, mp->comp_bytes);
+                  const uint64_t sb = reinterpret_cast<uint64_t>(ws.stash) + ip_stash_at(tb, idx);
+                  w.smv = (lt < sv.sm_tiles) ? sb - sv.sm_from : reinterpret_cast<uint64_t>(itm.payload);
+                  w.escv = sb + sv.esc_off - sv.esc_from;
+                  const IpDeps d = ip_deps(itm.n, w.off_sm, lt);
+                  uint4 dep = make_uint4(1, 0, 1, 0);
+                  if (d.pk_lo <= d.pk_hi) dep.x = uint32_t(d.pk_lo - lt), dep.y = uint32_t(d.pk_hi - lt);
+                  if (d.sm_lo <= d.sm_hi) dep.z = uint32_t(d.sm_lo - lt), dep.w = uint32_t(d.sm_hi - lt);
+                  w.dep = dep;
+                } else {
+                  w.smv = w.escv = reinterpret_cast<uint64_t>(itm.payload);
+                }
+                ok = 1;
               }
-              w_ok = true;
             }
           }
+          w.ok = ok;
         }
+        __syncwarp();
       }
-      const uint32_t src = win_pos++;
-      const uint64_t tile = shfl64(w_tile, src);
+      const WinEntry& w = sh.win[win_pos++];
+      const uint64_t tile = w.tile;
       if (INPLACE && tile == kNoTile) continue;  // past the end of a tensor: no stage
       int s;
       if (!acquire(s)) return;
-      if (!__shfl_sync(0xFFFFFFFFu, w_ok, src)) {
+      if (!w.ok) {
         if (lane == 0) {
           sh.st[s].flags = kStageInvalid;
           sh.st[s].tile = tile;
@@ -591,31 +604,12 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
         ++it;
         continue;
       }
-      const uint32_t k0 = __shfl_sync(0xFFFFFFFFu, w_rec.x, src);
-      const uint32_t k1 = __shfl_sync(0xFFFFFFFFu, w_rec.y, src);
-      const uint32_t lt = __shfl_sync(0xFFFFFFFFu, w_lt, src);
-      const uint32_t nt = __shfl_sync(0xFFFFFFFFu, w_nt, src);
-      const uint64_t g = shfl64(w_g, src);
-      const uint64_t off_sm = shfl64(w_off_sm, src), off_cid = shfl64(w_off_cid, src),
-                     off_lpos = shfl64(w_off_lpos, src), off_ev = shfl64(w_off_ev, src);
-      const uint8_t* base = reinterpret_cast<const uint8_t*>(shfl64(reinterpret_cast<uint64_t>(w_base), src));
-      const uint8_t* sm_src = base;   // where payload byte 0 of the sm section's source is
-      const uint8_t* esc_src = base;  // ... of the escape streams' source
-      uint4 dep = make_uint4(1, 0, 1, 0);
-      if constexpr (INPLACE) {
-        sm_src = reinterpret_cast<const uint8_t*>(shfl64(w_smv, src));
-        esc_src = reinterpret_cast<const uint8_t*>(shfl64(w_escv, src));
-        dep.x = __shfl_sync(0xFFFFFFFFu, w_dep.x, src);
-        dep.y = __shfl_sync(0xFFFFFFFFu, w_dep.y, src);
-        dep.z = __shfl_sync(0xFFFFFFFFu, w_dep.z, src);
-        dep.w = __shfl_sync(0xFFFFFFFFu, w_dep.w, src);
-      }
-      uint16_t* const out_t = reinterpret_cast<uint16_t*>(shfl64(reinterpret_cast<uint64_t>(w_out), src));
-      uint4 dlut;
-      dlut.x = __shfl_sync(0xFFFFFFFFu, w_dlut.x, src);
-      dlut.y = __shfl_sync(0xFFFFFFFFu, w_dlut.y, src);
-      dlut.z = __shfl_sync(0xFFFFFFFFu, w_dlut.z, src);
-      dlut.w = __shfl_sync(0xFFFFFFFFu, w_dlut.w, src);
+      const uint32_t k0 = w.k0, k1 = w.k1, lt = w.lt, nt = w.nt;
+      const uint64_t g = uint64_t(lt) * kTile;
+      const uint64_t off_sm = w.off_sm, off_cid = w.off_cid, off_lpos = w.off_lpos, off_ev = w.off_ev;
+      const uint8_t* base = w.base;
+      const uint8_t* sm_src = reinterpret_cast<const uint8_t*>(w.smv);    // payload byte 0 of the sm source
+      const uint8_t* esc_src = reinterpret_cast<const uint8_t*>(w.escv);  // ... of the escape streams' source
       const uint32_t m = (k1 > k0) ? k1 - k0 : 0u;
       const uint32_t pieces = m ? (m + kEcap - 1) / kEcap : 1u;
       const Slice spk = slice_of(g >> 1, (nt + 1) >> 1);
@@ -635,14 +629,14 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
                             (pm ? uint32_t(scid.a1 - scid.a0) + uint32_t(slp.a1 - slp.a0) + uint32_t(sev.a1 - sev.a0)
                                 : 0u);
         if (lane == 0) {
-          st.dec_lut = dlut;
-          st.out = out_t;
+          st.dec_lut = w.dec_lut;
+          st.out = w.out;
           st.m = pm;
           st.lt = lt;
           st.n_tile = nt;
           st.flags = (first ? 0u : kStageCont) | (pc + 1 < pieces ? kStageMore : 0u);
           st.tile = tile;
-          st.dep = dep;
+          if constexpr (INPLACE) st.dep = w.dep;
           st.sm_shift = uint32_t(off_sm + g - ssm.a0);
           st.cid_shift = uint32_t(off_cid + 4ull * pk0 - scid.a0);
           st.lpos_shift = uint32_t(off_lpos + 2ull * pk0 - slp.a0);
