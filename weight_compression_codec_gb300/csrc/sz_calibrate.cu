@@ -61,6 +61,7 @@ struct CalShared {
   uint64_t sel_full[2];
   uint64_t sel_empty[2];
   SelectScratch sel;  // select warp scratch
+  uint64_t fbar;      // the counting warps meet here when counts are flushed
   int s_last;
 };
 
@@ -112,6 +113,7 @@ __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __g
       mbar_init(&sh.sel_full[b], 1);
       mbar_init(&sh.sel_empty[b], 1);
     }
+    mbar_init(&sh.fbar, kCountWarps);
     fence_mbar_init();
   }
   __syncthreads();
@@ -219,67 +221,80 @@ __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __g
   }
 
   // ------------------------------------------------------------------ counting warps
+  // Each warp waits for its stages on its own (no lock-step between warps:
+  // a warp may run up to the ring's depth ahead of another); the warps meet
+  // only when counts are flushed, on an mbarrier with bounded waits, so a
+  // timed-out warp unwinds instead of leaving the others waiting.
   // this lane's counter column, as a byte address: bin b at col + 128 * b
   char* const col = reinterpret_cast<char*>(sh.cnt + lane);
   uint32_t cur = 0xFFFFFFFFu;
   uint32_t run = 0;    // tiles of `cur` counted since the last flush
   uint32_t posts = 0;  // histograms handed to the select warp
-  // Waits until buffer posts & 1 is free again (its previous histogram ranked).
-  auto wait_buffer = [&]() {
-    if (posts >= 2 && !mbar_wait(&sh.sel_empty[posts & 1u], ((posts >> 1) - 1) & 1u) && lane == 0)
-      set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+  uint32_t meets = 0;  // completed phases of sh.fbar
+  auto meet = [&]() -> bool {  // all counting warps here; writes before it visible after it
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.fbar);
+    const bool ok = __all_sync(FULL, mbar_wait(&sh.fbar, meets & 1u));
+    ++meets;
+    if (!ok && lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+    return ok;
   };
-  auto post = [&](uint32_t item) {  // after a named barrier over the counting threads
+  // Waits until buffer posts & 1 is free again (its previous histogram ranked).
+  auto wait_buffer = [&]() -> bool {
+    if (posts < 2) return true;
+    const bool ok = __all_sync(FULL, mbar_wait(&sh.sel_empty[posts & 1u], ((posts >> 1) - 1) & 1u));
+    if (!ok && lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+    return ok;
+  };
+  auto post = [&](uint32_t item) {  // after a meet
     if (tid == 0) {
       sh.sel_item[posts & 1u] = item;
       mbar_arrive(&sh.sel_full[posts & 1u]);
     }
     ++posts;
   };
-  auto flush = [&]() {
-    named_bar_sync(1, kCountThreads);  // every count of the tensor's tiles is in
+  auto flush = [&]() -> bool {
+    if (!meet()) return false;  // every count of the tensor's tiles is in
     const uint32_t sum = take_bin(sh.cnt, tid);  // thread b sums and clears bin b
     const uint64_t tiles = tiles_of(item_at(items, cur).n);
     if (uint64_t(run) == tiles) {
       // this CTA counted every tile of the tensor: hand the sums over directly
-      wait_buffer();
+      if (!wait_buffer()) return false;
       sh.h[posts & 1u][tid] = sum;
-      named_bar_sync(1, kCountThreads);  // sums written; counters clear for the next tensor
+      if (!meet()) return false;  // sums written; counters clear for the next tensor
       post(cur);
     } else {
       uint32_t* gh = ws.hist + uint64_t(cur) * 256;
       if (sum) atomicAdd(gh + tid, sum);
       __threadfence();
-      named_bar_sync(1, kCountThreads);
+      if (!meet()) return false;
       if (tid == 0) {
         const uint32_t old = atomicAdd(ws.done + cur, run);
         sh.s_last = ((old & kItemInvalid) == 0) && (uint64_t(old) + run == tiles);
       }
-      named_bar_sync(1, kCountThreads);
+      if (!meet()) return false;
       if (sh.s_last) {
         // the last CTA to add its counts ranks the tensor
         __threadfence();
-        wait_buffer();
+        if (!wait_buffer()) return false;
         sh.h[posts & 1u][tid] = __ldcg(gh + tid);
-        named_bar_sync(1, kCountThreads);
+        if (!meet()) return false;
         post(cur);
       }
     }
     run = 0;
+    return true;
   };
-  bool timed_out = false;
   for (uint32_t it = 0;; ++it) {
     const int s = int(it % kCalStages);
-    const bool ok = mbar_wait(&sh.full[s], (it / kCalStages) & 1);
-    const CalHdr hd = sh.hdr[s];  // read before the vote: the stage may be released right after
-    if (named_bar_red_or(1, kCountThreads, !ok)) {
-      if (tid == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
-      timed_out = true;
-      break;
+    if (!__all_sync(FULL, mbar_wait(&sh.full[s], (it / kCalStages) & 1))) {
+      if (lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+      return;  // the select warp stops on its own timeout
     }
+    const CalHdr hd = sh.hdr[s];
     if (hd.flags & kStageEnd) break;
     if (hd.item != cur) {
-      if (run) flush();
+      if (run && !flush()) return;
       cur = hd.item;
     }
     if (!(hd.flags & kStageInvalid)) {
@@ -289,10 +304,9 @@ __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __g
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty[s]);
   }
-  if (run && !timed_out) flush();
+  if (run && !flush()) return;
   // tell the select warp to stop once it has ranked everything posted
-  wait_buffer();
-  named_bar_sync(1, kCountThreads);
+  if (!wait_buffer() || !meet()) return;
   post(kSelectEnd);
 }
 
