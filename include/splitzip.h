@@ -236,15 +236,16 @@ SZ_API int sz_decode_many(const sz_item* d_items, uint32_t count, uint64_t total
  * BF16 destination, 2n bytes, 16-byte aligned, whose leading comp_bytes hold
  * the payload described by *d_meta (the bytes after it are ignored).  After
  * the call the slot holds the n decoded values.  The pages' decoder copies
- * the whole payload aside first; here only the bytes that a last-tile-first
- * decode would overwrite before reading them (the sm bytes of elements below
- * off_sm and the escape streams) are copied to the workspace, and each tile
- * is stored once the tiles whose payload bytes lie under it have been read.
+ * the whole payload aside first; here the tiles are decoded in an order
+ * that reads nearly everything in place (see sz_inplace_plan) and only the
+ * pk bytes of about a quarter of the tiles and the escape streams (about
+ * n / 8 + 7 n_esc bytes) are copied to the workspace; each tile is stored
+ * once the tiles whose payload bytes lie under it have been read.
  * A payload larger than 2n bytes cannot be in the slot: SZ_FLAG_META, slot
  * untouched (as for a meta that disagrees with the layout).  A meta with
  * SZ_META_GATED means the slot already holds the raw tensor: nothing is
  * written.  Workspace: sz_decode_inplace_workspace_bytes(1, tiles(n))
- * (decode workspace + 4 bytes and 12 KiB per tile + 256 bytes per tensor),
+ * (decode workspace + 4 bytes and 8 KiB per tile + 4352 bytes per tensor),
  * 256-byte aligned. */
 SZ_API int sz_decode_inplace(uint16_t* d_slot, uint64_t n, const sz_meta* d_meta, const sz_codebook* d_codebook,
                              void* d_workspace, size_t workspace_bytes, sz_stream stream);
@@ -254,19 +255,25 @@ SZ_API int sz_decode_inplace_many(const sz_item* d_items, uint32_t count, uint64
                                   void* d_workspace, size_t workspace_bytes, sz_stream stream);
 SZ_API size_t sz_decode_inplace_workspace_bytes(uint32_t count, uint64_t total_tiles);
 
-/* The in-place schedule of one tile, for inspection (host only): which
- * payload bytes are copied to the stash and which tiles must have read their
- * payload bytes before tile `tile` stores its output (local tile indices,
- * inclusive ranges, empty when lo > hi).  SZ_ERR_ARG for n == 0, n out of
- * range, n_esc > n or tile >= tiles(n); SZ_ERR_CAPACITY if the payload of
- * (n, n_esc) is larger than 2n bytes. */
+/* The in-place schedule of one tile, for inspection (host only).  Tiles of a
+ * tensor are decoded in three phases: A = [phase_a_first, tiles) from the
+ * top down, B = [0, phase_b_end) from the top down, then C = [phase_b_end,
+ * phase_a_first) from the bottom up; `rank` is the tile's position in that
+ * order.  The payload bytes copied to the stash before the decode are the pk
+ * bytes of phase C and the escape streams.  Before tile `tile` stores its
+ * output, the tiles whose in-place payload bytes lie under it must have read
+ * them (local tile indices, inclusive ranges, empty when lo > hi; the tile
+ * itself may appear).  SZ_ERR_ARG for n == 0, n out of range, n_esc > n or
+ * tile >= tiles(n); SZ_ERR_CAPACITY if the payload of (n, n_esc) is larger
+ * than 2n bytes. */
 typedef struct sz_inplace_tile {
-  uint64_t sm_stash_tiles;                /* tiles whose sm bytes are read from the stash   */
-  uint64_t stash_sm_from, stash_sm_to;    /* payload bytes stashed: sm part                 */
-  uint64_t stash_esc_from, stash_esc_to;  /* payload bytes stashed: escape streams          */
-  uint64_t stash_bytes, stash_budget;     /* stash bytes used / reserved for the tensor     */
-  uint64_t pk_lo, pk_hi;                  /* tiles whose pk bytes lie under this output     */
-  uint64_t sm_lo, sm_hi;                  /* tiles whose in-place sm bytes lie under it     */
+  uint64_t tiles, phase_a_first, phase_b_end;  /* T, tA = ceil(off_sm / 8192), tB = off_sm / 16384 */
+  uint64_t rank;                               /* position of `tile` in the decode order          */
+  uint64_t stash_pk_from, stash_pk_to;         /* payload bytes stashed: pk of phase C             */
+  uint64_t stash_esc_from, stash_esc_to;       /* payload bytes stashed: escape streams            */
+  uint64_t stash_bytes, stash_budget;          /* stash bytes used / reserved for the tensor       */
+  uint64_t pk_lo, pk_hi, pk2_lo, pk2_hi;       /* tiles whose pk bytes lie under this output       */
+  uint64_t sm_lo, sm_hi;                       /* tiles whose sm bytes lie under it                */
 } sz_inplace_tile;
 SZ_API int sz_inplace_plan(uint64_t n, uint64_t n_esc, uint64_t tile, sz_inplace_tile* h_out);
 

@@ -188,12 +188,12 @@ def _inplace_cases():
 
 @pytest.mark.parametrize("n,e", _inplace_cases())
 def test_inplace_schedule_covers_every_payload_byte(lib, n, e):
-    """For the last-tile-first decode over the slot: every payload byte that
-    is read in place is overwritten (slot byte b belongs to output tile
-    b // 16384) only by its own reader's tile or by a tile that waits for its
-    reader; every other byte is in the stash; readers waited for are never
-    lower tiles (so the descending order cannot deadlock); the stash fits its
-    budget."""
+    """For the decode over the slot, in the plan's order: every payload byte
+    read in place is overwritten (slot byte b belongs to output tile
+    b // 16384) only by its own reader's tile or by a later tile that waits
+    for its reader; every other byte read is in the stash; every tile waited
+    for comes earlier in the order (so the schedule cannot deadlock); the
+    order is a permutation; the stash fits its budget."""
     m = sz.sz_layout(n, e)
     if m.comp_bytes > 2 * n:
         with pytest.raises(B.SplitZipError):
@@ -202,41 +202,50 @@ def test_inplace_schedule_covers_every_payload_byte(lib, n, e):
     T = (n + 8191) // 8192
     plans = [sz.inplace_plan(n, e, u) for u in range(T)]
     p0 = plans[0]
-    assert all((p["sm_stash_tiles"], p["stash_sm_from"], p["stash_sm_to"], p["stash_esc_from"], p["stash_esc_to"])
-               == (p0["sm_stash_tiles"], p0["stash_sm_from"], p0["stash_sm_to"], p0["stash_esc_from"],
-                   p0["stash_esc_to"]) for p in plans)
-    assert p0["stash_bytes"] <= p0["stash_budget"]
-    for u, p in enumerate(plans):
-        for lo, hi in ((p["pk_lo"], p["pk_hi"]), (p["sm_lo"], p["sm_hi"])):
-            if lo <= hi:
-                assert u <= lo and hi < T
-    dep_lo = np.array([[p["pk_lo"], p["sm_lo"]] for p in plans], dtype=np.int64)
-    dep_hi = np.array([[p["pk_hi"], p["sm_hi"]] for p in plans], dtype=np.int64)
+    for p in plans:
+        for k in ("tiles", "phase_a_first", "phase_b_end", "stash_pk_from", "stash_pk_to", "stash_esc_from",
+                  "stash_esc_to", "stash_bytes", "stash_budget"):
+            assert p[k] == p0[k]
+    assert p0["tiles"] == T and p0["stash_bytes"] <= p0["stash_budget"]
+    tA, tB = p0["phase_a_first"], p0["phase_b_end"]
+    assert 0 <= tB <= tA <= T
+    rank = np.array([p["rank"] for p in plans], dtype=np.int64)
+    assert sorted(rank.tolist()) == list(range(T))
+    ranges = np.array([[p["pk_lo"], p["pk_hi"], p["pk2_lo"], p["pk2_hi"], p["sm_lo"], p["sm_hi"]] for p in plans],
+                      dtype=np.int64)
+    for u in range(T):
+        for lo, hi in ranges[u].reshape(3, 2):
+            for d in range(lo, hi + 1):
+                assert 0 <= d < T and (d == u or rank[d] < rank[u]), (u, d)
 
     def check_in_place(b, r):
         w = b // 16384
         assert np.all(w < T)
-        assert np.all(w <= r), "a byte is overwritten by a tile decoded before its reader"
-        later = w < r
-        ww, rr = w[later], r[later]
-        ok = ((dep_lo[ww, 0] <= rr) & (rr <= dep_hi[ww, 0])) | ((dep_lo[ww, 1] <= rr) & (rr <= dep_hi[ww, 1]))
+        other = w != r
+        ww, rr = w[other], r[other]
+        assert np.all(rank[rr] < rank[ww]), "a byte is overwritten by a tile decoded before its reader"
+        rg = ranges[ww]
+        ok = np.zeros(ww.size, dtype=bool)
+        for k in range(3):
+            ok |= (rg[:, 2 * k] <= rr) & (rr <= rg[:, 2 * k + 1])
         assert np.all(ok), "a tile stores over bytes whose reader it does not wait for"
 
-    # pk: element i's code is in byte i // 2, read by tile i // 8192
+    # pk: element i's code is in byte i // 2, read by tile i // 8192; phase C's pk comes from the stash
     b = np.arange(m.n_pairs, dtype=np.int64)
-    check_in_place(b, b // 4096)
-    # sm: element i's byte at off_sm + i, read by tile i // 8192
+    r = b // 4096
+    stashed = (tB <= r) & (r < tA)
+    assert np.all((p0["stash_pk_from"] <= b[stashed]) & (b[stashed] < p0["stash_pk_to"]))
+    check_in_place(b[~stashed], r[~stashed])
+    # sm: element i's byte at off_sm + i, read by tile i // 8192, always in place
     i = np.arange(n, dtype=np.int64)
-    r = i // 8192
-    stashed = r < p0["sm_stash_tiles"]
-    sb = m.off_sm + i[stashed]
-    assert np.all((p0["stash_sm_from"] <= sb) & (sb < p0["stash_sm_to"]))
-    check_in_place(m.off_sm + i[~stashed], r[~stashed])
+    check_in_place(m.off_sm + i, i // 8192)
     # escape streams: stashed whole
     if e:
         assert p0["stash_esc_from"] <= m.off_cid and p0["stash_esc_to"] >= m.off_ev + e
     else:
         assert p0["stash_esc_to"] == p0["stash_esc_from"]
+    # the stash is about n / 8 + 7 e bytes (the whole payload is 1.5 n + 7 e)
+    assert p0["stash_pk_to"] - p0["stash_pk_from"] <= n // 8 + 8200
 
 
 def test_inplace_plan_rejects_bad_arguments(lib):
@@ -247,4 +256,4 @@ def test_inplace_plan_rejects_bad_arguments(lib):
     assert lib.sz_inplace_plan(1, 0, 0, ctypes.byref(t)) == B.SZ_ERR_CAPACITY  # 8-byte payload, 2-byte slot
     assert lib.sz_inplace_plan(8192, 0, 0, None) == B.SZ_ERR_ARG
     assert lib.sz_decode_inplace_workspace_bytes(3, 10) == (lib.sz_decode_workspace_bytes(3, 10) + 256
-                                                            + 10 * 12288 + 3 * 256)
+                                                            + 10 * 8192 + 3 * 4352)

@@ -85,8 +85,8 @@ class SzGateReport(ctypes.Structure):
 
 class SzInplaceTile(ctypes.Structure):
     _fields_ = [(name, ctypes.c_uint64) for name in (
-        "sm_stash_tiles", "stash_sm_from", "stash_sm_to", "stash_esc_from", "stash_esc_to", "stash_bytes",
-        "stash_budget", "pk_lo", "pk_hi", "sm_lo", "sm_hi")]
+        "tiles", "phase_a_first", "phase_b_end", "rank", "stash_pk_from", "stash_pk_to", "stash_esc_from",
+        "stash_esc_to", "stash_bytes", "stash_budget", "pk_lo", "pk_hi", "pk2_lo", "pk2_hi", "sm_lo", "sm_hi")]
 
 
 CODEBOOK_BYTES = 304

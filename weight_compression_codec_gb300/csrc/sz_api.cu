@@ -141,16 +141,22 @@ SZ_API int sz_inplace_plan(uint64_t n, uint64_t n_esc, uint64_t tile, sz_inplace
   const Layout l = layout_of(n, n_esc);
   if (l.comp_bytes > 2 * n) return SZ_ERR_CAPACITY;
   const IpStash st = ip_stash(n, n_esc, l.off_sm, l.off_cid, l.comp_bytes);
+  const IpPhases ph = ip_phases(n, l.off_sm);
   const IpDeps d = ip_deps(n, l.off_sm, tile);
-  h_out->sm_stash_tiles = st.sm_tiles;
-  h_out->stash_sm_from = st.sm_from;
-  h_out->stash_sm_to = st.sm_to;
+  h_out->tiles = ph.T;
+  h_out->phase_a_first = ph.tA;
+  h_out->phase_b_end = ph.tB;
+  h_out->rank = ip_rank(ph, tile);
+  h_out->stash_pk_from = st.pk_from;
+  h_out->stash_pk_to = st.pk_to;
   h_out->stash_esc_from = st.esc_from;
   h_out->stash_esc_to = st.esc_to;
   h_out->stash_bytes = st.bytes;
   h_out->stash_budget = tiles_of(n) * kIpStashPerTile + kIpStashPerItem;
   h_out->pk_lo = d.pk_lo;
   h_out->pk_hi = d.pk_hi;
+  h_out->pk2_lo = d.pk2_lo;
+  h_out->pk2_hi = d.pk2_hi;
   h_out->sm_lo = d.sm_lo;
   h_out->sm_hi = d.sm_hi;
   return SZ_OK;

@@ -57,7 +57,8 @@ struct __align__(128) DecStage {
   uint32_t m, lt, n_tile, flags;
   uint32_t sm_shift, cid_shift, lpos_shift, ev_shift;
   uint64_t tile;  // flat tile index (in-place decode: its read_done word)
-  uint4 dep;      // in-place decode: tiles [tile + x, tile + y] and [tile + z, tile + w] to wait for
+  uint4 dep;      // in-place decode: tiles (local indices) [x, y] and [z, w] to wait for ...
+  uint2 dep2;     // ... and [x, y]
 };
 
 // What the producer needs of one tile, resolved by one lane of the producer
@@ -68,12 +69,13 @@ struct WinEntry {
   const uint8_t* base;  // payload
   uint16_t* out;        // the tile's first output element
   uint64_t off_sm, off_cid, off_lpos, off_ev;
-  uint64_t smv, escv;   // in place: address of payload byte 0 in the sm / escape source
+  uint64_t pkv, escv;   // address of payload byte 0 in the pk / escape source (in place: maybe the stash)
   uint64_t tile;        // flat tile index (in place: kNoTile for a hole past a tensor's end)
   uint4 dec_lut;
-  uint4 dep;            // in place: tiles to wait for (as DecStage::dep)
+  uint4 dep;            // in place: tiles to wait for (as DecStage::dep, dep2)
+  uint2 dep2;
   uint32_t k0, k1, lt, nt;
-  uint32_t ok, pad[3];
+  uint32_t ok;
 };
 
 struct DecShared {
@@ -328,11 +330,10 @@ constexpr uint64_t kIpEscPiece = 16384;  // escape-stream bytes stashed per tile
 constexpr int kStashWarps = 8;
 
 // In-place decode, before the main pass: per tile (one warp each), clears
-// its read_done word and copies its share of the bytes that the descending
-// decode would overwrite before reading them: its own sm bytes when it is
-// one of the first ip_sm_stash_tiles tiles, and the escape streams' 16 KiB
-// piece with its index (the escape part is at most n / 2 + 15 bytes, so the
-// tiles cover it).
+// its read_done word and copies its share of the bytes the decode order
+// would overwrite before reading them: its own pk bytes when it is a tile of
+// phase C, and the escape streams' 16 KiB piece with its index (the escape
+// part is at most n / 2 + 15 bytes, so the tiles cover it).
 __global__ void __launch_bounds__(kStashWarps * 32, 4) dip_stash(const __grid_constant__ Items items, DecWs ws) {
   if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
   const uint32_t lane = threadIdx.x & 31u;
@@ -349,11 +350,9 @@ __global__ void __launch_bounds__(kStashWarps * 32, 4) dip_stash(const __grid_co
     const uint64_t off_sm = mp->off_sm;
     const IpStash st = ip_stash(it.n, mp->n_esc, off_sm, mp->off_cid, mp->comp_bytes);
     const uint64_t base = reinterpret_cast<uint64_t>(ws.stash) + ip_stash_at(tb, idx);
-    if (lt < st.sm_tiles) {
-      const uint64_t a = lt == 0 ? st.sm_from : off_sm + lt * kTile;
-      const uint64_t b = (off_sm + (lt + 1) * kTile < st.sm_to) ? off_sm + (lt + 1) * kTile : st.sm_to;
-      stash_copy_warp(base - st.sm_from, it.payload, a, b, lane);
-    }
+    const uint64_t pa = lt * (kTile / 2), pb = (lt + 1) * (kTile / 2);  // the tile's pk bytes
+    if (pa >= st.pk_from && pa < st.pk_to)
+      stash_copy_warp(base - st.pk_from, it.payload, pa, pb < st.pk_to ? pb : st.pk_to, lane);
     const uint64_t ea = st.esc_from + lt * kIpEscPiece;
     if (ea < st.esc_to)
       stash_copy_warp(base + st.esc_off - st.esc_from, it.payload, ea,
@@ -361,14 +360,23 @@ __global__ void __launch_bounds__(kStashWarps * 32, 4) dip_stash(const __grid_co
   }
 }
 
-// The read_done word lane `lane` of a warp watches for the store of `tile`:
-// one tile of [tile + dep.x, tile + dep.y] or [tile + dep.z, tile + dep.w]
-// other than the tile itself (at most 4 + 3), or nullptr.
-__device__ __forceinline__ const uint32_t* dep_word(const DecWs& ws, uint64_t tile, uint4 dep, uint32_t lane) {
-  const uint32_t lo0 = dep.x == 0 ? 1u : dep.x, lo1 = dep.z == 0 ? 1u : dep.z;  // skip the tile itself
-  const uint32_t n0 = dep.y >= lo0 ? dep.y - lo0 + 1 : 0, n1 = dep.w >= lo1 ? dep.w - lo1 + 1 : 0;
-  if (lane < n0) return ws.read_done + tile + lo0 + lane;
-  if (lane < n0 + n1) return ws.read_done + tile + lo1 + (lane - n0);
+// The read_done word lane `lane` of a warp watches for the store of flat tile
+// `tile` (local index lt in its tensor): one tile of the local ranges
+// [dep.x, dep.y], [dep.z, dep.w], [dep2.x, dep2.y] other than the tile
+// itself (at most 4 + 3), or nullptr.
+__device__ __forceinline__ const uint32_t* dep_word(const DecWs& ws, uint64_t tile, uint32_t lt, uint4 dep,
+                                                    uint2 dep2, uint32_t lane) {
+  const uint32_t lo[3] = {dep.x, dep.z, dep2.x}, hi[3] = {dep.y, dep.w, dep2.y};
+  uint32_t k = lane;
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    const uint32_t cnt = hi[r] >= lo[r] ? hi[r] - lo[r] + 1 : 0;
+    if (k < cnt) {
+      const uint32_t t = lo[r] + k;
+      return t == lt ? nullptr : ws.read_done + (tile - lt + t);
+    }
+    k -= cnt;
+  }
   return nullptr;
 }
 
@@ -424,22 +432,23 @@ __device__ __forceinline__ Slice slice_of(uint64_t start, uint64_t bytes) {
   return s;
 }
 
-// In-place decode schedule.  Work is handed out in chunks of up to kIpChunk
-// consecutive tiles of one tensor, taken from the top down; chunk tickets are
-// ordered so that every tile comes after the tiles it waits for (tiles above
-// it in its own tensor).  When all K tensors have Tu tiles, chunk ticket q
-// is chunk rank q / K of tensor q % K (rank-major: a tile d chunks above
-// another in its tensor comes d K tickets earlier); otherwise the flat tile
-// space is cut into chunks from its last tile down.  CTA b of the R CTAs (a
-// cooperative launch, so all are resident) takes chunks b, b + R, b + 2R, ...
-// and the tiles of each chunk from the top down.  Every CTA meets its tiles
-// in increasing (chunk ticket, position) order and a tile only waits for
-// tiles earlier in that order, which are read before it by induction.
-// Chunks keep a CTA on consecutive tiles (measured on the 64-tensor KV cache:
-// 203 us with single tiles, 186 us with chunks of 4); longer chunks leave too
-// few chunks per CTA to balance (8: 192 us, 16: 200 us, 32: 231 us).  The
-// cyclic order over chunks keeps the CTAs advancing together, so waits are
-// short.
+// In-place decode schedule.  Each tensor's tiles are decoded in its phase
+// order (ip_rank: A from the top down, then B from the top down, then C
+// from the bottom up), and a tile only waits for tiles earlier in that
+// order.  Work is handed out in chunks of up to kIpChunk consecutive
+// positions of one tensor's order.  When all K tensors have Tu tiles, chunk
+// ticket q is chunk q / K of tensor q % K (rank-major: a tile d chunks
+// further in its tensor's order comes d K tickets later); otherwise the
+// tensors are taken from the last to the first, each in its order, and cut
+// into chunks.  CTA b of the R CTAs (a cooperative launch, so all are
+// resident) takes chunks b, b + R, b + 2R, ... and the positions of each
+// chunk in order.  Every CTA meets its tiles in increasing (chunk ticket,
+// position) order and a tile only waits for tiles earlier in that order,
+// which are read before it by induction.  Chunks keep a CTA on consecutive
+// tiles (measured on the 64-tensor KV cache: 203 us with single tiles, 186 us
+// with chunks of 4); longer chunks leave too few chunks per CTA to balance (8:
+// 192 us, 16: 200 us, 32: 231 us).  The cyclic order over chunks keeps the
+// CTAs advancing together, so waits are short.
 constexpr uint64_t kIpChunk = 4;
 constexpr uint64_t kNoTile = ~0ull;
 
@@ -450,15 +459,30 @@ __device__ __forceinline__ uint64_t ip_chunk_size(uint64_t Tu) {
 __device__ __forceinline__ uint64_t ip_chunks(uint64_t T, uint32_t K, uint64_t Tu, uint64_t C) {
   return Tu == 0 ? (T + C - 1) / C : uint64_t(K) * ((Tu + C - 1) / C);
 }
+// the phases of a tensor of n elements (off_sm from n alone: the meta of a
+// valid item agrees with it)
+__device__ __forceinline__ IpPhases ip_phases_of(uint64_t n) {
+  return ip_phases(n, ((n + 1) / 2 + 3) & ~uint64_t(3));
+}
 // flat tile at position j of chunk ticket q, or kNoTile past a tensor's end
-__device__ __forceinline__ uint64_t ip_tile_of(uint64_t q, uint64_t j, uint64_t T, uint32_t K, uint64_t Tu,
-                                               uint64_t C) {
+__device__ uint64_t ip_tile_of(const Items& items, const DecWs& ws, uint64_t q, uint64_t j, uint64_t T,
+                               uint64_t Tu, uint64_t C) {
   if (Tu == 0) {
     const uint64_t d = q * C + j;
-    return d < T ? T - 1 - d : kNoTile;
+    if (d >= T) return kNoTile;
+    const uint64_t p = T - 1 - d;  // the tensors from the last down, each in its own order
+    const uint32_t i = ws.tile_item ? ws.tile_item[p] : 0u;
+    if (i >= items.count) return p;
+    const sz_item& it = item_at(items, i);
+    const uint64_t tb = it.tile_begin;
+    if (it.n > SZ_MAX_ELEMS || p < tb || p - tb >= tiles_of(it.n)) return p;  // not a valid tensor tile
+    return tb + ip_tile_at(ip_phases_of(it.n), tb + tiles_of(it.n) - 1 - p);
   }
-  const uint64_t r = q / K, i = q - r * K, d = r * C + j;
-  return d < Tu ? i * Tu + (Tu - 1 - d) : kNoTile;
+  const uint64_t r = q / items.count, i = q - r * items.count, d = r * C + j;
+  if (d >= Tu) return kNoTile;
+  const uint64_t n = item_at(items, uint32_t(i)).n;
+  if (n > SZ_MAX_ELEMS || tiles_of(n) != Tu) return i * Tu + (Tu - 1 - d);
+  return i * Tu + ip_tile_at(ip_phases_of(n), d);
 }
 
 // INPLACE = false: sz_decode(_many); persistent CTAs own contiguous tile
@@ -543,7 +567,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
         if (uint32_t(lane) < win_len) {
           const uint64_t k = first + lane;
           const uint64_t mine =
-              INPLACE ? ip_tile_of(blockIdx.x + (k / C) * R, k % C, T, items.count, Tu, C) : k;
+              INPLACE ? ip_tile_of(items, ws, blockIdx.x + (k / C) * R, k % C, T, Tu, C) : k;
           WinEntry& w = sh.win[lane];
           w.tile = mine;
           uint32_t ok = 0;
@@ -570,16 +594,16 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
                 w.dec_lut = *reinterpret_cast<const uint4*>(itm.codebook->dec_lut);
                 if constexpr (INPLACE) {
                   const IpStash sv = ip_stash(itm.n, mp->n_esc, w.off_sm, w.off_cid, mp->comp_bytes);
+                  const IpPhases ph = ip_phases(itm.n, w.off_sm);
                   const uint64_t sb = reinterpret_cast<uint64_t>(ws.stash) + ip_stash_at(tb, idx);
-                  w.smv = (lt < sv.sm_tiles) ? sb - sv.sm_from : reinterpret_cast<uint64_t>(itm.payload);
+                  // phase C reads its pk bytes from the stash
+                  w.pkv = (lt >= ph.tB && lt < ph.tA) ? sb - sv.pk_from : reinterpret_cast<uint64_t>(itm.payload);
                   w.escv = sb + sv.esc_off - sv.esc_from;
                   const IpDeps d = ip_deps(itm.n, w.off_sm, lt);
-                  uint4 dep = make_uint4(1, 0, 1, 0);
-                  if (d.pk_lo <= d.pk_hi) dep.x = uint32_t(d.pk_lo - lt), dep.y = uint32_t(d.pk_hi - lt);
-                  if (d.sm_lo <= d.sm_hi) dep.z = uint32_t(d.sm_lo - lt), dep.w = uint32_t(d.sm_hi - lt);
-                  w.dep = dep;
+                  w.dep = make_uint4(uint32_t(d.pk_lo), uint32_t(d.pk_hi), uint32_t(d.pk2_lo), uint32_t(d.pk2_hi));
+                  w.dep2 = make_uint2(uint32_t(d.sm_lo), uint32_t(d.sm_hi));
                 } else {
-                  w.smv = w.escv = reinterpret_cast<uint64_t>(itm.payload);
+                  w.pkv = w.escv = reinterpret_cast<uint64_t>(itm.payload);
                 }
                 ok = 1;
               }
@@ -608,7 +632,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
       const uint64_t g = uint64_t(lt) * kTile;
       const uint64_t off_sm = w.off_sm, off_cid = w.off_cid, off_lpos = w.off_lpos, off_ev = w.off_ev;
       const uint8_t* base = w.base;
-      const uint8_t* sm_src = reinterpret_cast<const uint8_t*>(w.smv);    // payload byte 0 of the sm source
+      const uint8_t* pk_src = reinterpret_cast<const uint8_t*>(w.pkv);    // payload byte 0 of the pk source
       const uint8_t* esc_src = reinterpret_cast<const uint8_t*>(w.escv);  // ... of the escape streams' source
       const uint32_t m = (k1 > k0) ? k1 - k0 : 0u;
       const uint32_t pieces = m ? (m + kEcap - 1) / kEcap : 1u;
@@ -636,21 +660,24 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
           st.n_tile = nt;
           st.flags = (first ? 0u : kStageCont) | (pc + 1 < pieces ? kStageMore : 0u);
           st.tile = tile;
-          if constexpr (INPLACE) st.dep = w.dep;
+          if constexpr (INPLACE) {
+            st.dep = w.dep;
+            st.dep2 = w.dep2;
+          }
           st.sm_shift = uint32_t(off_sm + g - ssm.a0);
           st.cid_shift = uint32_t(off_cid + 4ull * pk0 - scid.a0);
           st.lpos_shift = uint32_t(off_lpos + 2ull * pk0 - slp.a0);
           st.ev_shift = uint32_t(off_ev + pk0 - sev.a0);
           mbar_arrive_expect_tx(&sh.full[s], tx);
-          if (first && spk.a1 > spk.a0) bulk_g2s(st.pk, base + spk.a0, uint32_t(spk.a1 - spk.a0), &sh.full[s]);
-          if (first && ssm.a1 > ssm.a0) bulk_g2s(st.sm, sm_src + ssm.a0, uint32_t(ssm.a1 - ssm.a0), &sh.full[s]);
+          if (first && spk.a1 > spk.a0) bulk_g2s(st.pk, pk_src + spk.a0, uint32_t(spk.a1 - spk.a0), &sh.full[s]);
+          if (first && ssm.a1 > ssm.a0) bulk_g2s(st.sm, base + ssm.a0, uint32_t(ssm.a1 - ssm.a0), &sh.full[s]);
           if (pm && scid.a1 > scid.a0) bulk_g2s(st.cid, esc_src + scid.a0, uint32_t(scid.a1 - scid.a0), &sh.full[s]);
           if (pm && slp.a1 > slp.a0) bulk_g2s(st.lpos, esc_src + slp.a0, uint32_t(slp.a1 - slp.a0), &sh.full[s]);
           if (pm && sev.a1 > sev.a0) bulk_g2s(st.ev, esc_src + sev.a0, uint32_t(sev.a1 - sev.a0), &sh.full[s]);
         } else if (first && lane == 1 && spk.end > spk.a1) {
-          cp_async16_zfill(st.pk + (spk.a1 - spk.a0), base + spk.a1, uint32_t(spk.end - spk.a1));
+          cp_async16_zfill(st.pk + (spk.a1 - spk.a0), pk_src + spk.a1, uint32_t(spk.end - spk.a1));
         } else if (first && lane == 2 && ssm.end > ssm.a1) {
-          cp_async16_zfill(st.sm + (ssm.a1 - ssm.a0), sm_src + ssm.a1, uint32_t(ssm.end - ssm.a1));
+          cp_async16_zfill(st.sm + (ssm.a1 - ssm.a0), base + ssm.a1, uint32_t(ssm.end - ssm.a1));
         } else if (pm && lane == 3 && scid.end > scid.a1) {
           cp_async16_zfill(reinterpret_cast<uint8_t*>(st.cid) + (scid.a1 - scid.a0), esc_src + scid.a1,
                            uint32_t(scid.end - scid.a1));
@@ -701,7 +728,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     uint16_t* const outs = sh.out[ob];
     if constexpr (INPLACE) {
       if (warp == 0 && !(flags & kStageCont)) {
-        dep_p = dep_word(ws, st.tile, st.dep, uint32_t(lane));
+        dep_p = dep_word(ws, st.tile, st.lt, st.dep, st.dep2, uint32_t(lane));
         dep_v = dep_p ? ld_relaxed_u32(dep_p) : 1u;
       }
     }

@@ -236,77 +236,104 @@ __host__ __device__ inline DecWs dec_ws(void* base, uint32_t count, uint64_t til
 
 // ------------------------------------------------------------------ in-place slot decode
 // The payload occupies the leading comp_bytes of the tensor's own 2n-byte
-// output (its slot) and the weight is decoded over it.  Tiles of a tensor
-// are decoded from the last to the first.  Output tile u covers slot bytes
-// [16384 u, 16384 u + 2 nt); a payload byte read by tile r and overwritten by
-// tile w = byte / 16384 is safe in place when w <= r (the reader comes first,
-// or is the writer itself).  pk bytes of tile t start at 4096 t, so they
-// always are; sm bytes of element i lie at off_sm + i, safe whenever
-// i >= off_sm; the escape streams are not.  So, before the decode, the sm
-// bytes of the first ip_sm_stash_tiles tiles (every element below off_sm)
-// and the whole escape streams are copied to a stash; everything else is
-// read in place, and a tile stores its output only after the tiles whose
-// in-place bytes lie under it have read them (ip_deps).
-
-// tiles whose sm bytes are read from the stash
-__host__ __device__ inline uint64_t ip_sm_stash_tiles(uint64_t n, uint64_t off_sm) {
-  const uint64_t m = n < off_sm ? n : off_sm;
-  return (m + kTile - 1) / kTile;
+// output (its slot) and the weight is decoded over it.  Output tile u covers
+// slot bytes [16384 u, 16384 u + 2 nt); a payload byte read by tile r and
+// overwritten by tile w = byte / 16384 must be read before w stores, so the
+// tiles of a tensor are decoded in an order that reads as much as possible in
+// place, in three phases (tA = ceil(off_sm / 8192), tB = off_sm / 16384):
+//   A  tiles [tA, T), from the top down.  pk bytes of tile t start at 4096 t,
+//      under tile t / 4 <= t; sm bytes of tile t >= tA lie under tiles <= t.
+//   B  tiles [0, tB), from the top down.  pk as in A; their sm bytes lie
+//      under tiles of C, which come later.
+//   C  tiles [tB, tA), from the bottom up.  Their sm bytes lie under tiles of
+//      C at or above them (off_sm + i >= 2 i for i < off_sm); their pk bytes
+//      lie under tiles of B, which came before, so they are copied to a
+//      stash before the decode, with the escape streams (under tiles of A).
+// The stash is about n / 8 + 7 e bytes (the whole payload is 1.5 n + 7 e).
+// A tile stores its output only after the tiles whose in-place bytes lie
+// under it have read them (ip_deps); all of them come earlier in the order.
+struct IpPhases {
+  uint64_t T, tA, tB;
+};
+__host__ __device__ inline IpPhases ip_phases(uint64_t n, uint64_t off_sm) {
+  IpPhases p;
+  p.T = (n + kTile - 1) / kTile;
+  p.tA = (off_sm + kTile - 1) / kTile;
+  if (p.tA > p.T) p.tA = p.T;
+  p.tB = off_sm / (2 * kTile);
+  if (p.tB > p.tA) p.tB = p.tA;
+  return p;
+}
+// position of tile t in the tensor's decode order, and its inverse
+__host__ __device__ inline uint64_t ip_rank(const IpPhases& p, uint64_t t) {
+  if (t >= p.tA) return p.T - 1 - t;
+  if (t < p.tB) return (p.T - p.tA) + (p.tB - 1 - t);
+  return (p.T - p.tA) + p.tB + (t - p.tB);
+}
+__host__ __device__ inline uint64_t ip_tile_at(const IpPhases& p, uint64_t r) {
+  if (r < p.T - p.tA) return p.T - 1 - r;
+  r -= p.T - p.tA;
+  if (r < p.tB) return p.tB - 1 - r;
+  return p.tB + (r - p.tB);
 }
 
-// Stash of one tensor: payload bytes [floor16(off_sm), off_sm + S) (S = the
-// stashed sm elements) at offset 0 and [floor16(off_cid), comp_bytes) at
-// esc_off; both keep their payload offsets mod 16.
+// Stash of one tensor: payload bytes [pk_from, pk_to) (the pk bytes of phase
+// C) at offset 0 and [floor16(off_cid), comp_bytes) at esc_off; both keep
+// their payload offsets mod 16 (pk_from is a multiple of 4096).
 struct IpStash {
-  uint64_t sm_tiles;  // tiles whose sm bytes come from the stash
-  uint64_t sm_from, sm_to;    // payload byte range of the sm part
+  uint64_t pk_from, pk_to;    // payload byte range of the pk part
   uint64_t esc_from, esc_to;  // payload byte range of the escape part (empty without escapes)
   uint64_t esc_off;           // stash offset of the escape part (16-byte multiple)
   uint64_t bytes;             // stash bytes used
 };
 __host__ __device__ inline IpStash ip_stash(uint64_t n, uint64_t n_esc, uint64_t off_sm, uint64_t off_cid,
                                             uint64_t comp_bytes) {
+  const IpPhases p = ip_phases(n, off_sm);
+  const uint64_t n_pairs = (n + 1) / 2;
   IpStash s;
-  s.sm_tiles = ip_sm_stash_tiles(n, off_sm);
-  const uint64_t S = (s.sm_tiles * kTile < n) ? s.sm_tiles * kTile : n;
-  s.sm_from = off_sm & ~uint64_t(15);
-  s.sm_to = S ? off_sm + S : s.sm_from;
+  s.pk_from = p.tB * (kTile / 2);
+  s.pk_to = p.tA * (kTile / 2) < n_pairs ? p.tA * (kTile / 2) : n_pairs;
+  if (s.pk_to < s.pk_from) s.pk_to = s.pk_from;
   s.esc_from = off_cid & ~uint64_t(15);
   s.esc_to = n_esc ? comp_bytes : s.esc_from;
-  s.esc_off = (s.sm_to - s.sm_from + 15) & ~uint64_t(15);
+  s.esc_off = (s.pk_to - s.pk_from + 15) & ~uint64_t(15);
   s.bytes = s.esc_off + (s.esc_to - s.esc_from);
   return s;
 }
 
 // Stash budget of a tensor of `tiles` tiles: enough for any payload of at
-// most 2n bytes (sm part <= n + 30, escape part <= n - off_sm + 15, with
-// off_sm >= n / 2 and n <= 8192 tiles).
-constexpr uint64_t kIpStashPerTile = 12288;
-constexpr uint64_t kIpStashPerItem = 256;
+// most 2n bytes (pk part <= min(n_pairs, n / 8 + 8200), escape part
+// <= n - off_sm + 15 with off_sm >= n / 2, n <= 8192 tiles).
+constexpr uint64_t kIpStashPerTile = 8192;
+constexpr uint64_t kIpStashPerItem = 4096 + 256;
 __host__ __device__ inline uint64_t ip_stash_at(uint64_t tile_begin, uint32_t item) {
   return tile_begin * kIpStashPerTile + uint64_t(item) * kIpStashPerItem;
 }
 
 // Tiles (local indices, inclusive ranges, empty when lo > hi) whose in-place
-// bytes lie under output tile u: pk of tiles 4u .. 4u + 3, and in-place sm
-// (tiles >= sm_tiles) of the tiles whose sm bytes meet [16384 u, 16384 u +
-// 16384).  Every such tile is >= u, so it is decoded first.
+// bytes lie under output tile u: pk of tiles 4u .. 4u + 3 outside phase C
+// (two ranges, below tB and from tA up), and the tiles whose sm bytes meet
+// [16384 u, 16384 u + 16384).  Every one of them other than u comes earlier
+// in the decode order (ip_rank).
 struct IpDeps {
-  uint64_t pk_lo, pk_hi, sm_lo, sm_hi;
+  uint64_t pk_lo, pk_hi, pk2_lo, pk2_hi, sm_lo, sm_hi;
 };
 __host__ __device__ inline IpDeps ip_deps(uint64_t n, uint64_t off_sm, uint64_t u) {
+  const IpPhases p = ip_phases(n, off_sm);
   IpDeps d;
-  const uint64_t T = (n + kTile - 1) / kTile;
-  d.pk_lo = 4 * u;
-  d.pk_hi = (4 * u + 3 < T) ? 4 * u + 3 : T - 1;
-  const uint64_t sm_tiles = ip_sm_stash_tiles(n, off_sm);
+  const uint64_t lo = 4 * u, hi = (4 * u + 3 < p.T) ? 4 * u + 3 : p.T - 1;
+  d.pk_lo = lo;
+  d.pk_hi = (hi < p.tB) ? hi : p.tB - 1;  // below tB (empty when tB == 0: hi wraps below lo)
+  if (p.tB == 0) d.pk_lo = 1, d.pk_hi = 0;
+  d.pk2_lo = (lo > p.tA) ? lo : p.tA;
+  d.pk2_hi = hi;
+  if (lo > hi) d.pk_lo = d.pk2_lo = 1, d.pk_hi = d.pk2_hi = 0;
   const uint64_t w0 = 2 * kTile * u, w1 = w0 + 2 * kTile;  // the output bytes of tile u (at most)
   // tile t's sm bytes [off_sm + 8192 t, off_sm + 8192 t + 8192) meet [w0, w1)
   d.sm_lo = (w0 >= off_sm + kTile) ? (w0 - off_sm - kTile) / kTile + 1 : 0;
   d.sm_hi = (w1 > off_sm) ? (w1 - off_sm - 1) / kTile : 0;
   if (w1 <= off_sm) d.sm_lo = 1, d.sm_hi = 0;
-  if (d.sm_lo < sm_tiles) d.sm_lo = sm_tiles;
-  if (d.sm_hi >= T) d.sm_hi = T - 1;
+  if (d.sm_hi >= p.T) d.sm_hi = p.T - 1;
   return d;
 }
 
