@@ -38,7 +38,9 @@ namespace {
 constexpr int kDecStages = 4;
 constexpr int kDecConsumerWarps = 8;
 constexpr int kDecConsumers = kDecConsumerWarps * 32;
-constexpr int kDecThreads = kDecConsumers + 32;
+constexpr int kDecProducerWarp = kDecConsumerWarps;
+constexpr int kDecStorerWarp = kDecConsumerWarps + 1;
+constexpr int kDecThreads = kDecConsumers + 64;  // + producer warp + storer warp
 constexpr int kDecCtasPerSm = 2;
 constexpr uint32_t kEcap = 1024;  // escapes per stage; a tile with more is sent as several stages
 constexpr uint32_t kRangeInvalid = 0xFFFFFFFFu;
@@ -78,12 +80,24 @@ struct WinEntry {
   uint32_t ok;
 };
 
+// A finished output tile handed from the consumer warps to the storer warp.
+struct StoreSlot {
+  uint16_t* out;  // the tile's first output element
+  uint64_t tile;  // flat tile index
+  uint4 dep;      // in place: tiles to wait for (as DecStage::dep, dep2)
+  uint2 dep2;
+  uint32_t nt, lt, end;  // end: no more tiles
+};
+
 struct DecShared {
   DecStage st[kDecStages];
   alignas(128) uint16_t out[2][kTile];
   WinEntry win[kWin];
+  StoreSlot sto[2];
   uint64_t full[kDecStages];
   uint64_t empty[kDecStages];
+  uint64_t out_full[2];   // out[b] holds a finished tile (sto[b] describes it)
+  uint64_t out_empty[2];  // the store of out[b] has read it
 };
 
 __device__ bool meta_ok(const sz_item& it, uint64_t n_esc_limit, uint64_t capacity) {
@@ -509,11 +523,57 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
       mbar_init(&sh.full[s], 1 + 32);
       mbar_init(&sh.empty[s], 1);
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh.out_full[b], 1);
+      mbar_init(&sh.out_empty[b], 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kDecConsumerWarps) {
+  if (warp == kDecStorerWarp) {
+    // ---------------------------------------------------------------- storer warp
+    // Takes each finished output tile from the consumer warps and stores it
+    // (TMA bulk store of its 16-byte body, plain stores for the ragged end);
+    // in place, first waits until the tiles whose payload bytes lie under it
+    // have read them.  Waiting here keeps the consumers decoding the next
+    // tile into the other output buffer.
+    for (uint32_t k = 0;; ++k) {
+      const int b = int(k & 1u);
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sh.out_full[b], (k >> 1) & 1u))) {
+        if (lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+        break;
+      }
+      const StoreSlot so = sh.sto[b];
+      if (so.end) break;
+      bool go = true;
+      if constexpr (INPLACE) {
+        const uint32_t* p = dep_word(ws, so.tile, so.lt, so.dep, so.dep2, uint32_t(lane));
+        go = wait_words_warp(ws, p, p ? ld_relaxed_u32(p) : 1u, uint32_t(lane));
+        if (lane == 0) {
+          if (go) {
+            fence_proxy_async_global();
+          } else {
+            set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+          }
+        }
+      }
+      const uint32_t body = (so.nt * 2u) & ~15u;
+      if (lane == 0) {
+        if (go && body) bulk_s2g(so.out, sh.out[b], body);
+        bulk_commit();
+      }
+      if (go)
+        for (uint32_t e = body / 2u + uint32_t(lane); e < so.nt; e += 32) so.out[e] = sh.out[b][e];
+      if (lane == 0) bulk_wait_read<0>();  // the bulk store has read out[b]
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.out_empty[b]);
+    }
+    if (lane == 0) bulk_wait_all<0>();
+    return;
+  }
+
+  if (warp == kDecProducerWarp) {
     // ---------------------------------------------------------------- producer warp
     // When a window of kWin tiles starts, lane l resolves tile l of it in
     // parallel (escape range, item through the tile -> item map, payload,
@@ -695,15 +755,16 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
 
   // ------------------------------------------------------------------ consumer warps
   uint32_t bad_escape = 0;
-  uint32_t tiles_done = 0;  // output buffer of the current tile: out[tiles_done & 1]
+  uint32_t tiles_done = 0;  // tiles handed to the storer; the current tile goes to out[tiles_done & 1]
   bool in_tile = false;     // the previous stage left its tile open (more escape stages)
-  const uint32_t* dep_p = nullptr;  // in place, warp 0: the read_done word this lane watches
-  uint32_t dep_v = 0;               // ... and its value read when the tile's first stage landed
+  // waits (bounded) until the storer has read out[tiles_done & 1]'s previous tile
+  auto out_free = [&]() -> bool {
+    return tiles_done < 2 || mbar_wait(&sh.out_empty[tiles_done & 1u], ((tiles_done >> 1) - 1) & 1u);
+  };
   for (uint32_t it = 0;; ++it) {
     const int s = int(it % kDecStages);
     const int ob = int(tiles_done & 1u);
-    if (tid == 0 && !in_tile) bulk_wait_read<1>();  // the store that last used out[ob] has read it
-    const bool ok = mbar_wait(&sh.full[s], (it / kDecStages) & 1);
+    bool ok = mbar_wait(&sh.full[s], (it / kDecStages) & 1);
     const DecStage& st = sh.st[s];
     // read before the vote: after it, an invalid tile's stage is released
     const uint32_t flags = ok ? st.flags : 0u;
@@ -715,6 +776,8 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
       // here, on every tile, cost a quarter of the kernel's time).
       if (tid == 0 && ok && !(flags & (kStageCont | kStageEnd))) st_relaxed_u32(ws.read_done + st.tile, 1u);
     }
+    // a tile's first stage writes out[ob]: its previous tile must have been read
+    if (ok && !in_tile && !(flags & (kStageEnd | kStageInvalid))) ok = out_free();
     if (named_bar_red_or(1, kDecConsumers, !ok)) {
       if (tid == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
       break;
@@ -726,12 +789,6 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     }
     const uint32_t nt = st.n_tile;
     uint16_t* const outs = sh.out[ob];
-    if constexpr (INPLACE) {
-      if (warp == 0 && !(flags & kStageCont)) {
-        dep_p = dep_word(ws, st.tile, st.lt, st.dep, st.dep2, uint32_t(lane));
-        dep_v = dep_p ? ld_relaxed_u32(dep_p) : 1u;
-      }
-    }
     if (!(flags & kStageCont)) {
       const uint4 dl = st.dec_lut;
       const uint32_t shift = st.sm_shift;
@@ -770,38 +827,34 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
     fence_proxy_async_smem();
     named_bar_sync(1, kDecConsumers);
     const bool more = (flags & kStageMore) != 0;
-    if (warp == 0) {
-      // the stage may be refilled once released: read what the store needs first
-      uint16_t* const outp = st.out;
-      __syncwarp();
-      if (tid == 0) mbar_arrive(&sh.empty[s]);
+    if (tid == 0) {
       if (!more) {
-        bool go = true;
+        // hand the finished tile to the storer (what it needs is read from
+        // the stage before the stage is released)
+        StoreSlot& so = sh.sto[ob];
+        so.out = st.out;
+        so.tile = st.tile;
+        so.lt = st.lt;
+        so.nt = nt;
         if constexpr (INPLACE) {
-          // the tiles whose in-place bytes lie under this output have read them
-          go = wait_words_warp(ws, dep_p, dep_v, uint32_t(lane));
-          if (tid == 0) {
-            if (go) {
-              fence_proxy_async_global();
-            } else {
-              set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
-            }
-          }
+          so.dep = st.dep;
+          so.dep2 = st.dep2;
         }
-        if (tid == 0) {
-          const uint32_t body = (nt * 2u) & ~15u;
-          if (go && body) bulk_s2g(outp, outs, body);
-          bulk_commit();
-          if (go)
-            for (uint32_t k = body / 2u; k < nt; ++k) outp[k] = outs[k];
-        }
+        so.end = 0;
       }
+      mbar_arrive(&sh.empty[s]);
+      if (!more) mbar_arrive(&sh.out_full[ob]);
     }
     in_tile = more;
     if (!more) ++tiles_done;
   }
   if (bad_escape) set_flag(ws.hdr, SZ_FLAG_ESCAPE);
-  if (tid == 0) bulk_wait_all<0>();
+  // tell the storer there is nothing more (in the slot it reads next)
+  if (tid == 0) {
+    if (!out_free()) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+    sh.sto[tiles_done & 1u].end = 1;
+    mbar_arrive(&sh.out_full[tiles_done & 1u]);
+  }
 }
 
 }  // namespace
