@@ -25,11 +25,12 @@
 //
 // In-place slot decode (the payload in the leading comp_bytes of the
 // tensor's own 2n-byte output, "splitzip_codec.py" GpuSplitZipDecoder): the
-// same prepare pass, then dip_stash copies aside only the bytes that a
-// last-tile-first decode would overwrite before reading them (the sm bytes
-// of elements below off_sm and the escape streams; the pages' decoder copies
-// the whole payload), then dec_main<true> decodes tiles in descending order,
-// each tile's store waiting for the tiles whose in-place bytes lie under it.
+// same prepare pass, which also copies the escape streams to a stash; then
+// dip_stash copies the pk bytes of phase C there (about n / 8 bytes; the
+// pages' decoder copies the whole payload), and dec_main<true> decodes each
+// tensor's tiles in an order that reads everything else in place (three
+// phases, see ip_phases), each tile storing once the tiles whose payload
+// bytes lie under it have read them.
 #include "sz_internal.h"
 
 namespace sz {
@@ -169,6 +170,31 @@ __device__ uint32_t lower_bound_cid32(const int32_t* cid, uint32_t e, uint32_t t
   return lo + __popc(__ballot_sync(0xFFFFFFFFu, less));
 }
 
+// Copies payload bytes [a, b) to dst_v + a .. dst_v + b (dst_v: the stash
+// address of payload byte 0, congruent to src mod 16; b - a <= 16400) with
+// one warp: each lane issues 8 16-byte loads before its stores.
+__device__ __noinline__ void stash_copy_warp(uint64_t dst_v, const uint8_t* src, uint64_t a, uint64_t b, uint32_t lane) {
+  const uint64_t a16 = (a + 15) & ~uint64_t(15), b16 = b & ~uint64_t(15);
+  if (a16 >= b16) {
+    for (uint64_t x = a + lane; x < b; x += 32) *reinterpret_cast<uint8_t*>(dst_v + x) = src[x];
+    return;
+  }
+  if (lane < a16 - a) *reinterpret_cast<uint8_t*>(dst_v + a + lane) = src[a + lane];
+  if (lane < b - b16) *reinterpret_cast<uint8_t*>(dst_v + b16 + lane) = src[b16 + lane];
+  const uint4* s4 = reinterpret_cast<const uint4*>(src) + a16 / 16;
+  uint4* d4 = reinterpret_cast<uint4*>(dst_v + a16);
+  const uint32_t nv = uint32_t((b16 - a16) / 16);  // at most 1025
+  for (uint32_t v0 = lane; v0 < nv; v0 += 8 * 32) {
+    uint4 r[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (v0 + 32u * j < nv) r[j] = s4[v0 + 32u * j];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (v0 + 32u * j < nv) d4[v0 + 32u * j] = r[j];
+  }
+}
+
 constexpr int kPrepWarps = 8;
 constexpr uint64_t kSmallTiles = 32;  // items of at most one 32-tile group are prepared by one warp
 constexpr uint32_t kDenseGroup = 4096;  // escapes in a 32-tile group above which tiles are searched, not counted
@@ -243,6 +269,21 @@ __device__ void prepare_group(const Items& items, const DecWs& ws, uint32_t i, c
   if (lane < ng && tt < items.total_tiles) {
     ws.ranges[tt] = r;
     if (ws.tile_item) ws.tile_item[tt] = i;
+    if (ws.read_done) ws.read_done[tt] = 0;
+  }
+  if (ws.stash && !bad) {
+    // in place: this group's share of the escape streams into the stash
+    const sz_meta* mp = it.meta;
+    const IpStash st = ip_stash(it.n, mp->n_esc, mp->off_sm, mp->off_cid, mp->comp_bytes);
+    const uint64_t len = st.esc_to - st.esc_from;
+    if (len) {
+      const uint64_t groups = (tiles + 31) / 32;
+      const uint64_t per = ((len + groups - 1) / groups + 15) & ~uint64_t(15);
+      const uint64_t ea = st.esc_from + (ta / 32) * per;
+      const uint64_t eb = (ea + per < st.esc_to) ? ea + per : st.esc_to;
+      const uint64_t base = reinterpret_cast<uint64_t>(ws.stash) + ip_stash_at(it.tile_begin, i);
+      if (ea < eb) stash_copy_warp(base + st.esc_off - st.esc_from, it.payload, ea, eb, lane);
+    }
   }
 }
 
@@ -315,62 +356,49 @@ __global__ void __launch_bounds__(kPrepWarps * 32) dec_prepare(const __grid_cons
   }
 }
 
-// Copies payload bytes [a, b) to dst_v + a .. dst_v + b (dst_v: the stash
-// address of payload byte 0, congruent to src mod 16; b - a <= 16400) with
-// one warp: each lane issues 8 16-byte loads before its stores.
-__device__ __noinline__ void stash_copy_warp(uint64_t dst_v, const uint8_t* src, uint64_t a, uint64_t b, uint32_t lane) {
-  const uint64_t a16 = (a + 15) & ~uint64_t(15), b16 = b & ~uint64_t(15);
-  if (a16 >= b16) {
-    for (uint64_t x = a + lane; x < b; x += 32) *reinterpret_cast<uint8_t*>(dst_v + x) = __ldg(src + x);
-    return;
-  }
-  if (lane < a16 - a) *reinterpret_cast<uint8_t*>(dst_v + a + lane) = __ldg(src + a + lane);
-  if (lane < b - b16) *reinterpret_cast<uint8_t*>(dst_v + b16 + lane) = __ldg(src + b16 + lane);
-  const uint4* s4 = reinterpret_cast<const uint4*>(src) + a16 / 16;
-  uint4* d4 = reinterpret_cast<uint4*>(dst_v + a16);
-  const uint32_t nv = uint32_t((b16 - a16) / 16);  // at most 1025
-  for (uint32_t v0 = lane; v0 < nv; v0 += 8 * 32) {
-    uint4 r[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (v0 + 32u * j < nv) r[j] = __ldg(s4 + v0 + 32u * j);
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (v0 + 32u * j < nv) d4[v0 + 32u * j] = r[j];
-  }
-}
-
-constexpr uint64_t kIpEscPiece = 16384;  // escape-stream bytes stashed per tile
 constexpr int kStashWarps = 8;
+constexpr uint64_t kStashTiles = 8;  // consecutive tiles per warp
 
-// In-place decode, before the main pass: per tile (one warp each), clears
-// its read_done word and copies its share of the bytes the decode order
-// would overwrite before reading them: its own pk bytes when it is a tile of
-// phase C, and the escape streams' 16 KiB piece with its index (the escape
-// part is at most n / 2 + 15 bytes, so the tiles cover it).
+// In-place decode, before the main pass: each warp takes kStashTiles
+// consecutive tiles and copies the pk bytes of those of them in phase C
+// (but tile 0) into the stash; the tensor is resolved once per run of tiles
+// in the same tensor.  (dec_prepare has cleared the read_done words and
+// copied the escape streams.)
 __global__ void __launch_bounds__(kStashWarps * 32, 4) dip_stash(const __grid_constant__ Items items, DecWs ws) {
   if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
   const uint32_t lane = threadIdx.x & 31u;
-  for (uint64_t tt = uint64_t(blockIdx.x) * kStashWarps + (threadIdx.x >> 5); tt < items.total_tiles;
-       tt += uint64_t(gridDim.x) * kStashWarps) {
-    if (lane == 0) ws.read_done[tt] = 0;
-    const uint32_t idx = ws.tile_item ? ws.tile_item[tt] : 0u;
-    if (idx >= items.count || ws.item_flags[idx] != 0) continue;
-    const sz_item& it = item_at(items, idx);
-    const uint64_t tb = it.tile_begin;
-    if (tt < tb || tt - tb >= tiles_of(it.n)) continue;
-    const uint64_t lt = tt - tb;
-    const sz_meta* mp = it.meta;
-    const uint64_t off_sm = mp->off_sm;
-    const IpStash st = ip_stash(it.n, mp->n_esc, off_sm, mp->off_cid, mp->comp_bytes);
-    const uint64_t base = reinterpret_cast<uint64_t>(ws.stash) + ip_stash_at(tb, idx);
-    const uint64_t pa = lt * (kTile / 2), pb = (lt + 1) * (kTile / 2);  // the tile's pk bytes
-    if (pa >= st.pk_from && pa < st.pk_to)
-      stash_copy_warp(base - st.pk_from, it.payload, pa, pb < st.pk_to ? pb : st.pk_to, lane);
-    const uint64_t ea = st.esc_from + lt * kIpEscPiece;
-    if (ea < st.esc_to)
-      stash_copy_warp(base + st.esc_off - st.esc_from, it.payload, ea,
-                      (ea + kIpEscPiece < st.esc_to) ? ea + kIpEscPiece : st.esc_to, lane);
+  const uint64_t T = items.total_tiles;
+  for (uint64_t t0 = (uint64_t(blockIdx.x) * kStashWarps + (threadIdx.x >> 5)) * kStashTiles; t0 < T;
+       t0 += uint64_t(gridDim.x) * kStashWarps * kStashTiles) {
+    const uint64_t t1 = (t0 + kStashTiles < T) ? t0 + kStashTiles : T;
+    for (uint64_t tt = t0; tt < t1;) {
+      // the run of tiles [tt, te) in one tensor
+      const uint32_t idx = ws.tile_item ? ws.tile_item[tt] : 0u;
+      if (idx >= items.count) {
+        ++tt;
+        continue;
+      }
+      const sz_item& it = item_at(items, idx);
+      const uint64_t tb = it.tile_begin;
+      const uint64_t tiles = (it.n > SZ_MAX_ELEMS) ? 0 : tiles_of(it.n);
+      if (tt < tb || tt - tb >= tiles) {
+        ++tt;
+        continue;
+      }
+      const uint64_t te = (tb + tiles < t1) ? tb + tiles : t1;
+      if (ws.item_flags[idx] == 0) {
+        const sz_meta* mp = it.meta;
+        const IpStash st = ip_stash(it.n, mp->n_esc, mp->off_sm, mp->off_cid, mp->comp_bytes);
+        uint64_t pa = (tt - tb) * (kTile / 2), pb = (te - tb) * (kTile / 2);  // the run's pk bytes
+        if (pa < st.pk_from) pa = st.pk_from;
+        if (pb > st.pk_to) pb = st.pk_to;
+        if (pa < pb) {
+          const uint64_t base = reinterpret_cast<uint64_t>(ws.stash) + ip_stash_at(tb, idx);
+          stash_copy_warp(base - st.pk_from, it.payload, pa, pb, lane);
+        }
+      }
+      tt = te;
+    }
   }
 }
 
@@ -656,8 +684,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
                   const IpStash sv = ip_stash(itm.n, mp->n_esc, w.off_sm, w.off_cid, mp->comp_bytes);
                   const IpPhases ph = ip_phases(itm.n, w.off_sm);
                   const uint64_t sb = reinterpret_cast<uint64_t>(ws.stash) + ip_stash_at(tb, idx);
-                  // phase C reads its pk bytes from the stash
-                  w.pkv = (lt >= ph.tB && lt < ph.tA) ? sb - sv.pk_from : reinterpret_cast<uint64_t>(itm.payload);
+                  // phase C reads its pk bytes from the stash (but tile 0, which
+                  // reads its own before it stores over them)
+                  w.pkv = (lt >= ph.tB && lt < ph.tA && lt > 0) ? sb - sv.pk_from
+                                                               : reinterpret_cast<uint64_t>(itm.payload);
                   w.escv = sb + sv.esc_off - sv.esc_from;
                   const IpDeps d = ip_deps(itm.n, w.off_sm, lt);
                   w.dep = make_uint4(uint32_t(d.pk_lo), uint32_t(d.pk_hi), uint32_t(d.pk2_lo), uint32_t(d.pk2_hi));
@@ -925,7 +955,7 @@ cudaError_t launch_decode_inplace(const Items& items, void* ws_base, cudaStream_
   cudaError_t err = cudaMemsetAsync(ws_base, 0, sizeof(WsHeader), stream);
   if (err != cudaSuccess || (err = launch_prepare(items, ws, stream, true)) != cudaSuccess) return err;
   if (items.total_tiles == 0) return cudaSuccess;
-  const uint64_t blocks = (items.total_tiles + kStashWarps - 1) / kStashWarps;
+  const uint64_t blocks = (items.total_tiles + kStashWarps * kStashTiles - 1) / (kStashWarps * kStashTiles);
   const uint64_t cap = uint64_t(dev.num_sms) * 32;  // four waves of 8 blocks per SM, then grid-stride
   dip_stash<<<unsigned(blocks < cap ? blocks : cap), kStashWarps * 32, 0, stream>>>(items, ws);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;

@@ -247,8 +247,10 @@ __host__ __device__ inline DecWs dec_ws(void* base, uint32_t count, uint64_t til
 //      under tiles of C, which come later.
 //   C  tiles [tB, tA), from the bottom up.  Their sm bytes lie under tiles of
 //      C at or above them (off_sm + i >= 2 i for i < off_sm); their pk bytes
-//      lie under tiles of B, which came before, so they are copied to a
-//      stash before the decode, with the escape streams (under tiles of A).
+//      lie under tile t / 4, of B (or of C below t when tB = 0), which comes
+//      before, so they are copied to a stash before the decode, with the
+//      escape streams (under tiles of A) -- but those of tile 0, which lie
+//      under tile 0 itself.
 // The stash is about n / 8 + 7 e bytes (the whole payload is 1.5 n + 7 e).
 // A tile stores its output only after the tiles whose in-place bytes lie
 // under it have read them (ip_deps); all of them come earlier in the order.
@@ -278,8 +280,9 @@ __host__ __device__ inline uint64_t ip_tile_at(const IpPhases& p, uint64_t r) {
 }
 
 // Stash of one tensor: payload bytes [pk_from, pk_to) (the pk bytes of phase
-// C) at offset 0 and [floor16(off_cid), comp_bytes) at esc_off; both keep
-// their payload offsets mod 16 (pk_from is a multiple of 4096).
+// C, but those of tile 0, which lie under tile 0 itself) at offset 0 and
+// [floor16(off_cid), comp_bytes) at esc_off; both keep their payload offsets
+// mod 16 (pk_from is a multiple of 4096).
 struct IpStash {
   uint64_t pk_from, pk_to;    // payload byte range of the pk part
   uint64_t esc_from, esc_to;  // payload byte range of the escape part (empty without escapes)
@@ -291,7 +294,7 @@ __host__ __device__ inline IpStash ip_stash(uint64_t n, uint64_t n_esc, uint64_t
   const IpPhases p = ip_phases(n, off_sm);
   const uint64_t n_pairs = (n + 1) / 2;
   IpStash s;
-  s.pk_from = p.tB * (kTile / 2);
+  s.pk_from = (p.tB > 0 ? p.tB : 1) * (kTile / 2);
   s.pk_to = p.tA * (kTile / 2) < n_pairs ? p.tA * (kTile / 2) : n_pairs;
   if (s.pk_to < s.pk_from) s.pk_to = s.pk_from;
   s.esc_from = off_cid & ~uint64_t(15);
