@@ -277,6 +277,21 @@ typedef struct sz_inplace_tile {
 } sz_inplace_tile;
 SZ_API int sz_inplace_plan(uint64_t n, uint64_t n_esc, uint64_t tile, sz_inplace_tile* h_out);
 
+/* ------------------------------------------------------------------ diagnostics */
+
+/* Every wait inside the kernels is bounded: after about 2 s it gives up,
+ * sets SZ_FLAG_TIMEOUT and lets the kernel end, so a stuck call reports an
+ * error instead of hanging the device.  This call checks that on the device
+ * it runs on: one CTA waits on an mbarrier phase that never completes, on a
+ * word polled by one thread and on words polled by a warp (the three kinds
+ * of waits the kernels use), none of which is ever satisfied.  Afterwards
+ * the workspace flags hold SZ_FLAG_TIMEOUT and the uint32 words at byte
+ * offsets 260, 264 and 268 of the workspace hold 1 (that wait gave up).
+ * About 2 s of device time; asynchronous like the other calls.  Workspace:
+ * SZ_CHECK_WAITS_WORKSPACE_BYTES, 256-byte aligned. */
+#define SZ_CHECK_WAITS_WORKSPACE_BYTES 512u
+SZ_API int sz_check_bounded_waits(void* d_workspace, size_t workspace_bytes, sz_stream stream);
+
 /* ------------------------------------------------------------------ decode streamed from host memory */
 
 /* Decode of tensors whose payloads are in pinned host memory

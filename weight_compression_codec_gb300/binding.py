@@ -118,6 +118,7 @@ SIGNATURES = {
     "sz_calibrate_encode": (_INT, [_VP, _U64, _VP, _VP, _U64, _VP, _VP, _SZ, _VP]),
     "sz_calibrate_encode_many": (_INT, [_VP, _U32, _U64, _VP, _SZ, _VP]),
     "sz_encode_gated_many": (_INT, [_VP, _U32, _U64, ctypes.c_double, _VP, _VP, _SZ, _VP]),
+    "sz_check_bounded_waits": (_INT, [_VP, _SZ, _VP]),
     "sz_decode_inplace": (_INT, [_VP, _U64, _VP, _VP, _VP, _SZ, _VP]),
     "sz_decode_inplace_many": (_INT, [_VP, _U32, _U64, _VP, _SZ, _VP]),
     "sz_decode_inplace_workspace_bytes": (_SZ, [_U32, _U64]),
@@ -130,6 +131,7 @@ SIGNATURES = {
 }
 
 SZ_NOALLOC_MAX_ELEMS = 268435456
+SZ_CHECK_WAITS_WORKSPACE_BYTES = 512
 
 _LIB = None
 

@@ -289,6 +289,11 @@ SZ_API int sz_decode_many(const sz_item* d_items, uint32_t count, uint64_t total
                                  reinterpret_cast<cudaStream_t>(stream), dev));
 }
 
+SZ_API int sz_check_bounded_waits(void* d_workspace, size_t workspace_bytes, sz_stream stream) {
+  if (int rc = check_ws(d_workspace, workspace_bytes, SZ_CHECK_WAITS_WORKSPACE_BYTES)) return rc;
+  return from_cuda(launch_wait_selftest(d_workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 SZ_API int sz_decode_inplace_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles, void* d_workspace,
                                   size_t workspace_bytes, sz_stream stream) {
   if (int rc = check_many(d_items, count, total_tiles)) return rc;

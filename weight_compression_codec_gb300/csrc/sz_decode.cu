@@ -402,6 +402,13 @@ __global__ void __launch_bounds__(kStashWarps * 32, 4) dip_stash(const __grid_co
   }
 }
 
+// Diagnostic (sz_check_bounded_waits): each kind of bounded wait the kernels
+// use, on something that never completes -- warp 0 an mbarrier phase that
+// gets one of its two arrivals, warp 1 a word polled by one thread, warp 2
+// words polled by a warp.  Each gives up, sets SZ_FLAG_TIMEOUT and writes 1
+// to gave_up[warp].
+__global__ void __launch_bounds__(96) wait_selftest(DecWs ws, const uint32_t* never, uint32_t* gave_up);
+
 // The read_done word lane `lane` of a warp watches for the store of flat tile
 // `tile` (local index lt in its tensor): one tile of the local ranges
 // [dep.x, dep.y], [dep.z, dep.w], [dep2.x, dep2.y] other than the tile
@@ -422,6 +429,20 @@ __device__ __forceinline__ const uint32_t* dep_word(const DecWs& ws, uint64_t ti
   return nullptr;
 }
 
+// One thread waits (bounded) until word p is set, with acquire ordering;
+// gives up after kWaitTimeoutNs, or at once when another CTA has already given
+// up (SZ_FLAG_TIMEOUT).
+__device__ bool wait_word(const DecWs& ws, const uint32_t* p) {
+  if (ld_acquire_u32(p)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (ld_acquire_u32(p)) return true;
+    if ((i & 63) == 0 &&
+        (global_timer_ns() - t0 > kWaitTimeoutNs || (ld_acquire_u32(&ws.hdr->flags) & SZ_FLAG_TIMEOUT)))
+      return false;
+  }
+}
+
 // One warp waits (bounded) until every lane's word p is set; v is a value of
 // it read earlier (the load is issued when the tile's first stage lands, so
 // its latency hides behind the decode, and the schedule makes the words
@@ -439,6 +460,31 @@ __device__ bool wait_words_warp(const DecWs& ws, const uint32_t* p, uint32_t v, 
     if ((i & 63) == 0 && __any_sync(0xFFFFFFFFu, lane == 0 && (global_timer_ns() - t0 > kWaitTimeoutNs ||
                                                               (ld_acquire_u32(&ws.hdr->flags) & SZ_FLAG_TIMEOUT))))
       return false;
+  }
+}
+
+__global__ void __launch_bounds__(96) wait_selftest(DecWs ws, const uint32_t* never, uint32_t* gave_up) {
+  __shared__ uint64_t bar;
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 2);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  bool ok;
+  if (warp == 0) {
+    if (lane == 0) mbar_arrive(&bar);  // one arrival of two: the phase never completes
+    ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar, 0));
+  } else if (warp == 1) {
+    ok = true;
+    if (lane == 0) ok = wait_word(ws, never);
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  } else {
+    ok = wait_words_warp(ws, lane < 4 ? never : nullptr, 0u, lane);
+  }
+  if (!ok && lane == 0) {
+    set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+    gave_up[warp] = 1;
   }
 }
 
@@ -948,6 +994,16 @@ cudaError_t launch_decode(const Items& items, void* ws_base, cudaStream_t stream
   if (err != cudaSuccess || (err = launch_prepare(items, ws, stream, false)) != cudaSuccess) return err;
   if (items.total_tiles == 0) return cudaSuccess;
   return launch_main<false>(items, ws, stream, dev);
+}
+
+cudaError_t launch_wait_selftest(void* ws_base, cudaStream_t stream) {
+  // workspace: header | never (u32, zero) | gave_up[3] u32
+  DecWs ws = dec_ws(ws_base, 1, 0);
+  uint32_t* words = reinterpret_cast<uint32_t*>(static_cast<char*>(ws_base) + sizeof(WsHeader));
+  cudaError_t err = cudaMemsetAsync(ws_base, 0, sizeof(WsHeader) + 16, stream);
+  if (err != cudaSuccess) return err;
+  wait_selftest<<<1, 96, 0, stream>>>(ws, words, words + 1);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode_inplace(const Items& items, void* ws_base, cudaStream_t stream, const DeviceInfo& dev) {

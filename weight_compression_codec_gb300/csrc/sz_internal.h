@@ -23,6 +23,8 @@ cudaError_t launch_calibrate(const Items& items, void* ws, cudaStream_t stream, 
 cudaError_t launch_encode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev,
                           double gate = -1.0, sz_gate_report* report = nullptr);
 cudaError_t launch_decode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
+// diagnostic: each kind of bounded wait, on something that never completes
+cudaError_t launch_wait_selftest(void* ws, cudaStream_t stream);
 // in-place slot decode (items with payload == out; ip_ws workspace)
 cudaError_t launch_decode_inplace(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
 // calibrate + encode in one streaming pass (CeWs workspace), then placement
