@@ -271,17 +271,18 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-KERNEL_SOURCES = {"cal_hist": "sz_calibrate.cu", "enc_main": "sz_encode.cu", "enc_place": "sz_encode.cu",
-                  "dec_main": "sz_decode.cu", "dec_main_inplace": "sz_decode.cu", "dip_stash": "sz_decode.cu"}
+KERNEL_SOURCES = {"cal_hist": ("sz_calibrate.cu", "sz_count.cuh"),
+                  "enc_main": ("sz_encode.cu", "sz_chunk.cuh"), "enc_place": ("sz_encode.cu", "sz_chunk.cuh"),
+                  "dec_main": ("sz_decode.cu",), "dec_main_inplace": ("sz_decode.cu",), "dip_stash": ("sz_decode.cu",)}
 
 
 def kernel_source_sha(kernel: str) -> str:
-    """Hash of the sources a kernel is built from (its .cu file, the shared
-    device header and the ABI header): a recorded ncu traffic figure is only
-    reported while this matches."""
+    """Hash of the sources a kernel is built from (its .cu file and the device
+    headers it includes, the shared device header and the ABI header): a
+    recorded ncu traffic figure is only reported while this matches."""
     h = hashlib.sha256()
-    for f in (CSRC / KERNEL_SOURCES[kernel], CSRC / "sz_device.cuh", CSRC / "sz_internal.h",
-              ROOT / "include" / "splitzip.h"):
+    for f in [CSRC / name for name in KERNEL_SOURCES[kernel]] + [
+            CSRC / "sz_device.cuh", CSRC / "sz_internal.h", ROOT / "include" / "splitzip.h"]:
         h.update(f.read_bytes())
     return h.hexdigest()[:16]
 

@@ -192,8 +192,11 @@ SZ_API int sz_calibrate(const uint16_t* d_x, uint64_t n, sz_codebook* d_codebook
                         void* d_workspace, size_t workspace_bytes, sz_stream stream);
 
 /* Encode ("splitzip_codec.py" encode_torch + assemble_payload) of d_x[0..n)
- * with *d_codebook (any codebook: escapes follow from it) into
- * d_payload[0..comp_bytes); writes *d_meta.  If the payload would exceed
+ * with *d_codebook into d_payload[0..comp_bytes); writes *d_meta.  Any
+ * codebook whose enc_lut entries are 0..15 or SZ_ESCAPE_CODE will do, such as
+ * one calibrated on another tensor: the escapes follow from it.  Other
+ * enc_lut values are not checked and give an unspecified payload (never a
+ * fault).  If the payload would exceed
  * `capacity`, the payload is not valid and d_meta->status and the workspace
  * flags get SZ_FLAG_CAPACITY; no byte beyond capacity is written. */
 SZ_API int sz_encode(const uint16_t* d_x, uint64_t n, const sz_codebook* d_codebook,

@@ -139,7 +139,11 @@ __device__ __forceinline__ uint32_t encode_chunk8(const Stage& st, uint32_t warp
   uint8_t* pkw = st.payload + (g >> 1) + (e0 >> 1);
   uint8_t* smw = st.payload + st.off_sm + g + e0;
   const bool sm8 = ((st.off_sm & 7u) == 0);
-  uint32_t lane_esc = 0;  // bit 8*row + k: element k of this lane's 8 in `row` escapes
+  // Escape flags of this lane's 8 elements in the 4 rows: element b (< 4) of
+  // row r at bit 8b + 2r, element 4 + b at bit 8b + 2r + 1.  enc_lut values are
+  // 0..15 or SZ_ESCAPE_CODE (16): bit 4 of a code marks an escape, whose low
+  // nibble, the code packed into pk, is already 0.
+  uint32_t lane_esc = 0;
 #pragma unroll
   for (int row = 0; row < 4; ++row) {
     const uint4 v = *reinterpret_cast<const uint4*>(xw + row * 256);
@@ -150,16 +154,8 @@ __device__ __forceinline__ uint32_t encode_chunk8(const Stage& st, uint32_t warp
     const uint32_t hi = uint32_t(lut[__byte_perm(a2, 0, 0x4441)]) | (uint32_t(lut[__byte_perm(a2, 0, 0x4443)]) << 8) |
                         (uint32_t(lut[__byte_perm(a3, 0, 0x4441)]) << 16) |
                         (uint32_t(lut[__byte_perm(a3, 0, 0x4443)]) << 24);
-    uint32_t clo = lo & 0x0F0F0F0Fu, chi = hi & 0x0F0F0F0Fu;
-    if ((lo | hi) & 0xF0F0F0F0u) {  // an enc_lut value >= 16: escape, stored as code 0
-      const uint32_t mlo = (((lo & 0xF0F0F0F0u) >> 4) + 0x7F7F7F7Fu) & 0x80808080u;
-      const uint32_t mhi = (((hi & 0xF0F0F0F0u) >> 4) + 0x7F7F7F7Fu) & 0x80808080u;
-      clo &= ~((mlo >> 7) * 0xFFu);
-      chi &= ~((mhi >> 7) * 0xFFu);
-      // gather bit 7 of each byte (element k of the 8) into bit k of this row's byte
-      const uint32_t g = ((((mlo >> 7) * 0x00204081u) >> 21) & 0xFu) | (((((mhi >> 7) * 0x00204081u) >> 21) & 0xFu) << 4);
-      lane_esc |= g << (8 * row);
-    }
+    lane_esc |= (((lo >> 4) & 0x01010101u) | ((hi >> 3) & 0x02020202u)) << (2 * row);
+    const uint32_t clo = lo & 0x0F0F0F0Fu, chi = hi & 0x0F0F0F0Fu;
     const uint32_t tlo = clo | (clo >> 4), thi = chi | (chi >> 4);
     *reinterpret_cast<uint32_t*>(pkw + row * 128) = __byte_perm(tlo, thi, 0x6420);
     const uint32_t s01 = sm_quad(v.x, v.y);
@@ -178,35 +174,41 @@ __device__ __forceinline__ uint32_t encode_chunk8(const Stage& st, uint32_t warp
   uint32_t multi = 0;  // non-zero if this lane has two or more escapes in a row
 #pragma unroll
   for (int row = 0; row < 4; ++row) {
-    const uint32_t b = (lane_esc >> (8 * row)) & 0xFFu;
-    multi |= b & (b - 1u);
+    const uint32_t m = (lane_esc >> (2 * row)) & 0x03030303u;
+    multi |= m & (m - 1u);
   }
   uint32_t run = 0;
   if (!__any_sync(0xFFFFFFFFu, multi != 0)) {
     // at most one escape per lane and row: a ballot per row places them
 #pragma unroll
     for (int row = 0; row < 4; ++row) {
-      const uint32_t byte = (lane_esc >> (8 * row)) & 0xFFu;
-      const uint32_t b = __ballot_sync(0xFFFFFFFFu, byte != 0);
-      if (byte) {
-        const uint32_t elem = uint32_t(row) * 256u + lane * 8u + uint32_t(__ffs(byte) - 1);  // chunk-local
+      const uint32_t m = (lane_esc >> (2 * row)) & 0x03030303u;
+      const uint32_t b = __ballot_sync(0xFFFFFFFFu, m != 0);
+      if (m) {
+        const uint32_t p = uint32_t(__ffs(m) - 1);  // 8 (k & 3) + (k >> 2)
+        const uint32_t elem = uint32_t(row) * 256u + lane * 8u + (p >> 3) + ((p & 1u) << 2);  // chunk-local
         slot[run + __popc(b & lane_lt)] = elem | ((uint32_t(xc[elem]) << 9) & 0x00FF0000u);
       }
       run += __popc(b);
     }
     return run;
   }
-  uint32_t before[4];
+  // Some lane has several escapes in a row: each row's flags as a byte, bit k
+  // for element k (bits 0, 8, 16, 24 gathered to 0..3 by one multiply).
+  uint32_t bytes[4], before[4];
 #pragma unroll
   for (int row = 0; row < 4; ++row) {
+    const uint32_t m = lane_esc >> (2 * row);
+    const uint32_t m0 = m & 0x01010101u, m1 = (m >> 1) & 0x01010101u;
+    bytes[row] = (((m0 * 0x00204081u) >> 21) & 0xFu) | ((((m1 * 0x00204081u) >> 21) & 0xFu) << 4);
     uint32_t total;
-    before[row] = run + warp_prefix(__popc((lane_esc >> (8 * row)) & 0xFFu), lane, &total);
+    before[row] = run + warp_prefix(__popc(bytes[row]), lane, &total);
     run += total;
   }
 #pragma unroll
   for (int row = 0; row < 4; ++row) {
     uint32_t pos = before[row];
-    for (uint32_t m = (lane_esc >> (8 * row)) & 0xFFu; m; m &= m - 1) {
+    for (uint32_t m = bytes[row]; m; m &= m - 1) {
       const uint32_t elem = uint32_t(row) * 256u + lane * 8u + uint32_t(__ffs(m) - 1);  // chunk-local
       slot[pos] = elem | ((uint32_t(xc[elem]) << 9) & 0x00FF0000u);  // position | exponent << 16
       ++pos;
