@@ -509,7 +509,7 @@ def run_ours(args, world, rank, local):
         assert hd.flags() == 0
         assert all(torch.equal(y, x.view(torch.int16)) for y, x in zip(outs, xs)), "decode from host"
         # host-to-device bandwidth drifts on a shared host: time the three
-        # interleaved, several rounds, and keep each one's median
+        # interleaved, several repetitions, and keep each one's median
         kh = max(3, K // 2)
         t = {name: [] for name in fns}
         for _ in range(5):
