@@ -63,6 +63,30 @@ def test_codebook_from_other_tensor():
     roundtrip_single(x, codebook_from=np.array([0x3F80, 0x3F80, 0x0000], dtype=np.uint16))
 
 
+def test_out_of_contract_enc_lut_stays_in_bounds():
+    """enc_lut entries other than 0..15 and SZ_ESCAPE_CODE are not checked: the
+    payload is then unspecified, but encode and decode stay within their
+    buffers, flag nothing and agree with the layout of the escape count."""
+    from weight_compression_codec_gb300 import binding as B
+
+    x = inputs.gaussian(3 * 8192 + 77, 1.0, seed=21)  # full tiles and a ragged one
+    rng = np.random.default_rng(21)
+    c = B.SzCodebook()
+    c.enc_lut[:] = rng.integers(0, 256, 256).tolist()
+    c.dec_lut[:] = rng.integers(0, 256, 16).tolist()
+    c.n_top, c.top_count, c.n, c.coverage = 16, 0, x.size, 0.5
+    cb = torch.frombuffer(bytearray(bytes(c)), dtype=torch.uint8).to(DEV)
+    ws = sz.Workspace(DEV)
+    payload, meta = sz.sz_encode(to_dev(x), cb, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    m = sz.read_meta(meta)
+    assert m.status == 0 and m.n_esc <= x.size
+    assert m.as_tuple() == oracle.layout(x.size, m.n_esc).as_tuple()
+    sz.sz_decode(payload, meta, cb, x.size, workspace=ws)
+    torch.cuda.synchronize()
+    assert sz.sz_workspace_flags(ws.buf) == 0
+
+
 def test_dense_escapes_spill_path():
     """Tiles with more escapes than the decoder stages in shared memory."""
     x = inputs.edge_case(3 * 8192 + 77, seed=11)
