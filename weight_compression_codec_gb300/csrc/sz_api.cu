@@ -2,6 +2,7 @@
 // argument checks, workspace sizing and kernel dispatch.  No call allocates
 // memory or synchronises the stream (except sz_workspace_flags, which exists
 // to read the device status back).
+#include <atomic>
 #include <cstring>
 
 #include "sz_internal.h"
@@ -11,19 +12,21 @@ namespace sz {
 thread_local TimingHook g_timing = {nullptr, nullptr};
 
 cudaError_t device_info(DeviceInfo* info) {
-  static int cached_sms[64] = {0};
+  // SM count per device, queried once; host threads may race to fill an
+  // entry, all with the same value
+  static std::atomic<int> cached_sms[64];
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (cached_sms[dev] == 0) {
-    int sms = 0;
+  int sms = cached_sms[dev].load(std::memory_order_relaxed);
+  if (sms == 0) {
     err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    cached_sms[dev] = sms;
+    cached_sms[dev].store(sms, std::memory_order_relaxed);
   }
   info->device = dev;
-  info->num_sms = cached_sms[dev];
+  info->num_sms = sms;
   return cudaSuccess;
 }
 
