@@ -1,0 +1,119 @@
+"""Seeded random batches through the whole path, every result against the oracle.
+
+Each batch draws:
+- a tensor count;
+- sizes: empty, tiny, around chunk and tile edges, or up to a few hundred
+  thousand elements;
+- value distributions: Gaussians of any scale, escape-heavy bit patterns,
+  mixtures of the two, constant tensors and uniform bit patterns.
+
+Some tensors are encoded with a codebook calibrated on another tensor of the
+batch, which forces escapes.  The batch is calibrated, encoded, decoded out of
+place, and decoded in place for the tensors whose payload fits their raw size.
+Every codebook, meta, payload and decode is compared with the oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import weight_compression_codec_gb300 as sz
+from weight_compression_codec_gb300 import inputs
+
+from gpu_util import DEV, check_codebook, to_dev, to_np_u16
+
+pytestmark = pytest.mark.gpu
+
+EDGE_SIZES = [0, 1, 2, 3, 5, 1023, 1024, 1025, 4095, 4096, 8191, 8192, 8193, 16383, 16384, 16385, 24577, 65536]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    sz.build()
+    torch.cuda.set_device(DEV)
+
+
+def _tensor(rng: np.random.Generator, n: int, seed: int) -> np.ndarray:
+    kind = int(rng.integers(0, 5))
+    if n == 0:
+        return np.zeros(0, np.uint16)
+    if kind == 0:
+        return inputs.gaussian(n, float(10 ** rng.uniform(-3, 1)), seed=seed)
+    if kind == 1:
+        return inputs.edge_case(n, seed=seed)
+    if kind == 2:
+        x = inputs.gaussian(n, 0.05, seed=seed)
+        mask = rng.random(n) < rng.uniform(0.0, 0.3)
+        x[mask] = inputs.edge_case(n, seed=seed + 1)[mask]
+        return x
+    if kind == 3:
+        return np.full(n, int(rng.integers(0, 65536)), dtype=np.uint16)
+    return rng.integers(0, 65536, n, dtype=np.uint16)  # every exponent occurs
+
+
+def _batch(seed: int) -> list[np.ndarray]:
+    rng = np.random.default_rng(1000 + seed)
+    count = int(rng.integers(1, 25))
+    sizes = [int(rng.choice(EDGE_SIZES)) if rng.random() < 0.6 else int(rng.integers(1, 300_000))
+             for _ in range(count)]
+    return [_tensor(rng, n, seed * 100 + i) for i, n in enumerate(sizes)]
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_batch_matches_oracle(seed):
+    arrays = _batch(seed)
+    count = len(arrays)
+    b = sz.Batch([to_dev(a) if a.size else torch.empty(0, dtype=torch.int16, device=DEV) for a in arrays])
+    ws = sz.Workspace(DEV)
+    sz.sz_calibrate_many(b.table, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    torch.cuda.synchronize()
+    ocbs = [oracle.calibrate(a) for a in arrays]
+    cbs = b.codebooks.cpu().numpy()
+    for i, a in enumerate(arrays):
+        check_codebook(sz.codebook_from_bytes(cbs[i]), ocbs[i], a.size)
+
+    # a third of the tensors take another tensor's codebook: row i copies row
+    # j as it is now, which may already hold a third tensor's codebook
+    rng = np.random.default_rng(2000 + seed)
+    use = list(range(count))  # use[i]: the tensor whose oracle codebook row i holds
+    for i in range(count):
+        if count > 1 and rng.random() < 1 / 3:
+            j = int(rng.integers(0, count))
+            b.codebooks[i].copy_(b.codebooks[j])
+            use[i] = use[j]
+    sz.sz_encode_many(b.table, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    sz.sz_decode_many(b.table, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    torch.cuda.synchronize()
+    metas = b.metas.cpu().numpy()
+    expect = []
+    for i, a in enumerate(arrays):
+        opay, om = oracle.encode(a, ocbs[use[i]])
+        m = sz.meta_from_bytes(metas[i])
+        assert m.status == 0 and m.as_tuple() == om.as_tuple(), (seed, i, m, om)
+        assert np.array_equal(b.payload_view(i, m.comp_bytes).cpu().numpy(), opay), f"payload {i}"
+        assert np.array_equal(to_np_u16(b.out_view(i)), a), f"decode {i}"
+        expect.append((opay, om))
+
+    # in place, for every tensor whose payload fits its raw size
+    fit = [i for i, (_, om) in enumerate(expect) if om.comp_bytes <= 2 * arrays[i].size]
+    if not fit:
+        return
+    gen = torch.Generator(device=DEV).manual_seed(seed)
+    slots = []
+    for i in fit:
+        s = torch.randint(-32768, 32767, (arrays[i].size,), dtype=torch.int16, device=DEV, generator=gen)
+        om = expect[i][1]
+        s.view(torch.uint8)[:om.comp_bytes].copy_(b.payload_view(i, om.comp_bytes))
+        slots.append(s)
+    t = sz.slot_table(slots, [b.codebooks[i] for i in fit], [b.metas[i] for i in fit])
+    sz.sz_decode_inplace_many(t, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    torch.cuda.synchronize()
+    for k, i in enumerate(fit):
+        assert np.array_equal(to_np_u16(slots[k]), arrays[i]), f"slot of tensor {i}"
