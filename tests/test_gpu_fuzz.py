@@ -10,7 +10,9 @@ Each batch draws:
 Some tensors are encoded with a codebook calibrated on another tensor of the
 batch, which forces escapes.  The batch is calibrated, encoded, decoded out of
 place, and decoded in place for the tensors whose payload fits their raw size.
-Every codebook, meta, payload and decode is compared with the oracle.
+Other batches go through the fused calibrate + encode, the decode from pinned
+host memory and the coverage gate.  Every codebook, meta, payload, report and
+decode is compared with the oracle.
 """
 from __future__ import annotations
 
@@ -20,6 +22,7 @@ import torch
 
 import oracle
 import weight_compression_codec_gb300 as sz
+from weight_compression_codec_gb300 import binding as B
 from weight_compression_codec_gb300 import inputs
 
 from gpu_util import DEV, check_codebook, to_dev, to_np_u16
@@ -117,3 +120,58 @@ def test_random_batch_matches_oracle(seed):
     torch.cuda.synchronize()
     for k, i in enumerate(fit):
         assert np.array_equal(to_np_u16(slots[k]), arrays[i]), f"slot of tensor {i}"
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_batch_fused_from_host_and_gated(seed):
+    arrays = _batch(100 + seed)
+    count = len(arrays)
+    ocbs = [oracle.calibrate(a) for a in arrays]
+    oenc = [oracle.encode(a, c) for a, c in zip(arrays, ocbs)]
+    devs = [to_dev(a) if a.size else torch.empty(0, dtype=torch.int16, device=DEV) for a in arrays]
+    ws = sz.Workspace(DEV)
+
+    # fused calibrate + encode
+    fus = sz.Batch(devs)
+    sz.sz_calibrate_encode_many(fus.table, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    torch.cuda.synchronize()
+    cbs = fus.codebooks.cpu().numpy()
+    metas = [sz.meta_from_bytes(fus.metas[i].cpu().numpy()) for i in range(count)]
+    for i, a in enumerate(arrays):
+        check_codebook(sz.codebook_from_bytes(cbs[i]), ocbs[i], a.size)
+        opay, om = oenc[i]
+        assert metas[i].status == 0 and metas[i].as_tuple() == om.as_tuple(), (seed, i)
+        assert np.array_equal(fus.payload_view(i, om.comp_bytes).cpu().numpy(), opay), f"fused payload {i}"
+
+    # decode from pinned host memory, the payloads back to back in one blob
+    blob = fus.payload.cpu().pin_memory()
+    views = [blob[o:o + m.comp_bytes] for o, m in zip(fus.payload_off, metas)]
+    outs = [torch.full((a.size,), 7, dtype=torch.int16, device=DEV) for a in arrays]
+    staging = max(4 * max(m.comp_bytes for m in metas), 1 << 20)
+    hd = sz.HostDecode(views, metas, [fus.codebooks[i] for i in range(count)], outs, staging)
+    hd.run()
+    assert hd.flags() == 0
+    torch.cuda.synchronize()
+    for i, a in enumerate(arrays):
+        assert np.array_equal(to_np_u16(outs[i]), a), f"decode from host {i}"
+
+    # coverage gate at a random threshold
+    gate = float(np.random.default_rng(3000 + seed).uniform(0.2, 1.0))
+    g = sz.Batch(devs)
+    g.payload.fill_(0x5A)
+    sz.sz_calibrate_many(g.table, workspace=ws)
+    report = sz.sz_encode_gated_many(g.table, gate, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    torch.cuda.synchronize()
+    for i, a in enumerate(arrays):
+        m = sz.meta_from_bytes(g.metas[i].cpu().numpy())
+        opay, om = oenc[i]
+        if oracle.gated(ocbs[i].coverage, gate):
+            assert m.status == B.SZ_META_GATED and m.comp_bytes == 0, (seed, i)
+            assert bool(torch.all(g.payload_view(i) == 0x5A)), f"gated tensor {i}: payload written"
+        else:
+            assert m.status == 0 and m.as_tuple() == om.as_tuple(), (seed, i)
+            assert np.array_equal(g.payload_view(i, om.comp_bytes).cpu().numpy(), opay), f"gated payload {i}"
+    expect = oracle.gate_report([a.size for a in arrays], [c.coverage for c in ocbs], [om for _, om in oenc], gate)
+    assert sz.read_gate_report(report) == expect
