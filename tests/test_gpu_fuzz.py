@@ -175,3 +175,39 @@ def test_random_batch_fused_from_host_and_gated(seed):
             assert np.array_equal(g.payload_view(i, om.comp_bytes).cpu().numpy(), opay), f"gated payload {i}"
     expect = oracle.gate_report([a.size for a in arrays], [c.coverage for c in ocbs], [om for _, om in oenc], gate)
     assert sz.read_gate_report(report) == expect
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_inplace_random_sizes_and_escape_rates(seed):
+    """In-place decode of the oracle's payloads: tensors of up to ~730 tiles,
+    with escape rates up to what still fits the slot (comp_bytes <= 2n), so the
+    three decode phases and the stash take every proportion."""
+    from gpu_util import oracle_codebook_bytes
+
+    rng = np.random.default_rng(4000 + seed)
+    count = int(rng.integers(1, 7))
+    arrays, slots, cbs, metas = [], [], [], []
+    while len(arrays) < count:
+        k = len(arrays)
+        n = int(rng.integers(1, 6_000_000)) if rng.random() < 0.7 else \
+            max(1, int(rng.integers(1, 40)) * 8192 + int(rng.integers(-2, 3)))
+        x = inputs.gaussian(n, 0.02, seed=seed * 10 + k)
+        mask = rng.random(n) < rng.uniform(0.0, 0.12)
+        x[mask] = inputs.edge_case(n, seed=seed * 10 + k)[mask]
+        cb = oracle.calibrate(x)
+        pay, m = oracle.encode(x, cb)
+        if m.comp_bytes > 2 * n:
+            continue  # an expanding tensor cannot sit in its slot
+        s = torch.randint(-32768, 32767, (n,), dtype=torch.int16, device=DEV)
+        s.view(torch.uint8)[:m.comp_bytes].copy_(torch.from_numpy(pay).to(DEV))
+        arrays.append(x)
+        slots.append(s)
+        cbs.append(torch.frombuffer(bytearray(oracle_codebook_bytes(cb, n)), dtype=torch.uint8).to(DEV))
+        metas.append(torch.frombuffer(bytearray(sz.meta_to_bytes(m)), dtype=torch.uint8).to(DEV))
+    t = sz.slot_table(slots, cbs, metas)
+    ws = sz.Workspace(DEV)
+    sz.sz_decode_inplace_many(t, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    torch.cuda.synchronize()
+    for k, x in enumerate(arrays):
+        assert np.array_equal(to_np_u16(slots[k]), x), f"slot {k} (n = {x.size})"
