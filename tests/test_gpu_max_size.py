@@ -83,3 +83,71 @@ def test_max_elements_round_trip_and_in_place():
     assert torch.equal(slot, xd), "in-place decode"
     del slot, xd, wd
     torch.cuda.empty_cache()
+
+
+def test_max_item_count_round_trip_and_in_place():
+    """SZ_MANY_MAX_ITEMS (65,535) tensors in one table: 1 to 4,000 elements
+    each (some at tile edges, a few of one element), every codebook, meta and
+    payload against the oracle, every decode and in-place decode exact."""
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    sz.build()
+    torch.cuda.set_device(DEV)
+    count = B.SZ_MANY_MAX_ITEMS
+    rng = np.random.default_rng(91)
+    sizes = rng.integers(1, 4_000, count)
+    sizes[::97] = 8192
+    sizes[1::97] = 8193
+    sizes[2::997] = 1
+    offs = np.concatenate([[0], np.cumsum((sizes + 7) // 8 * 8)])  # 16-byte aligned views
+    flat = np.zeros(int(offs[-1]), np.uint16)
+    for i in range(0, count, 4096):  # a few distributions, changing along the table
+        j = min(count, i + 4096)
+        a, b = int(offs[i]), int(offs[j])
+        flat[a:b] = inputs.gaussian(b - a, float(10 ** rng.uniform(-3, 0.5)), seed=100 + i)
+        heavy = rng.random(b - a) < rng.uniform(0, 0.05)
+        flat[a:b][heavy] = inputs.edge_case(b - a, seed=200 + i)[heavy]
+    arrays = [flat[offs[i]:offs[i] + sizes[i]] for i in range(count)]
+    dflat = torch.from_numpy(flat.view(np.int16)).to(DEV)
+    views = [dflat[int(offs[i]):int(offs[i]) + int(sizes[i])] for i in range(count)]
+    b = sz.Batch(views)
+    ws = sz.Workspace(DEV)
+    sz.sz_calibrate_many(b.table, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    sz.sz_encode_many(b.table, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    sz.sz_decode_many(b.table, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    torch.cuda.synchronize()
+    cbs = b.codebooks.cpu().numpy()
+    metas = b.metas.cpu().numpy()
+    pay = b.payload.cpu().numpy()
+    out = b.out.view(torch.int16).cpu().numpy().view(np.uint16)
+    om_list = []
+    for i, x in enumerate(arrays):
+        ocb = oracle.calibrate(x)
+        check_codebook(sz.codebook_from_bytes(cbs[i]), ocb, x.size)
+        opay, om = oracle.encode(x, ocb)
+        m = sz.meta_from_bytes(metas[i])
+        assert m.status == 0 and m.as_tuple() == om.as_tuple(), i
+        po = b.payload_off[i]
+        assert np.array_equal(pay[po:po + om.comp_bytes], opay), f"payload {i}"
+        oo = b.out_off[i] // 2
+        assert np.array_equal(out[oo:oo + x.size], x), f"decode {i}"
+        om_list.append((opay, om))
+
+    # in place: every tensor whose payload fits its slot, slots packed in one buffer
+    fit = [i for i, (_, om) in enumerate(om_list) if om.comp_bytes <= 2 * arrays[i].size]
+    soffs = np.concatenate([[0], np.cumsum([(sizes[i] + 7) // 8 * 8 for i in fit])])
+    host_slots = np.full(int(soffs[-1]), 0x5A5A, np.uint16)
+    for k, i in enumerate(fit):
+        opay, om = om_list[i]
+        host_slots[soffs[k]:soffs[k] + sizes[i]].view(np.uint8)[:om.comp_bytes] = opay
+    dslots = torch.from_numpy(host_slots.view(np.int16)).to(DEV)
+    slots = [dslots[int(soffs[k]):int(soffs[k]) + int(sizes[i])] for k, i in enumerate(fit)]
+    t = sz.slot_table(slots, [b.codebooks[i] for i in fit], [b.metas[i] for i in fit])
+    sz.sz_decode_inplace_many(t, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    back = dslots.cpu().numpy().view(np.uint16)
+    for k, i in enumerate(fit):
+        assert np.array_equal(back[soffs[k]:soffs[k] + sizes[i]], arrays[i]), f"slot of tensor {i}"
+    assert len(fit) > count // 2
