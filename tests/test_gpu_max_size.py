@@ -87,8 +87,9 @@ def test_max_elements_round_trip_and_in_place():
 
 def test_max_item_count_round_trip_and_in_place():
     """SZ_MANY_MAX_ITEMS (65,535) tensors in one table: 1 to 4,000 elements
-    each (some at tile edges, a few of one element), every codebook, meta and
-    payload against the oracle, every decode and in-place decode exact."""
+    each (some at tile edges, a few of one element). Separate calls, the fused
+    calibrate + encode and the gated encode give every codebook, meta, payload
+    and report the oracle gives; every decode and in-place decode is exact."""
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     sz.build()
     torch.cuda.set_device(DEV)
@@ -122,7 +123,7 @@ def test_max_item_count_round_trip_and_in_place():
     metas = b.metas.cpu().numpy()
     pay = b.payload.cpu().numpy()
     out = b.out.view(torch.int16).cpu().numpy().view(np.uint16)
-    om_list = []
+    om_list, ocbs = [], []
     for i, x in enumerate(arrays):
         ocb = oracle.calibrate(x)
         check_codebook(sz.codebook_from_bytes(cbs[i]), ocb, x.size)
@@ -134,6 +135,7 @@ def test_max_item_count_round_trip_and_in_place():
         oo = b.out_off[i] // 2
         assert np.array_equal(out[oo:oo + x.size], x), f"decode {i}"
         om_list.append((opay, om))
+        ocbs.append(ocb)
 
     # in place: every tensor whose payload fits its slot, slots packed in one buffer
     fit = [i for i, (_, om) in enumerate(om_list) if om.comp_bytes <= 2 * arrays[i].size]
@@ -151,3 +153,38 @@ def test_max_item_count_round_trip_and_in_place():
     for k, i in enumerate(fit):
         assert np.array_equal(back[soffs[k]:soffs[k] + sizes[i]], arrays[i]), f"slot of tensor {i}"
     assert len(fit) > count // 2
+
+    # the fused calibrate + encode over the same table
+    fus = sz.Batch(views)
+    sz.sz_calibrate_encode_many(fus.table, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    torch.cuda.synchronize()
+    fcbs, fmetas, fpay = fus.codebooks.cpu().numpy(), fus.metas.cpu().numpy(), fus.payload.cpu().numpy()
+    for i, x in enumerate(arrays):
+        opay, om = om_list[i]
+        check_codebook(sz.codebook_from_bytes(fcbs[i]), ocbs[i], x.size)
+        assert sz.meta_from_bytes(fmetas[i]).as_tuple() == om.as_tuple(), f"fused meta {i}"
+        po = fus.payload_off[i]
+        assert np.array_equal(fpay[po:po + om.comp_bytes], opay), f"fused payload {i}"
+    del fus, fpay
+
+    # the coverage gate at 0.99, with its report
+    g = sz.Batch(views)
+    sz.sz_calibrate_many(g.table, workspace=ws)
+    report = sz.sz_encode_gated_many(g.table, 0.99, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    torch.cuda.synchronize()
+    gmetas = g.metas.cpu().numpy()
+    gpay = g.payload.cpu().numpy()
+    for i, x in enumerate(arrays):
+        opay, om = om_list[i]
+        m = sz.meta_from_bytes(gmetas[i])
+        if oracle.gated(ocbs[i].coverage, 0.99):
+            assert m.status == B.SZ_META_GATED and m.comp_bytes == 0, f"gated meta {i}"
+        else:
+            assert m.status == 0 and m.as_tuple() == om.as_tuple(), f"gated-call meta {i}"
+            po = g.payload_off[i]
+            assert np.array_equal(gpay[po:po + om.comp_bytes], opay), f"gated-call payload {i}"
+    expect = oracle.gate_report([x.size for x in arrays], [c.coverage for c in ocbs], [om for _, om in om_list], 0.99)
+    assert sz.read_gate_report(report) == expect
+    assert 0 < expect["tensors_gated"] < count
