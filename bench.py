@@ -276,7 +276,7 @@ def measured_peaks() -> dict:
 
 KERNEL_SOURCES = {"cal_hist": ("sz_calibrate.cu", "sz_count.cuh"),
                   "enc_main": ("sz_encode.cu", "sz_chunk.cuh"), "enc_place": ("sz_encode.cu", "sz_chunk.cuh"),
-                  "dec_main": ("sz_decode.cu",), "dec_main_inplace": ("sz_decode.cu",), "dip_stash": ("sz_decode.cu",)}
+                  "dec_flat": ("sz_decode.cu",), "dec_inplace": ("sz_decode.cu",), "dip_stash": ("sz_decode.cu",)}
 
 
 def kernel_source_sha(kernel: str) -> str:
@@ -572,8 +572,8 @@ def run_ours(args, world, rank, local):
         kern_ms = float(np.mean([kb.elapsed_time(ka) for _, _, kb, ka in evs[1:]]))
         stash = sum(sz.inplace_plan(a.size, m.n_esc, 0)["stash_bytes"] for a, m in zip(arrays, metas) if a.size)
         alg = comp_total + raw_bytes
-        inplace = {"call_ms": call_ms, "kernel": "dec_main (in place)", "kernel_ms": kern_ms,
-                   "traffic": recorded_traffic("dec_main_inplace", args.workload),
+        inplace = {"call_ms": call_ms, "kernel": "dec_inplace", "kernel_ms": kern_ms,
+                   "traffic": recorded_traffic("dec_inplace", args.workload),
                    "stash_traffic": recorded_traffic("dip_stash", args.workload),
                    "raw_gbs": raw_bytes / (call_ms * 1e-3) / 1e9, "alg_bytes": alg,
                    "achieved_gbs": alg / (call_ms * 1e-3) / 1e9, "stash_bytes": stash,
@@ -591,11 +591,11 @@ def run_ours(args, world, rank, local):
     ms = {"calibrate": float(np.mean(t_cal)), "encode": float(np.mean(t_enc)), "decode": float(np.mean(t_dec))}
     # algorithmic bytes of each streaming kernel: cal_hist reads x; enc_main
     # reads x and writes the pk and sm sections (the escape streams are
-    # written by enc_place); dec_main reads the payload and writes x
+    # written by enc_place); dec_flat reads the payload and writes x
     dense_bytes = sum(m.off_cid for m in metas)
     alg = {"calibrate": raw_bytes, "encode": raw_bytes + dense_bytes, "decode": comp_total + raw_bytes}
     alg_ops = {"calibrate": raw_bytes, "encode": raw_bytes + comp_total, "decode": comp_total + raw_bytes}
-    kname = {"calibrate": "cal_hist", "encode": "enc_main", "decode": "dec_main"}
+    kname = {"calibrate": "cal_hist", "encode": "enc_main", "decode": "dec_flat"}
     kernels = {}
     for k in ms:
         achieved = alg[k] / (ms[k] * 1e-3) / 1e9

@@ -173,7 +173,10 @@ SZ_API uint64_t sz_max_payload_bytes(uint64_t n);
  * returns the total tile count in *h_total_tiles. */
 SZ_API int sz_items_prepare(sz_item* h_items, uint32_t count, uint64_t* h_total_tiles);
 
-/* Workspace sizes (bytes) of the compute calls. */
+/* Workspace sizes (bytes) of the compute calls.  The out-of-place decode
+ * needs only its 256-byte status header, whatever the tensors: each CTA of its
+ * single kernel checks the tensors of its tiles and finds their escape ranges
+ * itself. */
 SZ_API size_t sz_calibrate_workspace_bytes(uint32_t count);
 SZ_API size_t sz_encode_workspace_bytes(uint32_t count, uint64_t total_tiles);
 SZ_API size_t sz_decode_workspace_bytes(uint32_t count, uint64_t total_tiles);
@@ -223,7 +226,12 @@ SZ_API int sz_decode(const uint8_t* d_payload, uint64_t payload_bytes, const sz_
  * few large tensors and many mid-size ones run equally well.
  *   calibrate: reads x, n, tile_begin; writes *codebook.
  *   encode:    reads x, n, codebook, payload, capacity, tile_begin; writes payload, *meta.
- *   decode:    reads payload (capacity readable bytes), meta, codebook, n, tile_begin; writes out. */
+ *   decode:    reads payload (capacity readable bytes), meta, codebook, n, tile_begin; writes out.
+ * An inconsistent tile_begin chain sets SZ_FLAG_ITEMS; calibrate and encode
+ * then write nothing, decode skips (and flags) the tiles it cannot place in
+ * a consistent tensor and may decode the others -- never writing outside a
+ * tensor's own output.  A tensor with n == 0 has nothing to decode, and decode
+ * does not read its meta. */
 SZ_API int sz_calibrate_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles,
                              void* d_workspace, size_t workspace_bytes, sz_stream stream);
 SZ_API int sz_encode_many(const sz_item* d_items, uint32_t count, uint64_t total_tiles,
@@ -376,10 +384,10 @@ SZ_API int sz_calibrate_encode_many(const sz_item* d_items, uint32_t count, uint
  * libraries allocate, or a latency-critical path that must not call
  * cudaMalloc (which may synchronise the device).  No counterpart in the
  * SplitZip pages: it is sz_decode with the workspace replaced by a fixed
- * scratch array inside the library (a file-scope __device__ array of about
- * 257 KiB, present on every device that loads the library until the process
- * exits).  Nothing is allocated per call: no cudaMalloc, cudaFree or
- * allocating library routine.
+ * scratch array inside the library (a file-scope __device__ array of 256
+ * bytes, the decode's status header, present on every device that loads the
+ * library until the process exits).  Nothing is allocated per call: no
+ * cudaMalloc, cudaFree or allocating library routine.
  *   Arguments are those of sz_decode, without the workspace; n must not
  *   exceed SZ_NOALLOC_MAX_ELEMS (larger tensors: SZ_ERR_ARG, use sz_decode).
  *   d_flags: optional device pointer (4-byte aligned) that receives the
@@ -398,7 +406,7 @@ SZ_API int sz_decode_noalloc(const uint8_t* d_payload, uint64_t payload_bytes, c
 /* Timing hook: `before` and `after` are cudaEvent_t handles (or NULL to
  * clear).  While set, every compute call made by the calling host thread
  * records `before` on its stream just before its main kernel (the streaming
- * pass: cal_hist, enc_main or dec_main) and `after` just after it, so the
+ * pass: cal_hist, enc_main, dec_flat or dec_inplace) and `after` just after it, so the
  * caller can time that kernel alone with cudaEventElapsedTime.  The events are
  * borrowed, never destroyed. */
 SZ_API int sz_set_timing_events(void* before, void* after);

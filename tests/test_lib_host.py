@@ -165,7 +165,9 @@ def test_host_decode_planner_on_the_host():
     step = (comp + 255) // 256 * 256  # halves are whole multiples of 256 bytes
     one = lib.sz_decode_many_host_scratch_bytes(items, metas, count, 2 * step)       # a tensor per group
     all6 = lib.sz_decode_many_host_scratch_bytes(items, metas, count, 2 * 6 * step)  # all in one group
-    assert one > 0 and all6 > one  # a larger group needs a larger decode workspace
+    # metas, item tables and the decode workspace (its 256-byte status header, whatever the groups)
+    r256 = lambda v: (v + 255) // 256 * 256
+    assert one == all6 == r256(count * 96) + r256(count * 64) + 256
     assert lib.sz_decode_many_host_scratch_bytes(items, metas, count, comp) == 0  # a payload exceeds half
     metas[3].n = n + 1
     assert lib.sz_decode_many_host_scratch_bytes(items, metas, count, 2 * step) == 0  # meta disagrees with n
@@ -256,5 +258,7 @@ def test_inplace_plan_rejects_bad_arguments(lib):
     assert lib.sz_inplace_plan(100, 101, 0, ctypes.byref(t)) == B.SZ_ERR_ARG
     assert lib.sz_inplace_plan(1, 0, 0, ctypes.byref(t)) == B.SZ_ERR_CAPACITY  # 8-byte payload, 2-byte slot
     assert lib.sz_inplace_plan(8192, 0, 0, None) == B.SZ_ERR_ARG
-    assert lib.sz_decode_inplace_workspace_bytes(3, 10) == (lib.sz_decode_workspace_bytes(3, 10) + 256
-                                                            + 10 * 8192 + 3 * 4352)
+    # header, item flags, escape ranges and tile map (256 bytes each here), read_done, stash
+    assert lib.sz_decode_inplace_workspace_bytes(3, 10) == 4 * 256 + 256 + 10 * 8192 + 3 * 4352
+    # the out-of-place decode finds everything in the kernel: its workspace is the status header
+    assert lib.sz_decode_workspace_bytes(3, 10) == lib.sz_decode_workspace_bytes(1, 1 << 19) == 256

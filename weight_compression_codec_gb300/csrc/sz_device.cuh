@@ -206,8 +206,14 @@ __host__ __device__ inline CeWs ce_ws(void* base, uint32_t count, uint64_t tiles
   return w;
 }
 
-// decode: header | item_flags[count] u32 | ranges[total_tiles] (k0, k1) u32x2 |
-//         tile_item[total_tiles] u32 (tables of more than one item)
+// out-of-place decode: the 256-byte header only.  Each CTA of the decode
+// kernel validates the tensors of its tiles and finds its tiles' escape
+// ranges itself, so there is nothing to prepare.
+__host__ __device__ constexpr uint64_t dec_ws_bytes(uint32_t /*count*/, uint64_t /*tiles*/) { return 256; }
+
+// in-place decode, prepared by dec_prepare: header | item_flags[count] u32 |
+// ranges[total_tiles] (k0, k1) u32x2 | tile_item[total_tiles] u32 (tables of
+// more than one item) | read_done | stash (see ip_ws)
 struct DecWs {
   WsHeader* hdr;
   uint32_t* item_flags;
@@ -216,10 +222,10 @@ struct DecWs {
   uint32_t* read_done;  // in-place decode: per tile, its in-place input has been read
   uint8_t* stash;       // in-place decode: the bytes copied aside
 };
-__host__ __device__ inline uint64_t dec_ws_bytes(uint32_t count, uint64_t tiles) {
+__host__ __device__ inline uint64_t prep_ws_bytes(uint32_t count, uint64_t tiles) {
   return 256 + round_up256(uint64_t(count) * 4) + round_up256(tiles * 8) + tile_map_bytes(dec_uses_tile_map(count), tiles);
 }
-__host__ __device__ inline DecWs dec_ws(void* base, uint32_t count, uint64_t tiles) {
+__host__ __device__ inline DecWs prep_ws(void* base, uint32_t count, uint64_t tiles) {
   char* p = static_cast<char*>(base);
   DecWs w;
   w.hdr = reinterpret_cast<WsHeader*>(p);
@@ -229,6 +235,17 @@ __host__ __device__ inline DecWs dec_ws(void* base, uint32_t count, uint64_t til
   w.ranges = reinterpret_cast<uint2*>(p);
   p += round_up256(tiles * 8);
   w.tile_item = dec_uses_tile_map(count) ? reinterpret_cast<uint32_t*>(p) : nullptr;
+  w.read_done = nullptr;
+  w.stash = nullptr;
+  return w;
+}
+// the out-of-place decode's view of its workspace: the header alone
+__host__ __device__ inline DecWs dec_ws(void* base) {
+  DecWs w;
+  w.hdr = static_cast<WsHeader*>(base);
+  w.item_flags = nullptr;
+  w.ranges = nullptr;
+  w.tile_item = nullptr;
   w.read_done = nullptr;
   w.stash = nullptr;
   return w;
@@ -340,14 +357,14 @@ __host__ __device__ inline IpDeps ip_deps(uint64_t n, uint64_t off_sm, uint64_t 
   return d;
 }
 
-// in-place decode workspace: the decode workspace | read_done[tiles] u32 | stash
+// in-place decode workspace: the prepared layout | read_done[tiles] u32 | stash
 __host__ __device__ inline uint64_t ip_ws_bytes(uint32_t count, uint64_t tiles) {
-  return dec_ws_bytes(count, tiles) + round_up256(tiles * 4) + tiles * kIpStashPerTile +
+  return prep_ws_bytes(count, tiles) + round_up256(tiles * 4) + tiles * kIpStashPerTile +
          uint64_t(count) * kIpStashPerItem;
 }
 __host__ __device__ inline DecWs ip_ws(void* base, uint32_t count, uint64_t tiles) {
-  DecWs w = dec_ws(base, count, tiles);
-  char* p = static_cast<char*>(base) + dec_ws_bytes(count, tiles);
+  DecWs w = prep_ws(base, count, tiles);
+  char* p = static_cast<char*>(base) + prep_ws_bytes(count, tiles);
   w.read_done = reinterpret_cast<uint32_t*>(p);
   w.stash = reinterpret_cast<uint8_t*>(p + round_up256(tiles * 4));
   return w;

@@ -22,7 +22,10 @@ cudaError_t launch_calibrate(const Items& items, void* ws, cudaStream_t stream, 
 // (meta status SZ_META_GATED); report (device) receives the build report
 cudaError_t launch_encode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev,
                           double gate = -1.0, sz_gate_report* report = nullptr);
-cudaError_t launch_decode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
+// out-of-place decode; clear_header = false keeps the status flags of earlier
+// launches on the same workspace (the groups of one host-streamed call)
+cudaError_t launch_decode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev,
+                          bool clear_header = true);
 // diagnostic: each kind of bounded wait, on something that never completes
 cudaError_t launch_wait_selftest(void* ws, cudaStream_t stream);
 // in-place slot decode (items with payload == out; ip_ws workspace)

@@ -16,10 +16,12 @@ namespace {
 
 using namespace sz;
 
-// Scratch layout is the decode workspace of one tensor of up to
-// SZ_NOALLOC_MAX_ELEMS elements: header | item flags | per-tile ranges.
+// The scratch holds the decode workspace of one tensor of up to
+// SZ_NOALLOC_MAX_ELEMS elements (its size comes from the same function that
+// sizes the workspace of sz_decode, and every call checks it before launch).
 constexpr uint64_t kMaxTiles = (SZ_NOALLOC_MAX_ELEMS + kTile - 1) / kTile;
-constexpr size_t kScratchBytes = 256 + 256 + ((kMaxTiles * 8 + 255) / 256) * 256;
+constexpr size_t kScratchBytes = size_t(dec_ws_bytes(1, kMaxTiles));
+static_assert(kScratchBytes >= 256 && kScratchBytes % 256 == 0, "scratch holds at least the status header");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -54,6 +56,8 @@ extern "C" SZ_API int sz_decode_noalloc(const uint8_t* d_payload, uint64_t paylo
       (reinterpret_cast<uintptr_t>(d_flags) & 3))
     return SZ_ERR_ALIGN;
   if (layout_of(n, 0).off_cid > payload_bytes) return SZ_ERR_CAPACITY;
+  // the decode workspace of this n must fit in the array
+  if (dec_ws_bytes(1, tiles_of(n)) > sizeof(g_noalloc_scratch)) return SZ_ERR_ARG;
   DeviceInfo dev;
   if (device_info(&dev) != cudaSuccess) return SZ_ERR_CUDA;
   void* scratch = nullptr;
@@ -71,9 +75,9 @@ extern "C" SZ_API int sz_decode_noalloc(const uint8_t* d_payload, uint64_t paylo
   items.count = 1;
   items.total_tiles = tiles_of(n);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // launch_decode zeroes the header (status flags) itself, and its prepare
-  // pass rewrites every item flag and tile range it later reads, so nothing
-  // left in the array by an earlier call is used.
+  // launch_decode zeroes the header (the status flags) itself, and the
+  // decode reads nothing else of the array, so nothing an earlier call left
+  // there is used.
   if (launch_decode(items, scratch, s, dev) != cudaSuccess) return SZ_ERR_CUDA;
   if (d_flags != nullptr &&
       cudaMemcpyAsync(d_flags, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)

@@ -208,6 +208,8 @@ SZ_API int sz_decode_many_host(const sz_item* h_items, const sz_meta* h_metas, u
   // earlier work on `stream` (e.g. the staging buffer's previous use)
   if ((e = cudaEventRecord(decoded[0], s)) != cudaSuccess) return SZ_ERR_CUDA;
   if ((e = cudaEventRecord(decoded[1], s)) != cudaSuccess) return SZ_ERR_CUDA;
+  // one status word for the whole call: cleared once, each group's decode adds its flags
+  if ((e = cudaMemsetAsync(d_ws, 0, sizeof(WsHeader), s)) != cudaSuccess) return SZ_ERR_CUDA;
   size_t r = 0;
   for (size_t gi = 0; gi < plan.groups.size(); ++gi) {
     const Group& g = plan.groups[gi];
@@ -226,7 +228,7 @@ SZ_API int sz_decode_many_host(const sz_item* h_items, const sz_meta* h_metas, u
     std::memset(&items.one, 0, sizeof(items.one));
     items.count = g.count;
     items.total_tiles = g.tiles;
-    if ((e = launch_decode(items, d_ws, s, dev)) != cudaSuccess) return SZ_ERR_CUDA;
+    if ((e = launch_decode(items, d_ws, s, dev, false)) != cudaSuccess) return SZ_ERR_CUDA;
     if ((e = cudaEventRecord(decoded[h], s)) != cudaSuccess) return SZ_ERR_CUDA;
   }
   // the copy stream has no work left that `stream` does not wait for
