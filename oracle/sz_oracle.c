@@ -13,7 +13,7 @@
 /* [P1] _align4: round a byte offset up to a multiple of 4. */
 static uint64_t align4(uint64_t v) { return (v + 3u) & ~(uint64_t)3u; }
 
-/* [P1] module docstring: "The exponent byte (bits 7..14)". */
+/* [P1] module docstring: the exponent is bits 7..14 of the pattern. */
 static uint8_t exponent_byte(uint16_t x) { return (uint8_t)((x >> 7) & 0xFFu); }
 
 /* [P1] module docstring / encode_torch: the sign bit (bit 15) goes to bit 7
@@ -22,7 +22,8 @@ static uint8_t sign_mantissa_byte(uint16_t x) {
   return (uint8_t)(((x >> 8) & 0x80u) | (x & 0x7Fu));
 }
 
-/* [P1] module docstring: x_hat = ((sm & 0x80) << 8) | (exp << 7) | (sm & 0x7F). */
+/* [P1] module docstring: the sign goes back to bit 15, the exponent to bits
+ * 7..14, the low mantissa stays in bits 0..6 (the reconstruction merge). */
 static uint16_t merge(uint8_t sm, uint8_t exp) {
   return (uint16_t)(((uint32_t)(sm & 0x80u) << 8) | ((uint32_t)exp << 7) | (uint32_t)(sm & 0x7Fu));
 }
