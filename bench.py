@@ -15,10 +15,17 @@ Reported: ``value`` = raw BF16 bytes of the workload / step time (GB/s), the
 three main kernels' raw-BF16 GB/s and HBM roofline fractions, the payload
 ratio, ``e2e`` (the same step with the input in pinned host memory, copied in,
 and the decoded tensors copied back), clocks sampled during the timed region,
-and the CPU oracle on a bounded sample of the workload (``cpu_baseline``).
+and the CPU oracle on a bounded sample of the workload (``cpu_baseline``:
+calibrate, encode and decode separately, single-threaded, with the host's core
+count).  ``configs`` holds the same step measured on the other workloads --
+the 1 Mi-element weight tensor (L2-resident), the weight matrices, the
+escape-heavy tensor, the paged KV blocks and single N(0, 1) tensors of 256 MiB
+and 4 GiB -- each with its kernel and call fractions, ratio, escapes and
+clocks (fewer steps each: ``--config-steps``).
 
 ``--impl reference`` times the CPU oracle (the reference arm of this build) on
-a bounded sample of the same workload.
+the whole workload, one step being one pass of calibrate, encode and decode
+over all its tensors.
 """
 from __future__ import annotations
 
@@ -62,6 +69,8 @@ def parse_args():
     ap.add_argument("--no-inplace", action="store_true", help="skip the in-place slot decode measurement")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU oracle sample budget")
     ap.add_argument("--e2e-groups", type=int, default=8, help="tensor groups pipelined in the e2e step")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' sub-records")
+    ap.add_argument("--config-steps", type=int, default=10, help="timed steps of each sub-record")
     return ap.parse_args()
 
 
@@ -212,52 +221,80 @@ class ClockSampler:
 
 
 def cpu_oracle_sample(arrays: list[np.ndarray], budget_s: float) -> dict:
-    """The oracle (as it stands) on the host: calibrate + encode + decode of the
-    workload's tensors in order until ``budget_s`` seconds have passed."""
+    """The oracle (as it stands) on the host: calibrate, encode and decode of the
+    workload's tensors in order, each operation timed on its own, until
+    ``budget_s`` seconds have passed.  The oracle is plain single-threaded C."""
     import oracle
 
-    done_bytes, t0, k = 0, time.perf_counter(), 0
+    done_bytes, k = 0, 0
+    t_op = {"calibrate": 0.0, "encode": 0.0, "decode": 0.0}
+    t0 = time.perf_counter()
     while True:
         x = arrays[k % len(arrays)]
+        a = time.perf_counter()
         cb = oracle.calibrate(x)
+        b = time.perf_counter()
         p, m = oracle.encode(x, cb)
+        c = time.perf_counter()
         y = oracle.decode(p, m, cb.dec_lut)
+        d = time.perf_counter()
         assert y.size == x.size
+        t_op["calibrate"] += b - a
+        t_op["encode"] += c - b
+        t_op["decode"] += d - c
         done_bytes += 2 * x.size
         k += 1
         if time.perf_counter() - t0 >= budget_s:
             break
-    dt = time.perf_counter() - t0
-    return {"value": done_bytes / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{k} tensors of the workload, {done_bytes / 2**20:.0f} MiB (calibrate+encode+decode, "
-                      f"single-threaded C), {dt:.1f} s"}
+    total = sum(t_op.values())
+    return {"value": done_bytes / total / 1e9, "unit": UNIT, "cores": 1, "threads": 1,
+            "host_cores": os.cpu_count(), "kind": "oracle",
+            "ops": {op: {"raw_gbs": done_bytes / t / 1e9, "s": t} for op, t in t_op.items()},
+            "sample": f"{k} tensors of the workload, {done_bytes / 2**20:.0f} MiB (calibrate, encode and decode "
+                      f"each timed; single-threaded C on a host of {os.cpu_count()} cores), {total:.1f} s"}
 
 
 def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle over the whole workload, one step being
+    calibrate + encode + decode of every tensor of it."""
     if rank != 0:
         return 0
-    arrays = workload_sample(args)  # the first 16M elements of the workload per step
-    for _ in range(args.warmup):
-        cpu_oracle_sample(arrays[:1], 0.0)
-    times = []
+    arrays = workload_arrays(args, 0)
     import oracle
 
+    def one_step(t_op):
+        for x in arrays:
+            a = time.perf_counter()
+            cb = oracle.calibrate(x)
+            b = time.perf_counter()
+            p, m = oracle.encode(x, cb)
+            c = time.perf_counter()
+            oracle.decode(p, m, cb.dec_lut)
+            d = time.perf_counter()
+            if t_op is not None:
+                t_op["calibrate"] += b - a
+                t_op["encode"] += c - b
+                t_op["decode"] += d - c
+
+    for _ in range(args.warmup):
+        one_step(None)
+    t_op = {"calibrate": 0.0, "encode": 0.0, "decode": 0.0}
+    times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        for x in arrays:
-            cb = oracle.calibrate(x)
-            p, m = oracle.encode(x, cb)
-            oracle.decode(p, m, cb.dec_lut)
+        one_step(t_op)
         times.append(time.perf_counter() - t0)
     step = float(np.mean(times))
     raw = sum(2 * a.size for a in arrays)
     value = raw / step / 1e9
-    sample = f"first {len(arrays)} tensor(s) of the workload, {raw / 2**20:.0f} MiB raw per step"
+    sample = f"the whole workload, {len(arrays)} tensor(s), {raw / 2**20:.0f} MiB raw per step"
+    ops = {op: {"raw_gbs": raw * args.steps / t / 1e9, "s": t} for op, t in t_op.items()}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
-            "config": {"workload": workload_name(args), "sample": sample},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "config": {"workload": workload_name(args), "same_config": True, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "threads": 1, "host_cores": os.cpu_count(),
+                             "kind": "oracle", "ops": ops, "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -302,20 +339,26 @@ def recorded_traffic(kernel: str, workload: str):
     return rec.get("bytes_per_launch_full_workload")
 
 
-def run_ours(args, world, rank, local):
+def gpu_uuid(dev, local) -> str:
+    import torch
+
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        return str(local)
+
+
+def measure(arrays: list[np.ndarray], K: int, warmup: int, dev, gpu_id: str, world: int, peak: float,
+            workload: str, barrier: bool = False) -> dict:
+    """The step (calibrate -> encode -> decode over all tensors) on `arrays`:
+    W warm-up steps, a correctness gate, K timed steps with each call's main
+    kernel bracketed by the library's timing hook, then K steps timing the
+    calls themselves.  Returns the timings, the kernel and call fractions and
+    the objects the caller's extra legs reuse."""
     import torch
 
     import weight_compression_codec_gb300 as sz
 
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl", device_id=dev)
-    sz.build()
-
-    arrays = workload_arrays(args, rank)
     n_total = sum(a.size for a in arrays)
     raw_bytes = 2 * n_total
     xs = [torch.from_numpy(a.view(np.int16)).to(dev) for a in arrays]
@@ -328,18 +371,17 @@ def run_ours(args, world, rank, local):
         sz.sz_encode_many(batch.table, workspace=ws_enc)
         sz.sz_decode_many(batch.table, workspace=ws_dec)
 
-    for _ in range(max(args.warmup, 3)):
+    for _ in range(max(warmup, 3)):
         step()
     torch.cuda.synchronize()
     # correctness gate before timing: device flags clear, round trip exact
     for w in (ws_cal, ws_enc, ws_dec):
         assert sz.sz_workspace_flags(w.buf) == 0
-    for i in (0, len(xs) // 2, len(xs) - 1):
+    for i in sorted({0, len(xs) // 2, len(xs) - 1}):
         assert torch.equal(batch.out_view(i).view(torch.int16), xs[i].view(torch.int16)), f"round trip {i}"
-    metas = [sz.meta_from_bytes(batch.metas[i].cpu().numpy()) for i in range(len(xs))]
+    metas = [sz.meta_from_bytes(m) for m in batch.metas.cpu().numpy()]
     comp_total = sum(m.comp_bytes for m in metas)
 
-    K = args.steps
     # Kernel events, set through the library's timing hook around each call's
     # streaming kernel, are the only events inside the timed steps; the calls
     # (API call to API call) are timed in a separate pass afterwards.
@@ -351,12 +393,8 @@ def run_ours(args, world, rank, local):
     step_start = torch.cuda.Event(enable_timing=True)
     step_end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    if world > 1:
+    if barrier:
         torch.distributed.barrier()
-    try:
-        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        gpu_id = str(local)
     clocks = ClockSampler(gpu_id)
     clocks.start()
     time.sleep(0.3)
@@ -373,12 +411,12 @@ def run_ours(args, world, rank, local):
     step_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    if world > 1:
+    if barrier:
         torch.distributed.barrier()
     total_ms = step_start.elapsed_time(step_end)
-    t_cal = [ev["cb"][k].elapsed_time(ev["ca"][k]) for k in range(K)]
-    t_enc = [ev["eb"][k].elapsed_time(ev["ea"][k]) for k in range(K)]
-    t_dec = [ev["db"][k].elapsed_time(ev["da"][k]) for k in range(K)]
+    t_kern = {"calibrate": [ev["cb"][k].elapsed_time(ev["ca"][k]) for k in range(K)],
+              "encode": [ev["eb"][k].elapsed_time(ev["ea"][k]) for k in range(K)],
+              "decode": [ev["db"][k].elapsed_time(ev["da"][k]) for k in range(K)]}
     # the calls, from one call's start to the next's (after the timed steps)
     for k in range(K):
         ev["o0"][k].record(stream)
@@ -394,6 +432,86 @@ def run_ours(args, world, rank, local):
     for w in (ws_cal, ws_enc, ws_dec):
         assert sz.sz_workspace_flags(w.buf) == 0
 
+    ms = {k: float(np.mean(v)) for k, v in t_kern.items()}
+    # algorithmic bytes of each streaming kernel: cal_hist reads x; enc_main
+    # reads x and writes the pk and sm sections (the escape streams are
+    # written by enc_place); dec_flat reads the payload and writes x
+    dense_bytes = sum(m.off_cid for m in metas)
+    alg = {"calibrate": raw_bytes, "encode": raw_bytes + dense_bytes, "decode": comp_total + raw_bytes}
+    alg_ops = {"calibrate": raw_bytes, "encode": raw_bytes + comp_total, "decode": comp_total + raw_bytes}
+    kname = {"calibrate": "cal_hist", "encode": "enc_main", "decode": "dec_flat"}
+    kernels = {}
+    for k in ms:
+        achieved = alg[k] / (ms[k] * 1e-3) / 1e9
+        kernels[k] = {"kernel": kname[k], "ms": ms[k], "raw_gbs": raw_bytes / (ms[k] * 1e-3) / 1e9,
+                      "achieved_gbs": achieved, "frac": achieved / peak, "frac_nominal": achieved / NOMINAL_HBM_GBS,
+                      "alg_bytes": alg[k], "traffic": recorded_traffic(kname[k], workload)}
+    ops = {k: {"ms": t_ops[k], "raw_gbs": raw_bytes / (t_ops[k] * 1e-3) / 1e9,
+               "achieved_gbs": alg_ops[k] / (t_ops[k] * 1e-3) / 1e9,
+               "frac": alg_ops[k] / (t_ops[k] * 1e-3) / 1e9 / peak,
+               "frac_nominal": alg_ops[k] / (t_ops[k] * 1e-3) / 1e9 / NOMINAL_HBM_GBS, "alg_bytes": alg_ops[k]}
+           for k in t_ops}
+    return {"xs": xs, "batch": batch, "metas": metas, "stream": stream, "raw_bytes": raw_bytes,
+            "n_total": n_total, "comp_total": comp_total, "ms_step": total_ms / K, "ms": ms, "t_ops": t_ops,
+            "kernels": kernels, "ops": ops, "clocks": clk}
+
+
+def l2_note(raw_bytes: int) -> str:
+    return (f"inputs {raw_bytes / 2**20:.0f} MiB > L2, no flush" if raw_bytes > L2_BYTES
+            else f"inputs {raw_bytes / 2**20:.0f} MiB fit in L2: L2-resident, no roofline claim")
+
+
+# The sub-records of the JSON line: the step on the other workloads.
+def _c1(rank):
+    from weight_compression_codec_gb300 import inputs
+
+    return [inputs.gaussian(1 << 20, 0.02, seed=rank)]
+
+
+SUB_CONFIGS = [
+    ("c1_weight_tensor_1Mi", "gaussian_bf16_1048576_N(0,0.02)", _c1),
+    ("weights", WORKLOADS["weights"][0], lambda rank: [WORKLOADS["weights"][2](None, rank, i) for i in range(16)]),
+    ("edge_case", WORKLOADS["edge_case"][0], lambda rank: [WORKLOADS["edge_case"][2](None, rank, 0)]),
+    ("paged_kv", WORKLOADS["paged_kv"][0], lambda rank: [WORKLOADS["paged_kv"][2](None, rank, i) for i in range(8192)]),
+    ("sweep_256MiB", WORKLOADS[f"sweep_{256 << 20}"][0], lambda rank: [WORKLOADS[f"sweep_{256 << 20}"][2](None, rank, 0)]),
+    ("sweep_4GiB", WORKLOADS[f"sweep_{4 << 30}"][0], lambda rank: [WORKLOADS[f"sweep_{4 << 30}"][2](None, rank, 0)]),
+]
+
+
+def sub_record(m: dict) -> dict:
+    """What a sub-record keeps of measure()'s result."""
+    return {"ms_per_step": m["ms_step"], "raw_gbs_step": m["raw_bytes"] / (m["ms_step"] * 1e-3) / 1e9,
+            "tensors": len(m["metas"]), "elements": m["n_total"], "raw_bytes": m["raw_bytes"],
+            "l2": l2_note(m["raw_bytes"]), "ratio": m["comp_total"] / m["raw_bytes"],
+            "n_esc": int(sum(x.n_esc for x in m["metas"])), "kernels": m["kernels"], "ops": m["ops"],
+            "clocks": m["clocks"]}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import weight_compression_codec_gb300 as sz
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    sz.build()
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"]
+    gpu_id = gpu_uuid(dev, local)
+
+    arrays = workload_arrays(args, rank)
+    K = args.steps
+    head = measure(arrays, K, args.warmup, dev, gpu_id, world, peak, args.workload, barrier=world > 1)
+    xs, batch, metas, stream = head["xs"], head["batch"], head["metas"], head["stream"]
+    raw_bytes, n_total, comp_total = head["raw_bytes"], head["n_total"], head["comp_total"]
+    total_ms = head["ms_step"] * K
+    t_ops = head["t_ops"]
+    m_kernels, m_ops, m_ms, clk = head["kernels"], head["ops"], head["ms"], head["clocks"]
+    n_esc_total = int(sum(x.n_esc for x in metas))
     ms_step = max_over_ranks(total_ms / K, world, dev)
 
     # e2e: the same step through the public API with host-resident input and output
@@ -581,33 +699,28 @@ def run_ours(args, world, rank, local):
                    "path": "stash copy of the bytes the last-tile-first decode overwrites early, then decode"}
         del slot_buf, slots, flush
 
+    # the other workloads' sub-records (each measured on its own, then freed)
+    configs = None
+    if not args.no_configs:
+        del xs, batch
+        head.clear()
+        torch.cuda.empty_cache()
+        configs = {}
+        kc = max(1, min(args.config_steps, K))
+        for key, name, gen in SUB_CONFIGS:
+            t0 = time.time()
+            mc = measure(gen(rank), kc, 3, dev, gpu_id, world, peak, key, barrier=world > 1)
+            configs[key] = dict(sub_record(mc), workload=name, steps=kc, warmup=3,
+                                wall_s=round(time.time() - t0, 1))
+            mc.clear()
+            torch.cuda.empty_cache()
+
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return 0
 
-    peaks = measured_peaks()
-    peak = peaks["hbm_gbs"]
-    ms = {"calibrate": float(np.mean(t_cal)), "encode": float(np.mean(t_enc)), "decode": float(np.mean(t_dec))}
-    # algorithmic bytes of each streaming kernel: cal_hist reads x; enc_main
-    # reads x and writes the pk and sm sections (the escape streams are
-    # written by enc_place); dec_flat reads the payload and writes x
-    dense_bytes = sum(m.off_cid for m in metas)
-    alg = {"calibrate": raw_bytes, "encode": raw_bytes + dense_bytes, "decode": comp_total + raw_bytes}
-    alg_ops = {"calibrate": raw_bytes, "encode": raw_bytes + comp_total, "decode": comp_total + raw_bytes}
-    kname = {"calibrate": "cal_hist", "encode": "enc_main", "decode": "dec_flat"}
-    kernels = {}
-    for k in ms:
-        achieved = alg[k] / (ms[k] * 1e-3) / 1e9
-        kernels[k] = {"kernel": kname[k], "ms": ms[k], "raw_gbs": raw_bytes / (ms[k] * 1e-3) / 1e9,
-                      "achieved_gbs": achieved, "frac": achieved / peak, "frac_nominal": achieved / NOMINAL_HBM_GBS,
-                      "alg_bytes": alg[k],
-                      "traffic": recorded_traffic(kname[k], args.workload)}
-    ops = {k: {"ms": t_ops[k], "raw_gbs": raw_bytes / (t_ops[k] * 1e-3) / 1e9,
-               "achieved_gbs": alg_ops[k] / (t_ops[k] * 1e-3) / 1e9,
-               "frac": alg_ops[k] / (t_ops[k] * 1e-3) / 1e9 / peak,
-               "frac_nominal": alg_ops[k] / (t_ops[k] * 1e-3) / 1e9 / NOMINAL_HBM_GBS, "alg_bytes": alg_ops[k]}
-           for k in t_ops}
+    kernels, ops, ms = m_kernels, m_ops, m_ms
     dom = max(ms, key=ms.get)
     value = world * raw_bytes / (ms_step * 1e-3) / 1e9
     cpu = None
@@ -618,12 +731,10 @@ def run_ours(args, world, rank, local):
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u16", "data": "synthetic",
         "config": {"workload": workload_name(args), "tensors": len(arrays), "elements": n_total, "raw_bytes": raw_bytes,
-                   "step": "calibrate+encode+decode",
-                   "l2": f"inputs {raw_bytes / 2**20:.0f} MiB > L2, no flush" if raw_bytes > L2_BYTES
-                   else f"inputs {raw_bytes / 2**20:.0f} MiB fit in L2: L2-resident, no roofline claim",
+                   "step": "calibrate+encode+decode", "l2": l2_note(raw_bytes),
                    "parallelism": f"{world} independent shards" if world > 1 else "single GPU"},
         "ratio": comp_total / raw_bytes, "compression": raw_bytes / comp_total,
-        "n_esc": int(sum(m.n_esc for m in metas)),
+        "n_esc": n_esc_total,
         "encode_gbs": ops["encode"]["raw_gbs"], "decode_gbs": ops["decode"]["raw_gbs"],
         "calibrate_gbs": ops["calibrate"]["raw_gbs"],
         "roofline": {"bound": "hbm", "kernel": kernels[dom]["kernel"], "achieved": kernels[dom]["achieved_gbs"],
@@ -633,13 +744,14 @@ def run_ours(args, world, rank, local):
         "kernels": kernels,
         "ops": ops,
         "clocks": clk,
-        "gpu_launches": 7 * K,
+        "gpu_launches": 6 * K,
         "e2e": e2e,
         "decode_from_host": from_host,
         "decode_inplace": inplace if inplace is None else dict(
             inplace, frac=inplace["achieved_gbs"] / peak, kernel_frac=inplace["kernel_achieved_gbs"] / peak,
             vs_decode_call=t_ops["decode"] / inplace["call_ms"]),
         "cpu_baseline": cpu,
+        "configs": configs,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

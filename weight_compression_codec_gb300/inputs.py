@@ -26,13 +26,38 @@ activations and model weights), which are not available here:
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 BASE_SEED = 1000
+BLOCK = 1 << 24  # elements per independently seeded block of the large generators
 
 
 def _rng(*key: int) -> np.random.Generator:
     return np.random.default_rng(np.random.SeedSequence([BASE_SEED, *key]))
+
+
+def _blocks(n: int, key: tuple, fill) -> np.ndarray:
+    """n BF16 patterns made block by block: block b (elements [b BLOCK, (b + 1)
+    BLOCK)) is ``fill(rng, count)`` with its own generator seeded by key + (b,),
+    so the values do not depend on how many threads make them."""
+    out = np.empty(n, dtype=np.uint16)
+    nb = (n + BLOCK - 1) // BLOCK
+
+    def work(b: int) -> None:
+        lo = b * BLOCK
+        hi = min(n, lo + BLOCK)
+        out[lo:hi] = fill(_rng(*key, b), hi - lo)
+
+    if nb <= 1:
+        for b in range(nb):
+            work(b)
+    else:
+        with ThreadPoolExecutor(max_workers=min(nb, os.cpu_count() or 1, 16)) as ex:
+            list(ex.map(work, range(nb)))
+    return out
 
 
 def f32_to_bf16_bits(v: np.ndarray) -> np.ndarray:
@@ -56,8 +81,8 @@ def all_bit_patterns() -> np.ndarray:
 
 
 def gaussian(n: int, sigma: float = 0.02, seed: int = 0) -> np.ndarray:
-    r = _rng(1, seed)
-    return f32_to_bf16_bits(r.standard_normal(n, dtype=np.float32) * np.float32(sigma))
+    return _blocks(n, (1, seed),
+                   lambda r, k: f32_to_bf16_bits(r.standard_normal(k, dtype=np.float32) * np.float32(sigma)))
 
 
 def kv_cache_shape(layers=32, tokens=4096, kv_heads=8, head_dim=128):
@@ -81,19 +106,21 @@ def kv_cache(layers=32, tokens=4096, kv_heads=8, head_dim=128) -> list[np.ndarra
 
 def weight_tensor(index: int, pairs=8, d_model=4096, d_ff=14336) -> np.ndarray:
     """Tensor ``index`` of ``pairs`` (d_model x d_ff, d_ff x d_model) matrices."""
-    r = _rng(3, index)
-    n = d_model * d_ff
-    v = r.standard_normal(n, dtype=np.float32) * np.float32(0.02)
-    big = r.random(n) < 0.001
-    v[big] = r.standard_normal(int(big.sum()), dtype=np.float32)
-    if index == 2 * pairs - 1:
-        broad = r.random(n) < 0.03
-        k = int(broad.sum())
-        u = r.integers(-60, 21, size=k)
-        m = r.uniform(1.0, 2.0, size=k)
-        s = np.where(r.random(k) < 0.5, -1.0, 1.0)
-        v[broad] = (s * m * np.exp2(u.astype(np.float64))).astype(np.float32)
-    return f32_to_bf16_bits(v)
+
+    def fill(r: np.random.Generator, n: int) -> np.ndarray:
+        v = r.standard_normal(n, dtype=np.float32) * np.float32(0.02)
+        big = r.random(n) < 0.001
+        v[big] = r.standard_normal(int(big.sum()), dtype=np.float32)
+        if index == 2 * pairs - 1:
+            broad = r.random(n) < 0.03
+            k = int(broad.sum())
+            u = r.integers(-60, 21, size=k)
+            m = r.uniform(1.0, 2.0, size=k)
+            s = np.where(r.random(k) < 0.5, -1.0, 1.0)
+            v[broad] = (s * m * np.exp2(u.astype(np.float64))).astype(np.float32)
+        return f32_to_bf16_bits(v)
+
+    return _blocks(d_model * d_ff, (3, index), fill)
 
 
 def weight_shapes(pairs=8, d_model=4096, d_ff=14336):
@@ -106,7 +133,10 @@ def weight_pairs(pairs=8, d_model=4096, d_ff=14336) -> list[np.ndarray]:
 
 def edge_case(n: int = 100_000_003, seed: int = 0) -> np.ndarray:
     """Escape-heavy tensor with special values mixed in (see module docstring)."""
-    r = _rng(4, seed)
+    return _blocks(n, (4, seed), _edge_block)
+
+
+def _edge_block(r: np.random.Generator, n: int) -> np.ndarray:
     u = r.integers(-140, 41, size=n)
     m = r.uniform(1.0, 2.0, size=n)
     s = np.where(r.random(n) < 0.5, -1.0, 1.0)
@@ -156,5 +186,4 @@ def sweep_sizes(lo_bytes=1 << 20, hi_bytes=4 << 30) -> list[int]:
 
 
 def sweep_tensor(n: int) -> np.ndarray:
-    r = _rng(6, n)
-    return f32_to_bf16_bits(r.standard_normal(n, dtype=np.float32))
+    return _blocks(n, (6, n), lambda r, k: f32_to_bf16_bits(r.standard_normal(k, dtype=np.float32)))
