@@ -744,7 +744,7 @@ def run_ours(args, world, rank, local):
         "kernels": kernels,
         "ops": ops,
         "clocks": clk,
-        "gpu_launches": 6 * K,
+        "gpu_launches": 7 * K,
         "e2e": e2e,
         "decode_from_host": from_host,
         "decode_inplace": inplace if inplace is None else dict(

@@ -66,6 +66,7 @@ struct CalShared {
 };
 
 __global__ void cal_prepare(const __grid_constant__ Items items, CalWs ws) {
+  pdl_trigger();
   const uint64_t nthreads = uint64_t(gridDim.x) * blockDim.x;
   const uint64_t gtid = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   for (uint64_t w = gtid; w < uint64_t(items.count) * 256; w += nthreads) ws.hist[w] = 0;
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __g
   if (t0 >= t1) return;
   // An inconsistent item table (flagged by cal_prepare) is never walked: every
   // warp reads the flags, the producer after its first (bounds-safe) search.
+  pdl_wait();  // cal_prepare's writes
   const uint32_t hdr_flags = ws.hdr->flags;
 
   for (uint32_t w = tid; w < 256 * 32; w += kCalThreads) sh.cnt[w] = 0;
@@ -334,8 +336,7 @@ cudaError_t launch_calibrate(const Items& items, void* ws_base, cudaStream_t str
   const uint64_t cap = uint64_t(dev.num_sms) * kCalCtasPerSm;
   const unsigned grid = unsigned(items.total_tiles < cap ? items.total_tiles : cap);
   if (g_timing.before) cudaEventRecord(g_timing.before, stream);
-  cal_hist<<<grid, kCalThreads, smem, stream>>>(items, ws);
-  err = cudaGetLastError();
+  err = launch_pdl(cal_hist, dim3(grid), dim3(kCalThreads), smem, stream, items, ws);
   if (g_timing.after) cudaEventRecord(g_timing.after, stream);
   return err;
 }

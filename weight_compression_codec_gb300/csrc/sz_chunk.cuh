@@ -9,6 +9,13 @@
 
 namespace sz {
 
+// A chunk with more escapes than this is not staged: staging costs 4 bytes
+// written and read per escape, more than reading the chunk's 2 KiB of input
+// again, so the placement pass regenerates such a chunk's escapes from the
+// input instead (enc_place).  Chunks of partial tiles may still be staged;
+// the placement pass ignores the staging of every chunk above the limit.
+constexpr uint32_t kStageMax = 256;
+
 // Bounded mbarrier wait agreed by the whole warp.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xFFFFFFFFu, mbar_wait(bar, parity));
@@ -169,6 +176,8 @@ __device__ __forceinline__ uint32_t encode_chunk8(const Stage& st, uint32_t warp
   }
   // Escapes of the chunk, in element order (row, lane, k): one pass per chunk.
   if (__ballot_sync(0xFFFFFFFFu, lane_esc != 0) == 0) return 0;
+  const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, uint32_t(__popc(lane_esc)));
+  if (total > kStageMax) return total;  // regenerated from the input by the placement pass
   const uint32_t lane_lt = (1u << lane) - 1u;
   const uint16_t* xc = st.x + warp * kChunk;
   uint32_t multi = 0;  // non-zero if this lane has two or more escapes in a row

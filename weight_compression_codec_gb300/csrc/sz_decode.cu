@@ -361,6 +361,7 @@ __device__ void note_tile_count(const Items& items, const DecWs& ws, const sz_it
 // validating the item for itself).
 __global__ void __launch_bounds__(kPrepWarps * 32) dec_prepare(const __grid_constant__ Items items, DecWs ws,
                                                                 bool inplace) {
+  pdl_trigger();
   __shared__ uint32_t counts[kPrepWarps][32];
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t warp = threadIdx.x >> 5;
@@ -764,6 +765,7 @@ constexpr uint64_t kStashTiles = 2;  // consecutive tiles per warp (2: 202 us, 4
 // in the same tensor.  (dec_prepare has cleared the read_done words and
 // copied the escape streams.)
 __global__ void __launch_bounds__(kStashWarps * 32, 4) dip_stash(const __grid_constant__ Items items, DecWs ws) {
+  pdl_wait();  // dec_prepare's writes
   if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
   const uint32_t lane = threadIdx.x & 31u;
   const uint64_t T = items.total_tiles;
@@ -1641,8 +1643,8 @@ cudaError_t launch_decode_inplace(const Items& items, void* ws_base, cudaStream_
   if (items.total_tiles == 0) return cudaSuccess;
   const uint64_t blocks = (items.total_tiles + kStashWarps * kStashTiles - 1) / (kStashWarps * kStashTiles);
   const uint64_t cap = uint64_t(dev.num_sms) * 32;  // four waves of 8 blocks per SM, then grid-stride
-  dip_stash<<<unsigned(blocks < cap ? blocks : cap), kStashWarps * 32, 0, stream>>>(items, ws);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  err = launch_pdl(dip_stash, dim3(unsigned(blocks < cap ? blocks : cap)), dim3(kStashWarps * 32), 0, stream, items, ws);
+  if (err != cudaSuccess) return err;
   static thread_local int configured_device = -1, per_sm = kIpCtasPerSm;
   const size_t smem = sizeof(IpShared);
   err = configure(reinterpret_cast<const void*>(dec_inplace), smem, kIpThreads, dev.device, &configured_device,

@@ -89,7 +89,8 @@ struct WsHeader {
   uint32_t pad0;
   unsigned long long ticket;  // dynamic tile counter (encode)
   uint32_t tiles_differ;      // in-place decode: set when the tensors' tile counts are not all equal
-  uint32_t reserved[59];
+  uint32_t dense;             // encode: some chunk had too many escapes to stage (kStageMax)
+  uint32_t reserved[58];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
@@ -540,6 +541,16 @@ __device__ __forceinline__ bool named_bar_red_or(uint32_t id, uint32_t threads, 
 }
 
 __device__ __forceinline__ void set_flag(WsHeader* h, uint32_t bits) { atomicOr(&h->flags, bits); }
+
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start
+// while the kernel before it in the stream is still running: pdl_wait blocks
+// until that kernel has completed and its writes are visible (a no-op when
+// the kernel was launched normally), so it comes before any read of what the
+// earlier kernel wrote.  pdl_trigger lets the next kernel's CTAs be scheduled
+// once every CTA of this one has issued it; it orders nothing, since the next
+// kernel waits for this one's completion all the same.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 #endif  // __CUDACC__
 

@@ -85,6 +85,7 @@ struct EncShared {
 };
 
 __global__ void enc_prepare(const __grid_constant__ Items items, EncWs ws) {
+  pdl_trigger();
   const uint64_t nthreads = uint64_t(gridDim.x) * blockDim.x;
   const uint64_t gtid = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   for (uint64_t t = gtid; t < items.total_tiles; t += nthreads) ws.status[t] = 0ull;
@@ -130,6 +131,8 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  pdl_trigger();
+  pdl_wait();  // enc_prepare's writes
   // an inconsistent item table (flagged by enc_prepare) is never walked
   if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
 
@@ -227,6 +230,7 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
   // total only when the tensor changes: one global atomic per chunk would pile
   // hundreds of thousands of updates onto a few words (one L2 slice).
   uint32_t acc_item = 0xFFFFFFFFu, acc = 0;
+  bool dense = false;  // this warp staged no escapes of some chunk (enc_regen will write them)
   for (uint32_t it = 0;; ++it) {
     const int s = int(it % kEncStages);
     if (!warp_wait(&sh.full[s], (it / kEncStages) & 1)) {
@@ -248,12 +252,14 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
         acc = 0;
       }
       acc += run;
+      dense |= run > kStageMax;
       if (lane == 0) ws.chunk_cnt[chunk] = uint16_t(run);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty[s]);
   }
   if (lane == 0 && acc) atomicAdd(ws.item_esc + acc_item, acc);
+  if (lane == 0 && dense) atomicOr(&ws.hdr->dense, 1u);
 }
 
 // Decoupled lookback over the placement segments of one tensor: lane l reads
@@ -405,7 +411,11 @@ __device__ void place_small(const Items& items, const EncWs& ws, uint32_t i, uin
   uint8_t* const ev_p = it.payload + l.off_ev;
   for (uint32_t c = 0; c < chunks; ++c) {
     const uint32_t o = off[c], cnt = off[c + 1] - o;
-    if (cnt) scatter_chunk(ws, cid_p, lpos_p, ev_p, (chunk_base + c) * kChunk, c, o, cnt, e, lane, 32);
+    if (cnt > kStageMax) {
+      if (lane == 0) ws.stage[(chunk_base + c) * kChunk] = o;  // for enc_regen
+    } else if (cnt) {
+      scatter_chunk(ws, cid_p, lpos_p, ev_p, (chunk_base + c) * kChunk, c, o, cnt, e, lane, 32);
+    }
   }
   __syncwarp();  // off is reused by this warp's next item
 }
@@ -416,11 +426,14 @@ __device__ void place_small(const Items& items, const EncWs& ws, uint32_t i, uin
 // of 256 chunks claimed by ticket (so they start in order), a block scan of
 // the chunk counts and a decoupled lookback across the item's segments.
 __global__ void __launch_bounds__(kPlaceThreads, kPlaceBlocksPerSm) enc_place(const __grid_constant__ Items items, EncWs ws) {
-  __shared__ uint32_t off[kSegChunks + 1];  // exclusive offsets of the segment's chunks, then the total
+  __shared__ uint32_t off[kSegChunks + 1];   // exclusive offsets of the segment's chunks, then the total
+  __shared__ uint32_t offs[kSegChunks + 1];  // the same over the staged chunks (count <= kStageMax)
   __shared__ uint32_t woff[kPlaceWarps][kSegChunks + 1];
-  __shared__ uint32_t wsum[kPlaceThreads / 32];
+  __shared__ uint64_t wsum[kPlaceThreads / 32];
   __shared__ uint32_t s_seg, s_base;
   const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
+  pdl_trigger();
+  pdl_wait();  // the encode pass's counts and staging
   if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
   const uint32_t groups = (items.count + kPlaceWarps - 1) / kPlaceWarps;
   for (uint32_t grp = blockIdx.y; grp < groups; grp += gridDim.y) {
@@ -458,23 +471,30 @@ __global__ void __launch_bounds__(kPlaceThreads, kPlaceBlocksPerSm) enc_place(co
         __syncthreads();
         const uint64_t seg = s_seg;
         if (seg >= segs) break;
-        // block exclusive scan of the segment's chunk counts
+        // block exclusive scan of the segment's chunk counts, and of those
+        // of its staged chunks (both in one 64-bit word: staged << 32 | all)
         const uint64_t c = seg * kSegChunks + tid;
         const uint32_t cnt = (c < chunks) ? ws.chunk_cnt[chunk_base + c] : 0u;
-        uint32_t incl = cnt;
+        const uint64_t pair = (uint64_t(cnt <= kStageMax ? cnt : 0u) << 32) | cnt;
+        uint64_t incl = pair;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
-          const uint32_t o = __shfl_up_sync(FULL, incl, d);
+          const uint64_t o = __shfl_up_sync(FULL, incl, d);
           if (lane >= uint32_t(d)) incl += o;
         }
         if (lane == 31) wsum[warp] = incl;
         __syncthreads();
-        uint32_t wbase = 0;
+        uint64_t wbase = 0;
         for (uint32_t w = 0; w < warp; ++w) wbase += wsum[w];
-        off[tid] = wbase + incl - cnt;
-        if (tid == kPlaceThreads - 1) off[kSegChunks] = wbase + incl;
+        off[tid] = uint32_t(wbase + incl - pair);
+        offs[tid] = uint32_t((wbase + incl - pair) >> 32);
+        if (tid == kPlaceThreads - 1) {
+          off[kSegChunks] = uint32_t(wbase + incl);
+          offs[kSegChunks] = uint32_t((wbase + incl) >> 32);
+        }
         __syncthreads();
         const uint32_t agg = off[kSegChunks];
+        const uint32_t agg_staged = offs[kSegChunks];
         if (warp == 0) {
           unsigned long long* st = ws.status + it.tile_begin + seg * kSegTiles;
           uint32_t base = 0;
@@ -493,23 +513,26 @@ __global__ void __launch_bounds__(kPlaceThreads, kPlaceBlocksPerSm) enc_place(co
         }
         __syncthreads();
         const uint32_t base = s_base;
-        // scatter: escape j of the segment -> global index base + j.  Each
+        // scatter of the staged chunks: staged escape j of the segment (in
+        // chunk lo) -> global index base + off[lo] + (j - offs[lo]).  Each
         // thread takes kScatterUnroll escapes per round and issues all their
         // staging loads before any store, so a round costs one memory latency.
-        for (uint32_t j0 = 0; j0 < agg; j0 += kScatterUnroll * kPlaceThreads) {
+        for (uint32_t j0 = 0; j0 < agg_staged; j0 += kScatterUnroll * kPlaceThreads) {
           uint32_t q[kScatterUnroll], jj[kScatterUnroll], sv[kScatterUnroll];
 #pragma unroll
           for (uint32_t u = 0; u < kScatterUnroll; ++u) {
             const uint32_t j = j0 + u * kPlaceThreads + tid;
-            jj[u] = j;
-            uint32_t lo = 0;  // last chunk lo with off[lo] <= j (off[kSegChunks] = agg > j)
+            uint32_t lo = 0;  // last chunk lo with offs[lo] <= j (offs[kSegChunks] = agg_staged > j)
 #pragma unroll
             for (uint32_t b = kSegChunks / 2; b >= 1; b >>= 1)
-              if (off[lo + b] <= j) lo += b;
+              if (offs[lo + b] <= j) lo += b;
             q[u] = lo;
-            if (j < agg) {
-              const uint64_t slot = (chunk_base + seg * kSegChunks + lo) * kChunk + (j - off[lo]);
+            jj[u] = off[lo] + (j - offs[lo]);  // the escape's index in the segment
+            if (j < agg_staged) {
+              const uint64_t slot = (chunk_base + seg * kSegChunks + lo) * kChunk + (j - offs[lo]);
               sv[u] = ws.stage[slot];
+            } else {
+              jj[u] = agg;
             }
           }
 #pragma unroll
@@ -522,8 +545,217 @@ __global__ void __launch_bounds__(kPlaceThreads, kPlaceBlocksPerSm) enc_place(co
             }
           }
         }
+        // chunks too dense to stage: their escapes' first global index, in
+        // their (unused) staging slot, for enc_regen
+        if (c < chunks && cnt > kStageMax) ws.stage[(chunk_base + c) * kChunk] = base + off[tid];
       }
     }
+  }
+}
+
+constexpr int kRegenWarps = 8;
+
+// The chunk a regeneration warp works on: where its escapes go.
+struct RegenChunk {
+  const uint8_t* lut;                 // the tensor's enc_lut
+  uint8_t *cid_p, *lpos_p, *ev_p;     // the tensor's escape streams
+  const uint16_t* xc;                 // the chunk's input
+  uint32_t c, nvalid, e, bulk, first; // tensor-local chunk, elements, escapes of the tensor,
+                                      // bytes copied to shared memory, its first escape's index
+  uint32_t cnt;                       // the chunk's escapes
+};
+
+// The escapes of every chunk too dense to stage (count > kStageMax),
+// regenerated from the input after enc_place has given each such chunk the
+// global index of its first escape (in the first word of its staging slot).
+// Warps take the chunks of the whole table grid-stride, so the work spreads
+// over every SM however few segments hold it.  Each warp double-buffers its
+// chunks in shared memory: one lane issues the TMA bulk copy of the next
+// chunk's 2 KiB before the warp processes the current one.  Per chunk: rows
+// of 32 elements (lane l holds element 32 r + l), an escape being an element
+// whose enc_lut code has bit 4 set (as in the chunk encoder), compacted in
+// element order by one ballot per row, so a row's escapes are written next to
+// each other.  Items with a flag (failed, gated, over capacity) are skipped,
+// as enc_place skips them.  Returns at once when enc_main found no dense
+// chunk.
+__global__ void __launch_bounds__(kRegenWarps * 32) enc_regen(const __grid_constant__ Items items, EncWs ws) {
+  __shared__ __align__(128) uint16_t buf[kRegenWarps][2][kChunk];
+  __shared__ __align__(16) uint8_t lut_sh[kRegenWarps][256];  // the current chunk's enc_lut
+  __shared__ __align__(16) uint16_t lp_sh[kRegenWarps][kChunk + 8];  // a whole chunk's local_pos ...
+  __shared__ __align__(16) uint8_t ev_sh[kRegenWarps][kChunk + 16];  // ... and esc_val, then copied out
+  __shared__ uint64_t bar[kRegenWarps][2];
+  pdl_wait();  // enc_place's offsets
+  if (ws.hdr->dense == 0 || (ws.hdr->flags & SZ_FLAG_ITEMS)) return;
+  const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+  const uint32_t lane_lt = (1u << lane) - 1u;
+  const uint64_t total = items.total_tiles * kChunksPerTile;
+  const uint64_t stride = uint64_t(gridDim.x) * kRegenWarps;
+  if (lane == 0) {
+    mbar_init(&bar[warp][0], 1);
+    mbar_init(&bar[warp][1], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  // the item of the last chunk looked up: global chunks [cb0, cb1)
+  uint64_t cb0 = 1, cb1 = 0, item_n = 0;
+  RegenChunk item{};
+  bool item_ok = false;
+  // next dense chunk of this warp at or after g, with its item; total if none
+  auto next = [&](uint64_t g, RegenChunk& rc) -> uint64_t {
+    for (; g < total; g += stride) {
+      if (ws.chunk_cnt[g] <= kStageMax) continue;
+      if (g < cb0 || g >= cb1) {
+        const uint64_t tile = g / kChunksPerTile;
+        uint32_t idx = ws.tile_item ? ws.tile_item[tile] : find_item(items, tile);
+        if (idx >= items.count) idx = 0;
+        const sz_item& it = item_at(items, idx);
+        const uint32_t flags = ws.item_flags[idx];
+        const uint64_t n = (flags & SZ_FLAG_SIZE) ? 0 : it.n;
+        const uint32_t e = ws.item_esc[idx];
+        const Layout l = layout_of(n, e);
+        cb0 = it.tile_begin * kChunksPerTile;
+        cb1 = cb0 + (n + kChunk - 1) / kChunk;
+        item_ok = flags == 0 && l.comp_bytes <= it.capacity;
+        item.lut = item_ok ? it.codebook->enc_lut : nullptr;
+        item.cid_p = it.payload + l.off_cid;
+        item.lpos_p = it.payload + l.off_lpos;
+        item.ev_p = it.payload + l.off_ev;
+        item.xc = it.x;
+        item.e = e;
+        item_n = n;
+      }
+      if (!item_ok || g < cb0 || g >= cb1) {
+        cb0 = 1;
+        cb1 = 0;
+        continue;
+      }
+      rc = item;
+      rc.c = uint32_t(g - cb0);
+      const uint64_t first = uint64_t(rc.c) * kChunk;
+      rc.nvalid = (item_n - first < kChunk) ? uint32_t(item_n - first) : kChunk;
+      rc.xc = item.xc + first;
+      rc.bulk = (2u * rc.nvalid) & ~15u;
+      rc.first = ws.stage[g * kChunk];
+      rc.cnt = ws.chunk_cnt[g];
+      return g;
+    }
+    return total;
+  };
+  RegenChunk cur{}, nxt{};
+  const uint8_t* lut_src = nullptr;  // the enc_lut now in lut_sh[warp]
+  uint64_t g = next(uint64_t(blockIdx.x) * kRegenWarps + warp, cur);
+  auto issue = [&](const RegenChunk& rc, int b) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar[warp][b], rc.bulk);
+      if (rc.bulk) bulk_g2s(buf[warp][b], rc.xc, rc.bulk, &bar[warp][b]);
+    }
+  };
+  if (g < total) issue(cur, 0);
+  uint32_t phases = 0;  // bit b: parity of buffer b's next phase
+  for (int b = 0; g < total; b ^= 1) {
+    const uint64_t gn = next(g + stride, nxt);
+    if (gn < total) issue(nxt, b ^ 1);
+    if (!__all_sync(FULL, mbar_wait(&bar[warp][b], (phases >> b) & 1u))) {
+      if (lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+      if (gn < total) (void)__all_sync(FULL, mbar_wait(&bar[warp][b ^ 1], (phases >> (b ^ 1)) & 1u));  // in flight
+      return;
+    }
+    phases ^= 1u << b;
+    if (cur.lut != lut_src) {  // the tensor changed: its enc_lut into shared memory
+      __syncwarp();
+      reinterpret_cast<uint2*>(lut_sh[warp])[lane] = __ldg(reinterpret_cast<const uint2*>(cur.lut) + lane);
+      lut_src = cur.lut;
+      __syncwarp();
+    }
+    const uint8_t* lut = lut_sh[warp];
+    const uint16_t* xs = buf[warp][b];
+    // the chunk's escape streams from its first escape; `room`: escapes before the tensor's end
+    uint32_t* const cid_c = reinterpret_cast<uint32_t*>(cur.cid_p) + cur.first;
+    uint16_t* const lp_c = reinterpret_cast<uint16_t*>(cur.lpos_p) + cur.first;
+    uint8_t* const ev_c = cur.ev_p + cur.first;
+    const uint32_t room = cur.e > cur.first ? cur.e - cur.first : 0u;
+    uint32_t run = 0;
+    if (cur.bulk == 2u * kChunk) {
+      // A whole chunk in shared memory.  Its escapes' chunk_id entries are
+      // all c: written as a run (16-byte stores for its aligned body).
+      const uint32_t m = cur.cnt < room ? cur.cnt : room;
+      const uint32_t head = uint32_t((16u - (reinterpret_cast<uintptr_t>(cid_c) & 15u)) & 15u) / 4u;
+      const uint32_t h = head < m ? head : m;
+      if (lane < h) cid_c[lane] = cur.c;
+      const uint32_t body4 = (m - h) / 4u;
+      uint4* const cid4 = reinterpret_cast<uint4*>(cid_c + h);
+      for (uint32_t k = lane; k < body4; k += 32) cid4[k] = make_uint4(cur.c, cur.c, cur.c, cur.c);
+      for (uint32_t k = h + 4u * body4 + lane; k < m; k += 32) cid_c[k] = cur.c;
+      // local_pos and esc_val: lane l takes elements 4 l .. 4 l + 3 of each
+      // row of 128; four ballots give every lane the escapes before its
+      // own.  They are collected in shared memory, at the same offset mod 16
+      // as their destination, then copied out with 16-byte stores.
+      const uint32_t lp_sh0 = uint32_t(reinterpret_cast<uintptr_t>(lp_c) & 15u) / 2u;  // elements
+      const uint32_t ev_sh0 = uint32_t(reinterpret_cast<uintptr_t>(ev_c) & 15u);
+      uint16_t* const lps = lp_sh[warp] + lp_sh0;
+      uint8_t* const evs = ev_sh[warp] + ev_sh0;
+      const uint2* const xs2 = reinterpret_cast<const uint2*>(xs);
+#pragma unroll 2
+      for (uint32_t r = 0; r < kChunk / 128; ++r) {
+        const uint2 w = xs2[r * 32u + lane];
+        const uint32_t e0 = (w.x >> 7) & 0xFFu, e1 = (w.x >> 23) & 0xFFu;
+        const uint32_t e2 = (w.y >> 7) & 0xFFu, e3 = (w.y >> 23) & 0xFFu;
+        const uint32_t f = ((lut[e0] >> 4) & 1u) | ((lut[e1] >> 3) & 2u) | ((lut[e2] >> 2) & 4u) | ((lut[e3] >> 1) & 8u);
+        const uint32_t c4 = __popc(f);
+        const uint32_t b1 = __ballot_sync(FULL, c4 >= 1u), b2 = __ballot_sync(FULL, c4 >= 2u);
+        const uint32_t b3 = __ballot_sync(FULL, c4 >= 3u), b4 = __ballot_sync(FULL, c4 == 4u);
+        uint32_t q = run + __popc(b1 & lane_lt) + __popc(b2 & lane_lt) + __popc(b3 & lane_lt) + __popc(b4 & lane_lt);
+        const uint32_t p0 = r * 128u + 4u * lane;
+        const uint32_t ex4 = e0 | (e1 << 8) | (e2 << 16) | (e3 << 24);
+#pragma unroll
+        for (uint32_t k = 0; k < 4; ++k) {
+          if ((f >> k) & 1u) {
+            lps[q] = uint16_t(p0 + k);
+            evs[q] = uint8_t(ex4 >> (8 * k));
+            ++q;
+          }
+        }
+        run += __popc(b1) + __popc(b2) + __popc(b3) + __popc(b4);
+      }
+      __syncwarp();
+      // copy out: [0, m) at lp_c / ev_c, whole 16-byte words where both sides allow
+      {
+        const uint32_t lh = (lp_sh0 ? 8u - lp_sh0 : 0u) < m ? (lp_sh0 ? 8u - lp_sh0 : 0u) : m;
+        if (lane < lh) lp_c[lane] = lps[lane];
+        const uint32_t lb = (m - lh) / 8u;
+        const uint4* const ls4 = reinterpret_cast<const uint4*>(lps + lh);
+        uint4* const ld4 = reinterpret_cast<uint4*>(lp_c + lh);
+        for (uint32_t k = lane; k < lb; k += 32) ld4[k] = ls4[k];
+        for (uint32_t k = lh + 8u * lb + lane; k < m; k += 32) lp_c[k] = lps[k];
+        const uint32_t eh = (ev_sh0 ? 16u - ev_sh0 : 0u) < m ? (ev_sh0 ? 16u - ev_sh0 : 0u) : m;
+        if (lane < eh) ev_c[lane] = evs[lane];
+        const uint32_t eb = (m - eh) / 16u;
+        const uint4* const es4 = reinterpret_cast<const uint4*>(evs + eh);
+        uint4* const ed4 = reinterpret_cast<uint4*>(ev_c + eh);
+        for (uint32_t k = lane; k < eb; k += 32) ed4[k] = es4[k];
+        for (uint32_t k = eh + 16u * eb + lane; k < m; k += 32) ev_c[k] = evs[k];
+      }
+    } else {
+      // a tensor's last chunk: elements past the copied body (under 8) are read directly
+      for (uint32_t r = 0; r < kChunk / 32; ++r) {
+        const uint32_t p = r * 32u + lane;
+        const uint32_t v = 2u * p + 2u <= cur.bulk ? uint32_t(xs[p])
+                                                   : (p < cur.nvalid ? uint32_t(__ldg(cur.xc + p)) : 0u);
+        const uint32_t ex = (v >> 7) & 0xFFu;
+        const bool esc = p < cur.nvalid && ((lut[ex] >> 4) & 1u);
+        const uint32_t bal = __ballot_sync(FULL, esc);
+        const uint32_t q = run + __popc(bal & lane_lt);
+        if (esc && q < room) {
+          cid_c[q] = cur.c;
+          lp_c[q] = uint16_t(p);
+          ev_c[q] = uint8_t(ex);
+        }
+        run += __popc(bal);
+      }
+    }
+    __syncwarp();  // buf[b] is read before it is refilled
+    g = gn;
+    cur = nxt;
   }
 }
 
@@ -557,8 +789,7 @@ cudaError_t launch_encode(const Items& items, void* ws_base, cudaStream_t stream
     const uint64_t cap = uint64_t(dev.num_sms) * kEncCtasPerSm;
     const unsigned grid = unsigned(items.total_tiles < cap ? items.total_tiles : cap);
     if (g_timing.before) cudaEventRecord(g_timing.before, stream);
-    enc_main<<<grid, kEncThreads, smem, stream>>>(items, ws);
-    err = cudaGetLastError();
+    err = launch_pdl(enc_main, dim3(grid), dim3(kEncThreads), smem, stream, items, ws);
     if (g_timing.after) cudaEventRecord(g_timing.after, stream);
     if (err != cudaSuccess) return err;
   }
@@ -581,8 +812,16 @@ cudaError_t launch_place(const Items& items, const EncWs& ws, cudaStream_t strea
     // blocks take segments by ticket: about two waves of resident blocks suffice
     const uint64_t cap = 2ull * kPlaceBlocksPerSm * uint64_t(dev.num_sms) / gy;
     if (gx > cap) gx = cap > 0 ? cap : 1;
-    enc_place<<<dim3(unsigned(gx), gy), kPlaceThreads, 0, stream>>>(items, ws);
-    err = cudaGetLastError();
+    err = launch_pdl(enc_place, dim3(unsigned(gx), gy), dim3(kPlaceThreads), 0, stream, items, ws);
+    if (err != cudaSuccess) return err;
+  }
+  if (items.total_tiles > 0) {
+    // chunks too dense to stage (returns at once when there are none)
+    const uint64_t chunks = items.total_tiles * kChunksPerTile;
+    const uint64_t blocks = (chunks + kRegenWarps - 1) / kRegenWarps;
+    const uint64_t cap = uint64_t(dev.num_sms) * 8;
+    err = launch_pdl(enc_regen, dim3(unsigned(blocks < cap ? blocks : cap)), dim3(kRegenWarps * 32), 0, stream,
+                     items, ws);
   }
   return err;
 }

@@ -88,6 +88,7 @@ __device__ uint64_t group_first_tile(const Items& items, uint64_t g) {
 }
 
 __global__ void ce_prepare(const __grid_constant__ Items items, CeWs ws) {
+  pdl_trigger();
   const uint64_t nthreads = uint64_t(gridDim.x) * blockDim.x;
   const uint64_t gtid = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   for (uint64_t w = gtid; w < uint64_t(items.count) * 256; w += nthreads) ws.cal.hist[w] = 0;
@@ -402,6 +403,7 @@ __global__ void __launch_bounds__(kCeThreads, kCeCtasPerSm) ce_main(const __grid
   };
   // escape totals per tensor, per warp, added when the tensor changes
   uint32_t acc_item = kNoItem, acc = 0;
+  bool dense = false;  // this warp staged no escapes of some chunk (enc_regen will write them)
   bool failed = false;
   for (uint32_t it = 0;; ++it) {
     const int s = int(it % kCeStages);
@@ -448,12 +450,14 @@ __global__ void __launch_bounds__(kCeThreads, kCeCtasPerSm) ce_main(const __grid
         acc = 0;
       }
       acc += run_e;
+      dense |= run_e > kStageMax;
       if (lane == 0) ws.enc.chunk_cnt[chunk] = uint16_t(run_e);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty[s]);
   }
   if (lane == 0 && acc) atomicAdd(ws.enc.item_esc + acc_item, acc);
+  if (lane == 0 && dense) atomicOr(&ws.enc.hdr->dense, 1u);
   if (failed) return;  // the select warp stops on its own timeout
   if (run && !flush()) return;
   // tell the select warp to stop once it has ranked everything posted

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "sz_device.cuh"
@@ -34,6 +35,26 @@ cudaError_t launch_decode_inplace(const Items& items, void* ws, cudaStream_t str
 cudaError_t launch_calibrate_encode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
 // escape placement, pads and metas after an encode pass (enc_place)
 cudaError_t launch_place(const Items& items, const EncWs& ws, cudaStream_t stream, const DeviceInfo& dev);
+
+// Launches `kernel` on `stream` as a programmatic dependent of the kernel
+// before it: it may be scheduled while that kernel drains, and waits for it
+// in pdl_wait (every kernel launched this way calls pdl_wait before reading
+// global memory).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Optional timing hook: when set (non-null), launchers record `before` just
 // before and `after` just after their main kernel on the launch stream.
