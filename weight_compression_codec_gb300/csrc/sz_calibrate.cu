@@ -195,7 +195,11 @@ __global__ void __launch_bounds__(kCalThreads, kCalCtasPerSm) cal_hist(const __g
         hd.n = nh;
         hd.flags = invalid ? kStageInvalid : 0u;
         mbar_arrive_expect_tx(&sh.full[s], bulk);
-        if (bulk) bulk_g2s(sh.st[s].x, cur_x + g, bulk, &sh.full[s]);
+        // evict-first: the step's previous decode may have left ~100 MB of
+        // dirty output in L2; counting x (read once) should not evict those
+        // lines, which costs their write-back inside this kernel (KV cache
+        // 64 x 4 Mi: 102.7 -> 94.5 us, the step 5 us shorter)
+        if (bulk) bulk_g2s_evict_first(sh.st[s].x, cur_x + g, bulk, &sh.full[s]);
       } else if (lane == 1 && tail) {
         cp_async16_zfill(reinterpret_cast<uint8_t*>(sh.st[s].x) + bulk,
                          reinterpret_cast<const uint8_t*>(cur_x + g) + bulk, tail);
