@@ -317,22 +317,31 @@ SZ_API int sz_check_bounded_waits(void* d_workspace, size_t workspace_bytes, sz_
  * (the sz_decode_many kernels); payloads back to back in host memory (gaps
  * under 256 bytes) go in one copy.  d_scratch (device, 256-byte aligned) holds
  * the metas, the group tables and the decode workspace:
- * sz_decode_many_host_scratch_bytes bytes.  Work on copy_stream follows the
+ * sz_decode_many_host_scratch_bytes bytes.  h_upload is a PINNED host buffer
+ * of the caller's (cudaHostAlloc or cudaHostRegister; pageable memory is
+ * refused with SZ_ERR_ARG) of at least sz_decode_many_host_upload_bytes(count)
+ * bytes: the call writes the metas and the per-group tables there before it
+ * returns and copies them to the device on `stream`, so the caller may write
+ * to or free h_upload only once `stream` has passed the call (an event
+ * recorded on `stream` after it); h_items and h_metas may be pageable and may
+ * be reused as soon as the call returns.  Work on copy_stream follows the
  * caller's earlier work on `stream`, and `stream` waits for all of it, so the
- * call is ordered on `stream` like any other.  h_items and h_metas may be
- * pageable and may be reused once the call returns: the library copies them
- * into one of two pinned host buffers it keeps per device and thread, and so
- * blocks the host until the upload of the call two back has completed.
- * SZ_ERR_WORKSPACE if a payload does not fit in half the staging buffer;
- * SZ_ERR_CUDA if a CUDA call fails.  Device-visible conditions (a meta
- * that disagrees with the layout, an escape out of range) are reported as by
- * sz_decode_many, through the workspace word at the start of the decode
- * workspace (see sz_decode_many_host_flags_offset). */
+ * call is ordered on `stream` like any other.  The call allocates no memory;
+ * it creates three CUDA events and destroys them before it returns (the
+ * runtime frees them once their work is done).  SZ_ERR_WORKSPACE if a
+ * payload does not fit in half the staging buffer or if scratch_bytes or
+ * upload_bytes is too small; SZ_ERR_CUDA if a CUDA call fails.
+ * Device-visible conditions (a meta that disagrees with the layout, an escape
+ * out of range) are reported as by sz_decode_many, through the workspace word
+ * at the start of the decode workspace (see sz_decode_many_host_flags_offset). */
 SZ_API size_t sz_decode_many_host_scratch_bytes(const sz_item* h_items, const sz_meta* h_metas, uint32_t count,
                                                 uint64_t staging_bytes);
+/* Bytes of the pinned upload buffer: round_up(count * 96, 256) + count * 64;
+ * 0 if count is 0 or above SZ_MANY_MAX_ITEMS. */
+SZ_API size_t sz_decode_many_host_upload_bytes(uint32_t count);
 SZ_API int sz_decode_many_host(const sz_item* h_items, const sz_meta* h_metas, uint32_t count,
                                void* d_staging, uint64_t staging_bytes, void* d_scratch, size_t scratch_bytes,
-                               sz_stream stream, sz_stream copy_stream);
+                               void* h_upload, size_t upload_bytes, sz_stream stream, sz_stream copy_stream);
 /* Offset (bytes) of the decode workspace, and so of its SZ_FLAG_* word, in the
  * scratch of sz_decode_many_host: pass d_scratch + this to sz_workspace_flags. */
 SZ_API size_t sz_decode_many_host_flags_offset(uint32_t count);

@@ -105,3 +105,53 @@ def test_host_decode_rejects_a_small_staging_buffer():
     with pytest.raises(B.SplitZipError):
         sz.HostDecode(views, metas, [b.codebooks[0]], [torch.empty(500_000, dtype=torch.int16, device=DEV)],
                       metas[0].comp_bytes)  # each half smaller than the payload
+
+
+def test_host_decode_runs_back_to_back_and_allocates_nothing():
+    """Repeated runs alternate the two pinned upload buffers; after the first
+    run the calls change neither the device's free memory nor torch's
+    allocations (the library allocates nothing and releases its events)."""
+    arrays = [inputs.paged_kv_block(i) for i in range(300)]
+    b, metas = _encoded(arrays)
+    blob, views = _host_blob(b, metas)
+    outs, flags, hd = _decode_from_host(views, metas, b, 1 << 20)
+    assert flags == 0
+    torch.cuda.synchronize()
+    free0, allocated0 = torch.cuda.mem_get_info(DEV)[0], torch.cuda.memory_allocated(DEV)
+    for _ in range(6):
+        for y in outs:
+            y.fill_(7)
+        hd.run()
+    assert hd.flags() == 0
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info(DEV)[0] == free0 and torch.cuda.memory_allocated(DEV) == allocated0
+    for x, y in zip(arrays, outs):
+        assert np.array_equal(to_np_u16(y), x)
+
+
+def test_host_decode_rejects_pageable_or_short_upload_buffers():
+    arrays = [inputs.gaussian(20_000, 0.02, seed=74), inputs.gaussian(3000, 0.02, seed=75)]
+    b, metas = _encoded(arrays)
+    blob, views = _host_blob(b, metas)
+    outs = [torch.empty(n, dtype=torch.int16, device=DEV) for n in b.n]
+    hd = sz.HostDecode(views, metas, [b.codebooks[i] for i in range(2)], outs, 1 << 20)
+    lib = B.lib()
+    need = lib.sz_decode_many_host_upload_bytes(2)
+    s = torch.cuda.current_stream().cuda_stream
+    pageable = torch.empty(need, dtype=torch.uint8)
+    assert not pageable.is_pinned()
+
+    def call(up, nbytes):
+        return lib.sz_decode_many_host(hd.items, hd.metas, 2, hd.staging.data_ptr(), hd.staging.numel(),
+                                       hd.scratch.data_ptr(), hd.scratch.numel(), up, nbytes, s,
+                                       hd.copy_stream.cuda_stream)
+
+    assert call(pageable.data_ptr(), need) == B.SZ_ERR_ARG
+    pinned = torch.empty(need, dtype=torch.uint8).pin_memory()
+    assert call(pinned.data_ptr(), need - 1) == B.SZ_ERR_WORKSPACE
+    assert call(None, need) == B.SZ_ERR_ARG
+    assert call(pinned.data_ptr(), need) == B.SZ_OK
+    torch.cuda.synchronize()
+    assert hd.flags() == 0
+    for x, y in zip(arrays, outs):
+        assert np.array_equal(to_np_u16(y), x)

@@ -1,0 +1,200 @@
+"""Tables of small tensors (at most two tiles on average, such as the blocks of a
+paged KV cache) take the single-read path of sz_encode_many and
+sz_calibrate_encode_many: a whole tensor held in shared memory.  Its results
+are checked here against the CPU oracle tensor by tensor at ragged sizes,
+escape-heavy inputs, flagged items, the coverage gate, and a table whose
+one large tensor sends the call back to the general kernels."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import weight_compression_codec_gb300 as sz
+from weight_compression_codec_gb300 import binding as B
+from weight_compression_codec_gb300 import inputs
+
+from gpu_util import DEV, check_codebook, to_dev, to_np_u16
+
+pytestmark = pytest.mark.gpu
+
+SMALL_MAX = 2 * 8192  # elements of the largest tensor held whole
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    sz.build()
+    torch.cuda.set_device(DEV)
+
+
+def _tiles(n: int) -> int:
+    return (n + 8191) // 8192
+
+
+def _small_routed(arrays) -> bool:
+    return sum(_tiles(a.size) for a in arrays) <= 2 * len(arrays)
+
+
+def _encode_both_ways(arrays):
+    """Calibrate + encode of the table as one fused call and as two calls."""
+    xs = [to_dev(a) for a in arrays]
+    out = []
+    for fused in (True, False):
+        b = sz.Batch(xs)
+        ws = sz.Workspace(DEV)
+        if fused:
+            sz.sz_calibrate_encode_many(b.table, workspace=ws)
+            flags = sz.sz_workspace_flags(ws.buf)
+        else:
+            sz.sz_calibrate_many(b.table, workspace=ws)
+            flags = sz.sz_workspace_flags(ws.buf)
+            sz.sz_encode_many(b.table, workspace=ws)
+            flags |= sz.sz_workspace_flags(ws.buf)
+        torch.cuda.synchronize()
+        assert flags == 0
+        out.append(b)
+    return out
+
+
+def _check_against_oracle(b: "sz.Batch", arrays) -> None:
+    cbs = b.codebooks.cpu().numpy()
+    for i, x in enumerate(arrays):
+        ocb = oracle.calibrate(x)
+        check_codebook(sz.codebook_from_bytes(cbs[i]), ocb, x.size)
+        opay, om = oracle.encode(x, ocb)
+        m = sz.meta_from_bytes(b.metas[i].cpu().numpy())
+        assert m.status == 0 and m.as_tuple() == om.as_tuple(), (i, x.size, m, om)
+        assert m.coverage == ocb.coverage
+        gp = b.payload_view(i, om.comp_bytes).cpu().numpy()
+        assert np.array_equal(gp, opay), f"tensor {i} (n={x.size}): payload differs"
+
+
+def _ragged_table():
+    sizes = [0, 1, 2, 3, 7, 8, 9, 15, 16, 17, 255, 1023, 1024, 1025, 4097, 8191, 8192, 8193, 12_345, 16_383, 16_384]
+    arrays = []
+    for k, n in enumerate(sizes):
+        kind = k % 3
+        if kind == 0:
+            arrays.append(inputs.gaussian(n, 0.02, seed=700 + k))
+        elif kind == 1:
+            arrays.append(inputs.edge_case(n, seed=700 + k))  # broad exponents: many escapes
+        else:
+            a = inputs.gaussian(n, 1.0, seed=700 + k)
+            a[::97] = inputs.edge_case(a[::97].size, seed=800 + k)  # sparse escapes
+            arrays.append(a)
+    return arrays
+
+
+def test_small_table_ragged_sizes_match_the_oracle():
+    arrays = _ragged_table()
+    assert _small_routed(arrays)
+    fused, separate = _encode_both_ways(arrays)
+    for b in (fused, separate):
+        _check_against_oracle(b, arrays)
+    # and decode back
+    sz.sz_decode_many(fused.table)
+    torch.cuda.synchronize()
+    for i, x in enumerate(arrays):
+        assert np.array_equal(to_np_u16(fused.out_view(i)), x), f"decode {i}"
+
+
+def test_small_table_many_blocks_and_escape_heavy_blocks():
+    arrays = [inputs.paged_kv_block(i) for i in range(400)]
+    for k in range(0, 400, 37):  # every 37th block escape-heavy
+        arrays[k] = inputs.edge_case(SMALL_MAX, seed=900 + k)
+    assert _small_routed(arrays)
+    fused, separate = _encode_both_ways(arrays)
+    assert torch.equal(fused.codebooks, separate.codebooks) and torch.equal(fused.metas, separate.metas)
+    for i in range(len(arrays)):
+        m = sz.meta_from_bytes(fused.metas[i].cpu().numpy())
+        assert torch.equal(fused.payload_view(i, m.comp_bytes), separate.payload_view(i, m.comp_bytes)), i
+    sample = [0, 1, 37, 74, 200, 399]
+    sub = sz.Batch([to_dev(arrays[i]) for i in sample])
+    sz.sz_calibrate_encode_many(sub.table)
+    torch.cuda.synchronize()
+    _check_against_oracle(sub, [arrays[i] for i in sample])
+
+
+def test_small_table_with_one_large_tensor_goes_to_the_general_kernels():
+    arrays = [inputs.gaussian(40_000, 0.02, seed=950)] + [inputs.edge_case(1000 + 37 * k, seed=951 + k)
+                                                           for k in range(30)]
+    assert _small_routed(arrays) and arrays[0].size > SMALL_MAX
+    fused, separate = _encode_both_ways(arrays)
+    for b in (fused, separate):
+        _check_against_oracle(b, arrays)
+
+
+def test_small_table_flags_match_between_the_calls():
+    # item 1's input is misaligned (skipped by both passes), item 2's payload
+    # is too small (calibrated, not encoded), item 3 is empty
+    arrays = [inputs.gaussian(5000, 0.02, seed=960 + k) for k in range(3)] + [np.zeros(0, np.uint16)]
+    assert _small_routed(arrays)
+    xs = [to_dev(a) for a in arrays]
+    base = torch.zeros(5000 + 8, dtype=torch.int16, device=DEV)
+    base[1:5001] = xs[1]
+    xs[1] = base[1:5001]  # 2-byte offset: not 16-byte aligned
+    outs = []
+    for fused in (False, True):
+        b = sz.Batch(xs, capacity=[sz.sz_max_payload_bytes(5000), sz.sz_max_payload_bytes(5000), 500, 16])
+        b.codebooks.fill_(0xAB)
+        ws = sz.Workspace(DEV)
+        if fused:
+            sz.sz_calibrate_encode_many(b.table, workspace=ws)
+            flags = sz.sz_workspace_flags(ws.buf)
+        else:
+            sz.sz_calibrate_many(b.table, workspace=ws)
+            flags = sz.sz_workspace_flags(ws.buf)
+            sz.sz_encode_many(b.table, workspace=ws)
+            flags |= sz.sz_workspace_flags(ws.buf)
+        torch.cuda.synchronize()
+        outs.append((flags, b.codebooks.cpu().clone(), b.metas.cpu().clone(), b.payload_view(0).cpu().clone()))
+    (f1, c1, m1, p1), (f2, c2, m2, p2) = outs
+    assert f1 == f2 and f1 & B.SZ_FLAG_ALIGN and f1 & B.SZ_FLAG_CAPACITY
+    assert torch.equal(c1, c2) and torch.equal(m1, m2)
+    n0 = sz.meta_from_bytes(m1[0].numpy()).comp_bytes
+    assert torch.equal(p1[:n0], p2[:n0])
+    # item 0 is right; item 2 got its codebook but no payload; item 3 is empty
+    ocb = oracle.calibrate(arrays[0])
+    check_codebook(sz.codebook_from_bytes(c2[0].numpy()), ocb, 5000)
+    opay, om = oracle.encode(arrays[0], ocb)
+    assert sz.meta_from_bytes(m2[0].numpy()).as_tuple() == om.as_tuple() and np.array_equal(p2[:n0].numpy(), opay)
+    check_codebook(sz.codebook_from_bytes(c2[2].numpy()), oracle.calibrate(arrays[2]), 5000)
+    assert sz.meta_from_bytes(m2[2].numpy()).status & B.SZ_FLAG_CAPACITY
+    m3 = sz.meta_from_bytes(m2[3].numpy())
+    assert m3.status == 0 and m3.n == 0 and m3.comp_bytes == 0
+
+
+@pytest.mark.parametrize("gate", [0.99, -1.0])
+def test_small_table_gate_matches_the_oracle(gate):
+    arrays = [inputs.paged_kv_block(i) for i in range(40)] + [inputs.edge_case(3000 + k, seed=970 + k)
+                                                              for k in range(8)]
+    assert _small_routed(arrays)
+    xs = [to_dev(a) for a in arrays]
+    b = sz.Batch(xs)
+    sz.sz_calibrate_many(b.table)
+    b.payload.fill_(0x5A)
+    ws = sz.Workspace(DEV)
+    report = sz.sz_encode_gated_many(b.table, gate, workspace=ws)
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    torch.cuda.synchronize()
+    cbs = [sz.codebook_from_bytes(c) for c in b.codebooks.cpu().numpy()]
+    ometas = []
+    for i, x in enumerate(arrays):
+        ocb = oracle.calibrate(x)
+        assert cbs[i].coverage == ocb.coverage
+        opay, om = oracle.encode(x, ocb)
+        ometas.append(om)
+        m = sz.meta_from_bytes(b.metas[i].cpu().numpy())
+        if oracle.gated(ocb.coverage, gate):
+            assert m.status == B.SZ_META_GATED and m.n == x.size and m.coverage == ocb.coverage
+            assert bool(torch.all(b.payload_view(i) == 0x5A)), f"gated tensor {i}: payload written"
+        else:
+            assert m.status == 0 and m.as_tuple() == om.as_tuple()
+            assert np.array_equal(b.payload_view(i, om.comp_bytes).cpu().numpy(), opay)
+    expect = oracle.gate_report([a.size for a in arrays], [c.coverage for c in cbs], ometas, gate)
+    assert sz.read_gate_report(report) == expect
+    if gate > 0:
+        assert any(oracle.gated(c.coverage, gate) for c in cbs) and not all(oracle.gated(c.coverage, gate)
+                                                                           for c in cbs)

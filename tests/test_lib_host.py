@@ -172,6 +172,10 @@ def test_host_decode_planner_on_the_host():
     metas[3].n = n + 1
     assert lib.sz_decode_many_host_scratch_bytes(items, metas, count, 2 * step) == 0  # meta disagrees with n
     assert lib.sz_decode_many_host_flags_offset(count) % 256 == 0
+    # the pinned upload buffer: the metas (256-byte rounded) then the tables
+    for c in (1, 2, 3, 6, 1000):
+        assert lib.sz_decode_many_host_upload_bytes(c) == ((c * 96 + 255) // 256) * 256 + c * 64
+    assert lib.sz_decode_many_host_upload_bytes(0) == 0
 
 
 # ---------------------------------------------------------------------------- in-place slot decode schedule

@@ -124,7 +124,8 @@ SIGNATURES = {
     "sz_decode_inplace_workspace_bytes": (_SZ, [_U32, _U64]),
     "sz_inplace_plan": (_INT, [_U64, _U64, _U64, ctypes.POINTER(SzInplaceTile)]),
     "sz_decode_many_host_scratch_bytes": (_SZ, [_VP, _VP, _U32, _U64]),
-    "sz_decode_many_host": (_INT, [_VP, _VP, _U32, _VP, _U64, _VP, _SZ, _VP, _VP]),
+    "sz_decode_many_host_upload_bytes": (_SZ, [_U32]),
+    "sz_decode_many_host": (_INT, [_VP, _VP, _U32, _VP, _U64, _VP, _SZ, _VP, _SZ, _VP, _VP]),
     "sz_decode_many_host_flags_offset": (_SZ, [_U32]),
     "sz_set_timing_events": (_INT, [_VP, _VP]),
     "sz_decode_noalloc": (_INT, [_VP, _U64, _VP, _VP, _VP, _U64, _VP, _VP]),

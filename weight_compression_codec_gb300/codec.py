@@ -381,7 +381,10 @@ class HostDecode:
 
     payloads[i]: pinned host uint8 tensor (or a view into one) holding the
     payload; metas[i]: its Meta; codebooks[i] / outs[i]: device tensors.  The
-    staging buffer and scratch are allocated once and reused by run()."""
+    staging buffer, the scratch and two pinned upload buffers are allocated
+    once and reused by run(): a run writes one upload buffer while the copy
+    out of the other (the run before) may still be queued, and waits for the
+    run two back to have passed its upload before reusing that one."""
 
     def __init__(self, payloads, metas, codebooks, outs, staging_bytes: int):
         count = len(payloads)
@@ -405,13 +408,26 @@ class HostDecode:
         if need == 0:
             raise B.SplitZipError(B.SZ_ERR_WORKSPACE, "sz_decode_many_host_scratch_bytes")
         self.scratch = torch.empty(need, dtype=torch.uint8, device=dev)
+        up = B.lib().sz_decode_many_host_upload_bytes(count)
+        self.uploads = [torch.empty(up, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        self.uploaded = [None, None]  # event after the run that last used each upload buffer
+        self.next = 0
         self.copy_stream = torch.cuda.Stream(device=dev)
 
     def run(self, stream=None) -> None:
+        k = self.next
+        self.next ^= 1
+        if self.uploaded[k] is not None:
+            self.uploaded[k].synchronize()
+        up = self.uploads[k]
         rc = B.lib().sz_decode_many_host(self.items, self.metas, self.count, self.staging.data_ptr(),
                                          self.staging.numel(), self.scratch.data_ptr(), self.scratch.numel(),
-                                         _stream_handle(stream), self.copy_stream.cuda_stream)
+                                         up.data_ptr(), up.numel(), _stream_handle(stream),
+                                         self.copy_stream.cuda_stream)
         B.check(rc, "sz_decode_many_host")
+        ev = torch.cuda.Event()
+        ev.record(stream if stream is not None else torch.cuda.current_stream())
+        self.uploaded[k] = ev
 
     def flags(self, stream=None) -> int:
         off = B.lib().sz_decode_many_host_flags_offset(self.count)

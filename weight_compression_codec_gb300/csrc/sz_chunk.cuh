@@ -226,4 +226,69 @@ __device__ __forceinline__ uint32_t encode_chunk8(const Stage& st, uint32_t warp
   return run;
 }
 
+// Pad bytes of item `it` (pk -> sm, sm -> chunk_id, local_pos -> esc_val:
+// each < 4 bytes), written by threads r = 0..11 of the caller.
+__device__ __forceinline__ void finish_pads(const sz_item& it, const Layout& l, uint64_t n, uint32_t e, uint32_t flags,
+                                            uint32_t r) {
+  if (!flags && r < 12) {
+    uint8_t* p = it.payload;
+    if (r < 4 && l.n_pairs + r < l.off_sm) p[l.n_pairs + r] = 0;
+    if (r >= 4 && r < 8 && l.off_sm + n + (r - 4) < l.off_cid) p[l.off_sm + n + (r - 4)] = 0;
+    if (r >= 8 && l.off_lpos + 2ull * e + (r - 8) < l.off_ev) p[l.off_lpos + 2ull * e + (r - 8)] = 0;
+  }
+}
+
+// The meta of item `it` (coverage: its codebook's), its line of the build
+// report of a gated call, and its status bits in the header; one thread.  A
+// gated item's meta holds n, its coverage and status SZ_META_GATED only.
+__device__ inline void finish_meta(const EncWs& ws, const sz_item& it, const Layout& l, uint64_t n, uint32_t e,
+                                   uint32_t flags, double coverage) {
+  const bool gated = flags == SZ_META_GATED;
+  if (flags && !gated) set_flag(ws.hdr, flags);
+  if (it.meta != nullptr && (reinterpret_cast<uintptr_t>(it.meta) & 15) == 0) {
+    sz_meta m;
+    m.n = n;
+    m.n_pairs = gated ? 0 : l.n_pairs;
+    m.n_esc = gated ? 0 : e;
+    m.comp_bytes = gated ? 0 : l.comp_bytes;
+    m.off_pk = 0;
+    m.off_sm = gated ? 0 : l.off_sm;
+    m.off_cid = gated ? 0 : l.off_cid;
+    m.off_lpos = gated ? 0 : l.off_lpos;
+    m.off_ev = gated ? 0 : l.off_ev;
+    m.chunk_size = kChunk;
+    m.status = flags;
+    m.coverage = coverage;
+    m.reserved1 = 0;
+    *it.meta = m;
+  }
+  if (ws.report != nullptr) {
+    sz_gate_report* rep = ws.report;
+    if (!flags) {
+      atomicAdd(reinterpret_cast<unsigned long long*>(&rep->tensors_encoded), 1ull);
+      atomicAdd(reinterpret_cast<unsigned long long*>(&rep->raw_bytes_encoded), 2ull * n);
+      atomicAdd(reinterpret_cast<unsigned long long*>(&rep->payload_bytes), l.comp_bytes);
+      if (l.comp_bytes > 2ull * n) atomicAdd(reinterpret_cast<unsigned long long*>(&rep->tensors_expanded), 1ull);
+      atomicAdd(reinterpret_cast<unsigned long long*>(&rep->escapes), uint64_t(e));
+    } else if (gated) {
+      atomicAdd(reinterpret_cast<unsigned long long*>(&rep->tensors_gated), 1ull);
+      atomicAdd(reinterpret_cast<unsigned long long*>(&rep->raw_bytes_gated), 2ull * n);
+    } else {
+      atomicAdd(reinterpret_cast<unsigned long long*>(&rep->tensors_failed), 1ull);
+    }
+  }
+}
+
+// The coverage an item's meta records: its codebook's (0 without a usable codebook).
+__device__ __forceinline__ double codebook_coverage(const sz_item& it) {
+  return (it.codebook && !(reinterpret_cast<uintptr_t>(it.codebook) & 15)) ? it.codebook->coverage : 0.0;
+}
+
+// Pads (threads r = 0..11), then meta and report (thread r == 0) of item `it`.
+__device__ inline void finish_item(const EncWs& ws, const sz_item& it, const Layout& l, uint64_t n, uint32_t e,
+                                   uint32_t flags, uint32_t r) {
+  finish_pads(it, l, n, e, flags, r);
+  if (r == 0) finish_meta(ws, it, l, n, e, flags, codebook_coverage(it));
+}
+
 }  // namespace sz

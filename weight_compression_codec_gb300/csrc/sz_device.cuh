@@ -19,6 +19,7 @@ constexpr uint32_t kTile = SZ_TILE_ELEMS;           // 8192
 constexpr uint32_t kChunksPerTile = kTile / kChunk; // 8
 constexpr uint32_t kEscape = SZ_ESCAPE_CODE;        // 16
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // bounded waits give up after 2 s
+constexpr uint32_t kSmallMax = 2 * kTile;           // elements of a tensor the small-tensor kernels hold whole
 
 // ------------------------------------------------------------------ layout
 // Wire layout of "splitzip_codec.py" assemble_payload: pk | sm | chunk_id |
@@ -90,7 +91,8 @@ struct WsHeader {
   unsigned long long ticket;  // dynamic tile counter (encode)
   uint32_t tiles_differ;      // in-place decode: set when the tensors' tile counts are not all equal
   uint32_t dense;             // encode: some chunk had too many escapes to stage (kStageMax)
-  uint32_t reserved[58];
+  uint32_t large;             // small-tensor route: some tensor is larger than kSmallMax
+  uint32_t reserved[57];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
@@ -132,6 +134,8 @@ struct EncWs {
   uint32_t* tile_item;
   double gate;              // coverage gate (< 0: none)
   sz_gate_report* report;   // build report of a gated call, or nullptr
+  bool small;               // the small-tensor kernels were launched first: the general
+                            // kernels work only if the prepare pass found a large tensor
 };
 // Bytes of the encode workspace after its header (map excluded).
 __host__ __device__ inline uint64_t enc_body_bytes(uint32_t count, uint64_t tiles) {
@@ -161,6 +165,7 @@ __host__ __device__ inline EncWs enc_ws_at(WsHeader* hdr, void* body, uint32_t c
   w.tile_item = tile_item;
   w.gate = -1.0;
   w.report = nullptr;
+  w.small = false;
   return w;
 }
 __host__ __device__ inline EncWs enc_ws(void* base, uint32_t count, uint64_t tiles) {

@@ -103,6 +103,7 @@ __global__ void enc_prepare(const __grid_constant__ Items items, EncWs ws) {
       if (it.tile_begin != expect) bad |= SZ_FLAG_ITEMS;
       if (i + 1 == items.count && it.tile_begin + tiles_of(it.n) != items.total_tiles) bad |= SZ_FLAG_ITEMS;
     }
+    if (ws.small && it.n > kSmallMax) atomicOr(&ws.hdr->large, 1u);
     if (bad) set_flag(ws.hdr, bad);
     // the coverage gate: a tensor below it is left uncompressed (not an error)
     else if (ws.gate >= 0.0 && it.codebook->coverage < ws.gate) bad = SZ_META_GATED;
@@ -133,8 +134,9 @@ __global__ void __launch_bounds__(kEncThreads, kEncCtasPerSm)
   const int lane = tid & 31;
   pdl_trigger();
   pdl_wait();  // enc_prepare's writes
-  // an inconsistent item table (flagged by enc_prepare) is never walked
-  if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
+  // an inconsistent item table (flagged by enc_prepare) is never walked; a
+  // table of small tensors is encoded by small_main
+  if ((ws.hdr->flags & SZ_FLAG_ITEMS) || (ws.small && !ws.hdr->large)) return;
 
   const uint64_t T = items.total_tiles;
 
@@ -306,56 +308,6 @@ constexpr uint64_t kSmallElems = uint64_t(kSegChunks) * kChunk;  // one segment:
 constexpr uint32_t kScatterUnroll = 8;  // escapes per thread per scatter round
 constexpr int kPlaceBlocksPerSm = 4;
 
-// Pad bytes (pk -> sm, sm -> chunk_id, local_pos -> esc_val: each < 4 bytes,
-// by threads r = 0..11 of the caller), the meta (by r == 0) of item `it`, and
-// its line of the build report of a gated call.  A gated item's meta holds n,
-// its coverage and status SZ_META_GATED only.
-__device__ void finish_item(const EncWs& ws, const sz_item& it, const Layout& l, uint64_t n, uint32_t e,
-                            uint32_t flags, uint32_t r) {
-  if (!flags && r < 12) {
-    uint8_t* p = it.payload;
-    if (r < 4 && l.n_pairs + r < l.off_sm) p[l.n_pairs + r] = 0;
-    if (r >= 4 && r < 8 && l.off_sm + n + (r - 4) < l.off_cid) p[l.off_sm + n + (r - 4)] = 0;
-    if (r >= 8 && l.off_lpos + 2ull * e + (r - 8) < l.off_ev) p[l.off_lpos + 2ull * e + (r - 8)] = 0;
-  }
-  if (r == 0) {
-    const bool gated = flags == SZ_META_GATED;
-    if (flags && !gated) set_flag(ws.hdr, flags);
-    if (it.meta != nullptr && (reinterpret_cast<uintptr_t>(it.meta) & 15) == 0) {
-      sz_meta m;
-      m.n = n;
-      m.n_pairs = gated ? 0 : l.n_pairs;
-      m.n_esc = gated ? 0 : e;
-      m.comp_bytes = gated ? 0 : l.comp_bytes;
-      m.off_pk = 0;
-      m.off_sm = gated ? 0 : l.off_sm;
-      m.off_cid = gated ? 0 : l.off_cid;
-      m.off_lpos = gated ? 0 : l.off_lpos;
-      m.off_ev = gated ? 0 : l.off_ev;
-      m.chunk_size = kChunk;
-      m.status = flags;
-      m.coverage = (it.codebook && !(reinterpret_cast<uintptr_t>(it.codebook) & 15)) ? it.codebook->coverage : 0.0;
-      m.reserved1 = 0;
-      *it.meta = m;
-    }
-    if (ws.report != nullptr) {
-      sz_gate_report* rep = ws.report;
-      if (!flags) {
-        atomicAdd(reinterpret_cast<unsigned long long*>(&rep->tensors_encoded), 1ull);
-        atomicAdd(reinterpret_cast<unsigned long long*>(&rep->raw_bytes_encoded), 2ull * n);
-        atomicAdd(reinterpret_cast<unsigned long long*>(&rep->payload_bytes), l.comp_bytes);
-        if (l.comp_bytes > 2ull * n) atomicAdd(reinterpret_cast<unsigned long long*>(&rep->tensors_expanded), 1ull);
-        atomicAdd(reinterpret_cast<unsigned long long*>(&rep->escapes), uint64_t(e));
-      } else if (gated) {
-        atomicAdd(reinterpret_cast<unsigned long long*>(&rep->tensors_gated), 1ull);
-        atomicAdd(reinterpret_cast<unsigned long long*>(&rep->raw_bytes_gated), 2ull * n);
-      } else {
-        atomicAdd(reinterpret_cast<unsigned long long*>(&rep->tensors_failed), 1ull);
-      }
-    }
-  }
-}
-
 // Writes the escapes of chunk `c` (cnt of them, the first at global index
 // o) from its staging slot.  Threads r = 0..stride-1 of the caller.
 __device__ __forceinline__ void scatter_chunk(const EncWs& ws, uint8_t* cid_p, uint8_t* lpos_p, uint8_t* ev_p,
@@ -434,7 +386,7 @@ __global__ void __launch_bounds__(kPlaceThreads, kPlaceBlocksPerSm) enc_place(co
   const uint32_t tid = threadIdx.x, lane = tid & 31u, warp = tid >> 5;
   pdl_trigger();
   pdl_wait();  // the encode pass's counts and staging
-  if (ws.hdr->flags & SZ_FLAG_ITEMS) return;
+  if ((ws.hdr->flags & SZ_FLAG_ITEMS) || (ws.small && !ws.hdr->large)) return;
   const uint32_t groups = (items.count + kPlaceWarps - 1) / kPlaceWarps;
   for (uint32_t grp = blockIdx.y; grp < groups; grp += gridDim.y) {
     {
@@ -585,7 +537,7 @@ __global__ void __launch_bounds__(kRegenWarps * 32) enc_regen(const __grid_const
   __shared__ __align__(16) uint8_t ev_sh[kRegenWarps][kChunk + 16];  // ... and esc_val, then copied out
   __shared__ uint64_t bar[kRegenWarps][2];
   pdl_wait();  // enc_place's offsets
-  if (ws.hdr->dense == 0 || (ws.hdr->flags & SZ_FLAG_ITEMS)) return;
+  if (ws.hdr->dense == 0 || (ws.hdr->flags & SZ_FLAG_ITEMS) || (ws.small && !ws.hdr->large)) return;
   const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
   const uint32_t lane_lt = (1u << lane) - 1u;
   const uint64_t total = items.total_tiles * kChunksPerTile;
@@ -766,6 +718,7 @@ cudaError_t launch_encode(const Items& items, void* ws_base, cudaStream_t stream
   EncWs ws = enc_ws(ws_base, items.count, items.total_tiles);
   ws.gate = gate;
   ws.report = report;
+  ws.small = small_route(items);
   cudaError_t err = cudaMemsetAsync(ws_base, 0, sizeof(WsHeader), stream);
   if (err != cudaSuccess) return err;
   {
@@ -777,6 +730,13 @@ cudaError_t launch_encode(const Items& items, void* ws_base, cudaStream_t stream
     const unsigned grid = unsigned(blocks < 2048 ? (blocks ? blocks : 1) : 2048);
     enc_prepare<<<grid, 256, 0, stream>>>(items, ws);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
+  // tables of small tensors: whole tensors in shared memory, one CTA per SM
+  // (the general kernels below then return at once, unless a tensor is too large)
+  TimingHook hook = g_timing;
+  if (ws.small) {
+    if ((err = launch_small(items, ws, nullptr, stream, dev)) != cudaSuccess) return err;
+    g_timing = TimingHook{nullptr, nullptr};
   }
   if (items.total_tiles > 0) {
     static thread_local int configured_device = -1;
@@ -791,9 +751,14 @@ cudaError_t launch_encode(const Items& items, void* ws_base, cudaStream_t stream
     if (g_timing.before) cudaEventRecord(g_timing.before, stream);
     err = launch_pdl(enc_main, dim3(grid), dim3(kEncThreads), smem, stream, items, ws);
     if (g_timing.after) cudaEventRecord(g_timing.after, stream);
-    if (err != cudaSuccess) return err;
+    if (err != cudaSuccess) {
+      g_timing = hook;
+      return err;
+    }
   }
-  return launch_place(items, ws, stream, dev);
+  err = launch_place(items, ws, stream, dev);
+  g_timing = hook;
+  return err;
 }
 
 cudaError_t launch_place(const Items& items, const EncWs& ws, cudaStream_t stream, const DeviceInfo& dev) {

@@ -114,6 +114,7 @@ __global__ void ce_prepare(const __grid_constant__ Items items, CeWs ws) {
     if (!(enc_bad & SZ_FLAG_SIZE) && layout_of(it.n, 0).off_cid > it.capacity) enc_bad |= SZ_FLAG_CAPACITY;
     ws.cal.done[i] = cal_bad ? kItemInvalid : 0u;
     ws.enc.item_flags[i] = enc_bad;
+    if (ws.enc.small && it.n > kSmallMax) atomicOr(&ws.enc.hdr->large, 1u);
     ws.enc.item_esc[i] = 0;
     ws.enc.seg_ticket[i] = 0;
     ws.ready[i] = 0;
@@ -146,8 +147,9 @@ __global__ void __launch_bounds__(kCeThreads, kCeCtasPerSm) ce_main(const __grid
   CeShared& sh = *reinterpret_cast<CeShared*>(smem_raw);
   const uint32_t tid = threadIdx.x;
   const uint32_t warp = tid >> 5, lane = tid & 31u;
-  // an inconsistent item table (flagged by ce_prepare) is never walked
-  if (ws.cal.hdr->flags & SZ_FLAG_ITEMS) return;
+  // an inconsistent item table (flagged by ce_prepare) is never walked; a
+  // table of small tensors is done by small_main
+  if ((ws.cal.hdr->flags & SZ_FLAG_ITEMS) || (ws.enc.small && !ws.enc.hdr->large)) return;
 
   for (uint32_t w = tid; w < 256 * 32; w += kCeThreads) sh.cnt[w] = 0;
   if (tid == 0) {
@@ -469,6 +471,7 @@ __global__ void __launch_bounds__(kCeThreads, kCeCtasPerSm) ce_main(const __grid
 
 cudaError_t launch_calibrate_encode(const Items& items, void* ws_base, cudaStream_t stream, const DeviceInfo& dev) {
   CeWs ws = ce_ws(ws_base, items.count, items.total_tiles);
+  ws.enc.small = small_route(items);
   cudaError_t err = cudaMemsetAsync(ws_base, 0, sizeof(WsHeader), stream);
   if (err != cudaSuccess) return err;
   {
@@ -479,6 +482,14 @@ cudaError_t launch_calibrate_encode(const Items& items, void* ws_base, cudaStrea
     const unsigned grid = unsigned(blocks < 2048 ? (blocks ? blocks : 1) : 2048);
     ce_prepare<<<grid, 256, 0, stream>>>(items, ws);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  }
+  // tables of small tensors: whole tensors in shared memory, each read once,
+  // one CTA per SM (the general kernels below then return at once, unless a
+  // tensor is too large)
+  TimingHook hook = g_timing;
+  if (ws.enc.small) {
+    if ((err = launch_small(items, ws.enc, ws.cal.done, stream, dev)) != cudaSuccess) return err;
+    g_timing = TimingHook{nullptr, nullptr};
   }
   if (items.total_tiles > 0) {
     static thread_local int configured_device = -1;
@@ -502,9 +513,14 @@ cudaError_t launch_calibrate_encode(const Items& items, void* ws_base, cudaStrea
     err = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(ce_main), dim3(grid), dim3(kCeThreads), args,
                                       smem, stream);
     if (g_timing.after) cudaEventRecord(g_timing.after, stream);
-    if (err != cudaSuccess) return err;
+    if (err != cudaSuccess) {
+      g_timing = hook;
+      return err;
+    }
   }
-  return launch_place(items, ws.enc, stream, dev);
+  err = launch_place(items, ws.enc, stream, dev);
+  g_timing = hook;
+  return err;
 }
 
 }  // namespace sz

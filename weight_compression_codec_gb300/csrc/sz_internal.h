@@ -35,6 +35,14 @@ cudaError_t launch_decode_inplace(const Items& items, void* ws, cudaStream_t str
 cudaError_t launch_calibrate_encode(const Items& items, void* ws, cudaStream_t stream, const DeviceInfo& dev);
 // escape placement, pads and metas after an encode pass (enc_place)
 cudaError_t launch_place(const Items& items, const EncWs& ws, cudaStream_t stream, const DeviceInfo& dev);
+// Small-tensor route: true for a table whose tensors average at most two
+// tiles.  launch_small runs small_main over the table after the prepare pass
+// (calibrate + encode when cal_done, the count pass's validity marks, is
+// given; encode alone otherwise); it does the work only if the prepare pass
+// found no tensor larger than kSmallMax.
+bool small_route(const Items& items);
+cudaError_t launch_small(const Items& items, const EncWs& ws, const uint32_t* cal_done, cudaStream_t stream,
+                         const DeviceInfo& dev);
 
 // Launches `kernel` on `stream` as a programmatic dependent of the kernel
 // before it: it may be scheduled while that kernel drains, and waits for it

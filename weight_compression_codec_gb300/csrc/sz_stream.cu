@@ -9,9 +9,11 @@
 // the halves apart.  Payloads that lie back to back in host memory (at most
 // 255 bytes apart, as in a packed shard blob) go in one copy per run.  The
 // metas (host copies, as a manifest holds them) and the per-group item
-// tables go to the device in one copy per call, through one of two pinned
-// host buffers kept per device: a copy from pageable memory may wait for the
-// stream, which would stall the pipeline between calls.
+// tables go to the device in one copy per call, through a pinned host buffer
+// of the caller's: a copy from pageable memory may wait for the stream, which
+// would stall the pipeline between calls.  The call allocates nothing; its
+// three events are created per call and released as soon as their work is
+// done.
 #include <cstring>
 #include <vector>
 
@@ -99,42 +101,35 @@ uint64_t scratch_bytes(uint32_t count, const Plan& plan) {
          plan.max_ws;
 }
 
-// Two pinned host buffers per device for the metas and tables of a call; a
-// buffer is reused once the copy out of it (two calls back) has completed.
-struct Upload {
-  void* buf[2] = {nullptr, nullptr};
-  uint64_t cap[2] = {0, 0};
-  cudaEvent_t done[2] = {nullptr, nullptr};
-  bool pending[2] = {false, false};
-  int next = 0;
-};
-
-// the pinned buffer of this call, at least `bytes` long, free to overwrite
-int upload_buffer(Upload& up, uint64_t bytes, int* slot) {
-  const int k = up.next;
-  up.next ^= 1;
-  if (up.done[k] == nullptr && cudaEventCreateWithFlags(&up.done[k], cudaEventDisableTiming) != cudaSuccess)
-    return SZ_ERR_CUDA;
-  if (up.pending[k]) {
-    if (cudaEventSynchronize(up.done[k]) != cudaSuccess) return SZ_ERR_CUDA;
-    up.pending[k] = false;
-  }
-  if (up.cap[k] < bytes) {
-    if (up.buf[k] != nullptr && cudaFreeHost(up.buf[k]) != cudaSuccess) return SZ_ERR_CUDA;
-    up.buf[k] = nullptr;
-    up.cap[k] = 0;
-    const uint64_t cap = round_up256(bytes + bytes / 4);
-    if (cudaHostAlloc(&up.buf[k], cap, cudaHostAllocDefault) != cudaSuccess) return SZ_ERR_CUDA;
-    up.cap[k] = cap;
-  }
-  *slot = k;
-  return SZ_OK;
+// bytes of the metas and tables as uploaded (and as laid out in the scratch)
+uint64_t upload_size(uint32_t count) {
+  return round_up256(uint64_t(count) * sizeof(sz_meta)) + uint64_t(count) * sizeof(sz_item);
 }
+
+// Events of one call, destroyed on every way out (a recorded event is
+// released by the runtime once its work has completed).
+struct CallEvents {
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  ~CallEvents() {
+    for (cudaEvent_t e : ev)
+      if (e != nullptr) cudaEventDestroy(e);
+  }
+  bool create() {
+    for (cudaEvent_t& e : ev)
+      if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return false;
+    return true;
+  }
+};
 
 }  // namespace
 }  // namespace sz
 
 using namespace sz;
+
+SZ_API size_t sz_decode_many_host_upload_bytes(uint32_t count) {
+  if (count == 0 || count > SZ_MANY_MAX_ITEMS) return 0;
+  return size_t(upload_size(count));
+}
 
 SZ_API size_t sz_decode_many_host_flags_offset(uint32_t count) {
   return size_t(round_up256(uint64_t(count) * sizeof(sz_meta)) + round_up256(uint64_t(count) * sizeof(sz_item)));
@@ -149,35 +144,35 @@ SZ_API size_t sz_decode_many_host_scratch_bytes(const sz_item* h_items, const sz
 }
 
 SZ_API int sz_decode_many_host(const sz_item* h_items, const sz_meta* h_metas, uint32_t count, void* d_staging,
-                               uint64_t staging_bytes, void* d_scratch, size_t scratch_size, sz_stream stream,
-                               sz_stream copy_stream) {
+                               uint64_t staging_bytes, void* d_scratch, size_t scratch_size, void* h_upload,
+                               size_t upload_bytes, sz_stream stream, sz_stream copy_stream) {
   if (h_items == nullptr || h_metas == nullptr || count == 0 || count > SZ_MANY_MAX_ITEMS) return SZ_ERR_ARG;
-  if (d_staging == nullptr || d_scratch == nullptr) return SZ_ERR_ARG;
+  if (d_staging == nullptr || d_scratch == nullptr || h_upload == nullptr) return SZ_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(d_staging) & 255) || (reinterpret_cast<uintptr_t>(d_scratch) & 255))
     return SZ_ERR_ALIGN;
   const uint64_t half = (staging_bytes / 2) & ~uint64_t(255);
   Plan plan;
   if (int rc = make_plan(h_items, h_metas, count, half, &plan)) return rc;
-  if (scratch_size < scratch_bytes(count, plan)) return SZ_ERR_WORKSPACE;
+  if (scratch_size < scratch_bytes(count, plan) || upload_bytes < upload_size(count)) return SZ_ERR_WORKSPACE;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, h_upload) != cudaSuccess) {
+    cudaGetLastError();  // clear it: an unknown pointer is the caller's error
+    return SZ_ERR_ARG;
+  }
+  if (attr.type != cudaMemoryTypeHost) return SZ_ERR_ARG;  // pinned host memory only
   DeviceInfo dev;
   if (device_info(&dev) != cudaSuccess) return SZ_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(copy_stream);
-  if (dev.device < 0 || dev.device >= 64) return SZ_ERR_CUDA;
   char* scratch = static_cast<char*>(d_scratch);
   const uint64_t tables_off = round_up256(uint64_t(count) * sizeof(sz_meta));
-  const uint64_t upload_bytes = tables_off + uint64_t(count) * sizeof(sz_item);
   sz_meta* d_metas = reinterpret_cast<sz_meta*>(scratch);
   sz_item* d_tables = reinterpret_cast<sz_item*>(scratch + tables_off);
   void* d_ws = scratch + tables_off + round_up256(uint64_t(count) * sizeof(sz_item));
   uint8_t* stage[2] = {static_cast<uint8_t*>(d_staging), static_cast<uint8_t*>(d_staging) + half};
 
-  // metas and tables, laid out as in the scratch, in a pinned host buffer
-  static thread_local Upload uploads[64];
-  Upload& up = uploads[dev.device];
-  int slot = 0;
-  if (int rc = upload_buffer(up, upload_bytes, &slot)) return rc;
-  char* pinned = static_cast<char*>(up.buf[slot]);
+  // metas and tables, laid out as in the scratch, in the caller's pinned buffer
+  char* pinned = static_cast<char*>(h_upload);
   std::memcpy(pinned, h_metas, uint64_t(count) * sizeof(sz_meta));
   sz_item* tables = reinterpret_cast<sz_item*>(pinned + tables_off);
   std::memcpy(tables, h_items, uint64_t(count) * sizeof(sz_item));
@@ -194,16 +189,11 @@ SZ_API int sz_decode_many_host(const sz_item* h_items, const sz_meta* h_metas, u
     }
   }
   // events: copy of group j done; decode of the group last in each half done
-  static thread_local cudaEvent_t events[64][3] = {};  // per device, created on first use
-  cudaEvent_t* ev = events[dev.device];
-  for (int k = 0; k < 3; ++k) {
-    if (ev[k] == nullptr && cudaEventCreateWithFlags(&ev[k], cudaEventDisableTiming) != cudaSuccess)
-      return SZ_ERR_CUDA;
-  }
-  cudaEvent_t copied = ev[0], decoded[2] = {ev[1], ev[2]};
-  cudaError_t e = cudaMemcpyAsync(d_metas, pinned, upload_bytes, cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess || (e = cudaEventRecord(up.done[slot], s)) != cudaSuccess) return SZ_ERR_CUDA;
-  up.pending[slot] = true;
+  CallEvents events;
+  if (!events.create()) return SZ_ERR_CUDA;
+  cudaEvent_t copied = events.ev[0], decoded[2] = {events.ev[1], events.ev[2]};
+  cudaError_t e = cudaMemcpyAsync(d_metas, pinned, upload_size(count), cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return SZ_ERR_CUDA;
   // nothing of this call starts on the copy stream before the caller's
   // earlier work on `stream` (e.g. the staging buffer's previous use)
   if ((e = cudaEventRecord(decoded[0], s)) != cudaSuccess) return SZ_ERR_CUDA;
