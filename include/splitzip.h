@@ -32,9 +32,9 @@
  * h_* (host memory).  The library allocates nothing: the caller owns every
  * buffer, including the workspace, whose size the *_workspace_bytes queries
  * give.  All compute calls are asynchronous on `stream` (a cudaStream_t; NULL
- * is the legacy default stream), never synchronise, and may be captured in a
- * CUDA graph.  A workspace may be reused by calls ordered on one stream; calls
- * that may overlap on the GPU need separate workspaces.
+ * is the legacy default stream) and never synchronise.  A workspace may be
+ * reused by calls ordered on one stream; calls that may overlap on the GPU
+ * need separate workspaces.
  *
  * Alignment.  Every BF16 input/output and payload pointer must be 16-byte
  * aligned; codebook, meta and item-table pointers 16-byte aligned; workspaces
@@ -223,7 +223,13 @@ SZ_API int sz_decode(const uint8_t* d_payload, uint64_t payload_bytes, const sz_
  * any size, each with its own codebook and meta, described by the device
  * item table d_items (tile_begin filled as sz_items_prepare does;
  * total_tiles = its total).  Work is spread over all SMs tile by tile, so a
- * few large tensors and many mid-size ones run equally well.
+ * few large tensors and many mid-size ones run equally well.  A table whose
+ * tensors average at most two tiles (16,384 elements, e.g. the blocks of a
+ * paged KV cache) is encoded whole-tensor by whole-tensor in shared memory
+ * instead, reading each input once and staging nothing; if one of its
+ * tensors is larger than two tiles the call falls back, inside the same
+ * launches, to the tile-by-tile kernels.  Either way the results are the
+ * same bytes.
  *   calibrate: reads x, n, tile_begin; writes *codebook.
  *   encode:    reads x, n, codebook, payload, capacity, tile_begin; writes payload, *meta.
  *   decode:    reads payload (capacity readable bytes), meta, codebook, n, tile_begin; writes out.
@@ -367,16 +373,19 @@ SZ_API int sz_encode_gated_many(const sz_item* d_items, uint32_t count, uint64_t
  * then encode_torch + assemble_payload with the codebook it returns) in one
  * call that reads each input from its memory once: the tensors are taken in
  * groups of about 32 MiB, each group counted and, two groups later, encoded
- * while it is still in L2.  The codebooks, payloads, metas and flags are
+ * while it is still in L2; a table of small tensors (as in sz_encode_many)
+ * is counted, ranked and encoded one whole tensor at a time in shared
+ * memory.  The codebooks, payloads, metas and flags are
  * those of sz_calibrate (or sz_calibrate_many) followed by sz_encode
  * (sz_encode_many), byte for byte; the table fields read and written are the
  * union of the two calls'.  The main kernel is a cooperative launch (all its
  * CTAs resident at once); SZ_ERR_CUDA if the device cannot run it.
- * On a GB300 with the input in HBM the two separate calls are faster (the
- * split-and-pack pass is bound by instruction issue, not by HBM, so the saved
- * read does not shorten it, and the per-group codebook hand-off costs time);
- * this call halves the input traffic, which matters where reading the input
- * is the bottleneck.  The pages calibrate offline, one tensor at a time, and
+ * On a GB300 with the input in HBM the two separate calls are faster for
+ * large tensors (the split-and-pack pass is bound by instruction issue, not
+ * by HBM, so the saved read does not shorten it, and the per-group codebook
+ * hand-off costs time); for tables of small tensors this call is the faster
+ * one (8192 tensors of 16,384 elements: 161 against 171 us).  It halves the
+ * input traffic, which matters where reading the input is the bottleneck.  The pages calibrate offline, one tensor at a time, and
  * encode after a host round trip; this fusion has no counterpart there. */
 SZ_API int sz_calibrate_encode(const uint16_t* d_x, uint64_t n, sz_codebook* d_codebook,
                                uint8_t* d_payload, uint64_t capacity, sz_meta* d_meta,
@@ -402,8 +411,8 @@ SZ_API int sz_calibrate_encode_many(const sz_item* d_items, uint32_t count, uint
  *   d_flags: optional device pointer (4-byte aligned) that receives the
  *   call's SZ_FLAG_* word asynchronously (0 = no device-side problem).
  * The first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call before any stream
- * capture.  All calls on a device share the one array and each call starts
+ * device current) and caches it.  All calls on a device share the one array
+ * and each call starts
  * by resetting what it reads, but calls whose work may overlap on the GPU
  * (different streams without ordering) race on it: order them. */
 SZ_API int sz_decode_noalloc(const uint8_t* d_payload, uint64_t payload_bytes, const sz_meta* d_meta,
@@ -415,7 +424,8 @@ SZ_API int sz_decode_noalloc(const uint8_t* d_payload, uint64_t payload_bytes, c
 /* Timing hook: `before` and `after` are cudaEvent_t handles (or NULL to
  * clear).  While set, every compute call made by the calling host thread
  * records `before` on its stream just before its main kernel (the streaming
- * pass: cal_hist, enc_main, dec_flat or dec_inplace) and `after` just after it, so the
+ * pass: cal_hist, enc_main or small_main, ce_main or small_main, dec_flat or
+ * dec_inplace) and `after` just after it, so the
  * caller can time that kernel alone with cudaEventElapsedTime.  The events are
  * borrowed, never destroyed. */
 SZ_API int sz_set_timing_events(void* before, void* after);
