@@ -33,6 +33,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -321,12 +322,16 @@ KERNEL_SOURCES = {"cal_hist": ("sz_calibrate.cu", "sz_count.cuh"),
 
 def kernel_source_sha(kernel: str) -> str:
     """Hash of the sources a kernel is built from (its .cu file and the device
-    headers it includes, the shared device header and the ABI header): a
-    recorded ncu traffic figure is only reported while this matches."""
+    headers it includes, the shared device header and the ABI header), with
+    their comments removed: a recorded ncu traffic figure is only reported
+    while this matches, so any change to the code, but not to its comments,
+    invalidates it."""
     h = hashlib.sha256()
     for f in [CSRC / name for name in KERNEL_SOURCES[kernel]] + [
             CSRC / "sz_device.cuh", CSRC / "sz_internal.h", ROOT / "include" / "splitzip.h"]:
-        h.update(f.read_bytes())
+        text = re.sub(r"/\*.*?\*/", "", f.read_text(), flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(line.rstrip() for line in text.splitlines() if line.strip()).encode())
     return h.hexdigest()[:16]
 
 
