@@ -1455,6 +1455,30 @@ __device__ void prime_carry(const Items& items, uint64_t t0, uint32_t cur, uint3
   cache.tiles = tiles;
 }
 
+// find_item_warp with 8 probes a lane (256 a round), for the resolver's first
+// search, which lies on the path to the CTA's first tile: 8192 tensors take
+// two dependent rounds of loads instead of three.
+__device__ uint32_t find_item_wide(const Items& items, uint64_t tile, uint32_t lane) {
+  constexpr unsigned kAll = 0xFFFFFFFFu;
+  if (items.table == nullptr) return 0;
+  uint32_t lo = 0, hi = items.count;  // table[lo].tile_begin <= tile; the answer is in [lo, hi)
+  while (hi - lo > 32) {
+    const uint32_t step = (hi - lo + 255) / 256;
+    uint32_t c = 0;  // this lane's probes at or before `tile` (a prefix of them: the probes ascend)
+#pragma unroll
+    for (uint32_t k = 0; k < 8; ++k) {
+      const uint64_t p = uint64_t(lo) + uint64_t(lane * 8u + k) * step;
+      c += (p < hi && items.table[p].tile_begin <= tile) ? 1u : 0u;
+    }
+    const uint32_t total = __reduce_add_sync(kAll, c);  // probes 0 .. total-1 are at or before it
+    if (total) lo += (total - 1u) * step;                // probe 0 is lo itself unless the table is not consecutive
+    if (lo + step < hi) hi = lo + step;
+  }
+  const uint32_t p = lo + lane;
+  const uint32_t m = __ballot_sync(kAll, p < hi && items.table[p].tile_begin <= tile);
+  return m ? lo + (31u - __clz(m)) : lo;
+}
+
 // Out-of-place decode (sz_decode(_many)).  One CTA per SM owns a contiguous
 // range of tiles, cut into windows of kFlatWin tiles.  The resolver warp
 // resolves the windows in order (prime_carry for the first tile, then
@@ -1499,8 +1523,15 @@ __global__ void __launch_bounds__(kFlatThreads, 1) dec_flat(const __grid_constan
     if (t0 >= t1) return;
     RangeCarry carry;
     ItemCache& cache = sh.cache;
-    uint32_t cur = find_item_warp(items, t0, uint32_t(lane));
-    prime_carry(items, t0, cur, uint32_t(lane), carry, cache);
+    uint32_t cur = find_item_wide(items, t0, uint32_t(lane));
+    // a CTA whose first tile starts its tensor needs no carry: the first
+    // window finds its tensors and escape ranges itself
+    if (t0 != item_at(items, cur).tile_begin) {
+      prime_carry(items, t0, cur, uint32_t(lane), carry, cache);
+    } else {
+      carry = RangeCarry{kNoItem, 0u, 0u, 0.0f};
+      if (lane == 0) cache = ItemCache{};
+    }
     __syncwarp();
     for (uint32_t w = 0;; ++w) {
       const uint64_t first = t0 + uint64_t(w) * kFlatWin;
