@@ -25,6 +25,37 @@ __device__ inline void write_empty_codebook(sz_codebook* cb) {
   cb->coverage = 1.0;
 }
 
+// t / n correctly rounded (to nearest, ties to even) to an IEEE double, for
+// integers 0 <= t <= n < 2^31, in integer arithmetic -- the value a double
+// division t / n gives, at a fraction of the cost of FP64 work on this part.
+// Schoolbook long division: t is scaled by 2^s so that n <= T < 2n; the
+// quotient floor(T 2^53 / n) (54 bits: 53 for the significand, one to round
+// on) comes from two steps of 22 and 31 bits, and the last remainder tells
+// whether anything lies below the rounding bit.
+__device__ __forceinline__ double ratio_rn(uint32_t t, uint32_t n) {
+  if (t == 0) return 0.0;
+  if (t >= n) return 1.0;
+  int s = __clz(t) - __clz(n);  // t 2^s has the bit length of n
+  uint64_t T = uint64_t(t) << s;
+  if (T < n) {
+    T <<= 1;
+    ++s;
+  }
+  const uint64_t A = T << 22;                // < 2^54
+  const uint64_t q1 = A / n, r1 = A % n;     // q1 < 2^23
+  const uint64_t B = r1 << 31;               // < 2^62
+  const uint64_t q2 = B / n, r2 = B % n;     // q2 < 2^31
+  const uint64_t Q = (q1 << 31) | q2;        // floor(T 2^53 / n), in [2^53, 2^54)
+  uint64_t mant = Q >> 1;                    // in [2^52, 2^53)
+  if ((Q & 1u) && (r2 != 0 || (mant & 1u))) ++mant;
+  int e = -s;                                // t / n = mant 2^-52 2^e
+  if (mant == (1ull << 53)) {
+    mant >>= 1;
+    ++e;
+  }
+  return __longlong_as_double(static_cast<long long>((uint64_t(1023 + e) << 52) | (mant & ((1ull << 52) - 1u))));
+}
+
 // Ranks the 256 bins of histogram h (count desc, value asc) and writes the
 // codebook of `it`; run by one warp, lane l loading bins 8l .. 8l+7.  Only
 // non-zero bins take part: they are compacted in bin order as keys
@@ -76,7 +107,8 @@ __device__ inline void select_top16(const sz_item& it, const uint32_t* h, Select
     cb->reserved0 = 0;
     cb->top_count = top;
     cb->n = n;
-    cb->coverage = n ? double(top) / double(n) : 1.0;
+    // the division in integer arithmetic where it fits (FP64 is slow on this part)
+    cb->coverage = n == 0 ? 1.0 : (n < (1ull << 31) ? ratio_rn(uint32_t(top), uint32_t(n)) : double(top) / double(n));
   }
   __syncwarp();  // key, lut and dl are reused by the next select
 }

@@ -197,37 +197,6 @@ __device__ void small_emit(const uint16_t* xs, uint32_t c, const ChunkFlags& f, 
 static_assert(sizeof(SmallShared<true>) <= 227u * 1024u && sizeof(SmallShared<false>) <= 227u * 1024u,
               "one CTA's shared memory");
 
-// t / n correctly rounded (to nearest, ties to even) to an IEEE double, for
-// integers 0 <= t <= n < 2^31, in integer arithmetic -- the value a double
-// division t / n gives, at a fraction of the cost of FP64 work on this part.
-// Schoolbook long division: t is scaled by 2^s so that n <= T < 2n; the
-// quotient floor(T 2^53 / n) (54 bits: 53 for the significand, one to round
-// on) comes from two steps of 22 and 31 bits, and the last remainder tells
-// whether anything lies below the rounding bit.
-__device__ __forceinline__ double ratio_rn(uint32_t t, uint32_t n) {
-  if (t == 0) return 0.0;
-  if (t >= n) return 1.0;
-  int s = __clz(t) - __clz(n);  // t 2^s has the bit length of n
-  uint64_t T = uint64_t(t) << s;
-  if (T < n) {
-    T <<= 1;
-    ++s;
-  }
-  const uint64_t A = T << 22;                // < 2^54
-  const uint64_t q1 = A / n, r1 = A % n;     // q1 < 2^23
-  const uint64_t B = r1 << 31;               // < 2^62
-  const uint64_t q2 = B / n, r2 = B % n;     // q2 < 2^31
-  const uint64_t Q = (q1 << 31) | q2;        // floor(T 2^53 / n), in [2^53, 2^54)
-  uint64_t mant = Q >> 1;                    // in [2^52, 2^53)
-  if ((Q & 1u) && (r2 != 0 || (mant & 1u))) ++mant;
-  int e = -s;                                // t / n = mant 2^-52 2^e
-  if (mant == (1ull << 53)) {
-    mant >>= 1;
-    ++e;
-  }
-  return __longlong_as_double(static_cast<long long>((uint64_t(1023 + e) << 52) | (mant & ((1ull << 52) - 1u))));
-}
-
 // The producer's part of the CTA's tensors [j0, j1) (at most 32, released by
 // their groups): lane l writes the meta -- and, calibrated here, the
 // codebook's header -- of tensor j0 + l, so that the scalar work of 32
