@@ -131,7 +131,7 @@ def test_small_sizes_round_trip_and_layout(oracle, n):
     x = r.integers(0, 65536, size=n, dtype=np.uint16)
     cb = oracle.calibrate(x)
     payload, m = oracle.encode(x, cb)
-    # the benchmark spec size: the aligned sum of ceil(n/2) + n + 7 * n_esc; pads are below 4 bytes each
+    # the payload size: the aligned sum of ceil(n/2) + n + 7 * n_esc; pads are below 4 bytes each
     raw = (n + 1) // 2 + n + 7 * m.n_esc
     assert 0 <= m.comp_bytes - raw <= 3 + 3 + 3
     for off in (m.off_sm, m.off_cid, m.off_lpos, m.off_ev):
