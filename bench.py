@@ -643,10 +643,32 @@ def run_ours(args, world, rank, local):
         e2e_ms = a.elapsed_time(b) / ke
         assert all(torch.equal(ho, hi) for ho, hi in zip(host_out, host_in)), "e2e round trip"
         meta_bytes = sum(m.numel() for m in host_meta)
+        # the host link with both directions busy: the same bytes copied in
+        # and out at once, with no codec work (the bound e2e can approach)
+        link = []
+        for _ in range(3):
+            for st in (s_in, s_out):
+                st.wait_stream(torch.cuda.current_stream())
+            la, lb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            la.record(s_in)
+            s_out.wait_event(la)
+            for j in range(len(groups)):
+                with torch.cuda.stream(s_in):
+                    dev_in[j].copy_(host_in[j], non_blocking=True)
+                with torch.cuda.stream(s_out):
+                    host_out[j].copy_(dev_in[j], non_blocking=True)
+            s_in.wait_stream(s_out)
+            lb.record(s_in)
+            torch.cuda.synchronize()
+            link.append(la.elapsed_time(lb))
+        link_ms = float(np.median(link))
         e2e_ms = max_over_ranks(e2e_ms, world, dev)
         e2e = {"value": world * raw_bytes / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                "h2d_bytes_per_step": raw_bytes, "d2h_bytes_per_step": raw_bytes + meta_bytes,
                "ms_per_step": e2e_ms, "groups": len(groups),
+               "link_both_ways_gbs": 2 * raw_bytes / (link_ms * 1e-3) / 1e9,
+               "link_bound": world * raw_bytes / (link_ms * 1e-3) / 1e9,
+               "vs_link_bound": link_ms / e2e_ms,
                "path": "pinned host -> device -> calibrate/encode/decode -> pinned host, 3 streams"}
 
     # decode with the payloads in pinned host memory (the pages' deployment:
