@@ -318,7 +318,8 @@ KERNEL_SOURCES = {"cal_hist": ("sz_calibrate.cu", "sz_count.cuh"),
                   "small_main": ("sz_small.cu", "sz_chunk.cuh", "sz_count.cuh"),
                   "small_main_fused": ("sz_small.cu", "sz_chunk.cuh", "sz_count.cuh"),
                   "ce_main": ("sz_fused.cu", "sz_chunk.cuh", "sz_count.cuh"),
-                  "dec_flat": ("sz_decode.cu",), "dec_inplace": ("sz_decode.cu",), "dip_stash": ("sz_decode.cu",)}
+                  "dec_flat": ("sz_decode.cu",), "dec_small": ("sz_decode.cu",), "dec_inplace": ("sz_decode.cu",),
+                  "dip_stash": ("sz_decode.cu",)}
 
 
 def kernel_source_sha(kernel: str) -> str:
@@ -465,16 +466,18 @@ def measure(arrays: list[np.ndarray], K: int, warmup: int, dev, gpu_id: str, wor
     # algorithmic bytes of each streaming kernel: cal_hist reads x; enc_main
     # reads x and writes the pk and sm sections (the escape streams are
     # written by enc_place), or, for a table of small tensors, small_main
-    # reads x and writes the whole payload; dec_flat reads the payload and
-    # writes x; the fused call's main kernel reads x from HBM once and writes
-    # the payload (small_main) or its pk and sm sections (ce_main)
+    # reads x and writes the whole payload; dec_flat (dec_small for a table of
+    # small tensors) reads the payload and writes x; the fused call's main
+    # kernel reads x from HBM once and writes the payload (small_main) or its
+    # pk and sm sections (ce_main)
     dense_bytes = sum(m.off_cid for m in metas)
     small = small_route([m.n for m in metas])
     alg = {"calibrate": raw_bytes, "encode": raw_bytes + (comp_total if small else dense_bytes),
            "decode": comp_total + raw_bytes, "calibrate_encode": raw_bytes + (comp_total if small else dense_bytes)}
     alg_ops = {"calibrate": raw_bytes, "encode": raw_bytes + comp_total, "decode": comp_total + raw_bytes,
                "calibrate_encode": raw_bytes + comp_total}
-    kname = {"calibrate": "cal_hist", "encode": "small_main" if small else "enc_main", "decode": "dec_flat",
+    kname = {"calibrate": "cal_hist", "encode": "small_main" if small else "enc_main",
+             "decode": "dec_small" if small else "dec_flat",
              "calibrate_encode": "small_main_fused" if small else "ce_main"}
     kernels = {}
     for k in ms:

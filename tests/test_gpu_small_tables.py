@@ -1,9 +1,10 @@
 """Tables of small tensors (at most two tiles on average, such as the blocks of a
-paged KV cache) take the single-read path of sz_encode_many and
-sz_calibrate_encode_many: a whole tensor held in shared memory.  Its results
-are checked here against the CPU oracle tensor by tensor at ragged sizes,
-escape-heavy inputs, flagged items, the coverage gate, and a table whose
-one large tensor sends the call back to the general kernels."""
+paged KV cache) take the whole-tensor paths of sz_encode_many,
+sz_calibrate_encode_many and sz_decode_many: each tensor held in shared
+memory.  Their results are checked here against the CPU oracle tensor by
+tensor at ragged sizes, escape-heavy inputs, flagged items, the coverage
+gate, and tables with a tensor the whole-tensor kernels leave to the tile
+kernels."""
 from __future__ import annotations
 
 import numpy as np
@@ -15,6 +16,7 @@ import weight_compression_codec_gb300 as sz
 from weight_compression_codec_gb300 import binding as B
 from weight_compression_codec_gb300 import inputs
 
+import gpu_util
 from gpu_util import DEV, check_codebook, to_dev, to_np_u16
 
 pytestmark = pytest.mark.gpu
@@ -198,3 +200,86 @@ def test_small_table_gate_matches_the_oracle(gate):
     if gate > 0:
         assert any(oracle.gated(c.coverage, gate) for c in cbs) and not all(oracle.gated(c.coverage, gate)
                                                                            for c in cbs)
+
+
+def _decode_table(b: "sz.Batch", fill: int = 7) -> int:
+    b.out.view(torch.int16).fill_(fill)
+    ws = sz.Workspace(DEV)
+    sz.sz_decode_many(b.table, workspace=ws)
+    flags = sz.sz_workspace_flags(ws.buf)
+    torch.cuda.synchronize()
+    return flags
+
+
+def test_small_table_decode_of_the_oracle_payloads():
+    """Payloads written by the CPU oracle (not by this library), decoded as a
+    table of small tensors: ragged sizes, escapes, and tensors whose payload
+    is too large for the whole-tensor kernel (left to the tile kernel)."""
+    arrays = _ragged_table() + [inputs.edge_case(SMALL_MAX, seed=990), inputs.edge_case(9000, seed=991)]
+    assert _small_routed(arrays)
+    b = sz.Batch([to_dev(a) for a in arrays])
+    for i, x in enumerate(arrays):
+        ocb = oracle.calibrate(x)
+        opay, om = oracle.encode(x, ocb)
+        b.codebooks[i].copy_(torch.frombuffer(bytearray(gpu_util.oracle_codebook_bytes(ocb, x.size)),
+                                              dtype=torch.uint8).to(DEV))
+        b.metas[i].copy_(torch.frombuffer(bytearray(sz.meta_to_bytes(om)), dtype=torch.uint8).to(DEV))
+        if om.comp_bytes:
+            b.payload_view(i, om.comp_bytes).copy_(torch.from_numpy(opay).to(DEV))
+    assert _decode_table(b) == 0
+    for i, x in enumerate(arrays):
+        assert np.array_equal(to_np_u16(b.out_view(i)), x), f"tensor {i} (n={x.size})"
+
+
+def test_small_table_decode_with_one_large_tensor_and_flags():
+    arrays = [inputs.gaussian(40_000, 0.02, seed=992)] + [inputs.gaussian(5000 + 7 * k, 0.5, seed=1000 + k)
+                                                           for k in range(20)]
+    assert _small_routed(arrays) and arrays[0].size > SMALL_MAX
+    b = sz.Batch([to_dev(a) for a in arrays])
+    sz.sz_calibrate_encode_many(b.table)
+    torch.cuda.synchronize()
+    assert _decode_table(b) == 0
+    for i, x in enumerate(arrays):
+        assert np.array_equal(to_np_u16(b.out_view(i)), x), f"tensor {i}"
+    # a meta that disagrees with the layout: that tensor is flagged and left untouched, the rest decoded
+    import dataclasses
+
+    m3 = sz.meta_from_bytes(b.metas[3].cpu().numpy())
+    b.metas[3].copy_(torch.frombuffer(bytearray(sz.meta_to_bytes(dataclasses.replace(m3, off_sm=m3.off_sm + 4))),
+                                      dtype=torch.uint8).to(DEV))
+    flags = _decode_table(b)
+    assert flags & B.SZ_FLAG_META
+    assert bool(torch.all(b.out_view(3).view(torch.int16) == 7))
+    for i, x in enumerate(arrays):
+        if i != 3:
+            assert np.array_equal(to_np_u16(b.out_view(i)), x), f"tensor {i}"
+
+
+def test_small_table_decode_flags_an_escape_outside_its_chunk():
+    arrays = [inputs.edge_case(2000, seed=993 + k) for k in range(3)]
+    assert _small_routed(arrays)
+    b = sz.Batch([to_dev(a) for a in arrays])
+    sz.sz_calibrate_encode_many(b.table)
+    torch.cuda.synchronize()
+    m = sz.meta_from_bytes(b.metas[1].cpu().numpy())
+    assert m.n_esc > 0 and m.comp_bytes <= 26_624  # decoded whole (its payload fits a buffer)
+    lpos = b.payload_view(1, m.comp_bytes)[m.off_lpos:m.off_lpos + 2]
+    lpos.copy_(torch.tensor([0x00, 0x04], dtype=torch.uint8, device=DEV))  # local_pos 1024
+    flags = _decode_table(b)
+    assert flags & B.SZ_FLAG_ESCAPE
+    for i in (0, 2):
+        assert np.array_equal(to_np_u16(b.out_view(i)), arrays[i]), f"tensor {i}"
+
+
+def test_small_table_decode_leaves_gated_tensors_untouched():
+    arrays = [inputs.paged_kv_block(i) for i in range(10)] + [inputs.edge_case(6000, seed=996)]
+    assert _small_routed(arrays)
+    b = sz.Batch([to_dev(a) for a in arrays])
+    sz.sz_calibrate_many(b.table)
+    sz.sz_encode_gated_many(b.table, 0.99)
+    torch.cuda.synchronize()
+    assert sz.meta_from_bytes(b.metas[10].cpu().numpy()).status == B.SZ_META_GATED
+    assert _decode_table(b) == 0
+    assert bool(torch.all(b.out_view(10).view(torch.int16) == 7))
+    for i in range(10):
+        assert np.array_equal(to_np_u16(b.out_view(i)), arrays[i]), f"tensor {i}"

@@ -530,6 +530,13 @@ __device__ __forceinline__ void prefetch_count(const uint8_t* payload, uint64_t 
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a), "r"(uint32_t(b - a)) : "memory");
 }
 
+// Tensors dec_small decodes whole (their item checks passed): at most two
+// tiles, and a payload that fits one of its buffers.
+constexpr uint32_t kSdPay = 26624;  // payload bytes a dec_small buffer holds
+__device__ __forceinline__ bool small_fits(const sz_item& it) {
+  return it.n <= kSmallMax && it.meta->comp_bytes <= kSdPay;
+}
+
 // Out-of-place decode, resolver warp: lane l < len resolves tile first + l
 // into win[l]; all 32 lanes take part.
 //  * A window that continues the tensor of the last one (carry) takes the
@@ -599,6 +606,7 @@ __device__ void resolve_window(const Items& items, const DecWs& ws, WinOut* win,
       if (!(bad & SZ_FLAG_SIZE) && (mine < it.tile_begin || mine - it.tile_begin >= tiles_of(it.n))) bad |= SZ_FLAG_ITEMS;
     }
     ok = act && bad == 0;
+    if (ok && ws.small_done && small_fits(it)) ok = false;  // dec_small decoded it
     if (ok) {
       const sz_meta* mp = it.meta;
       lt = uint32_t(mine - it.tile_begin);
@@ -1517,6 +1525,10 @@ __global__ void __launch_bounds__(kFlatThreads, 1) dec_flat(const __grid_constan
   if (t1 > T) t1 = T;
   uint64_t t0 = uint64_t(blockIdx.x) * per;
   if (t0 > t1) t0 = t1;
+  if (ws.small_done) {
+    pdl_wait();  // dec_small's header bits
+    if (!ws.hdr->large) return;  // dec_small decoded every tensor
+  }
 
   if (warp == kFlatResolverWarp) {
     // ---------------------------------------------------------------- resolver warp
@@ -1526,7 +1538,8 @@ __global__ void __launch_bounds__(kFlatThreads, 1) dec_flat(const __grid_constan
     uint32_t cur = find_item_wide(items, t0, uint32_t(lane));
     // a CTA whose first tile starts its tensor needs no carry: the first
     // window finds its tensors and escape ranges itself
-    if (t0 != item_at(items, cur).tile_begin) {
+    const bool kept = !ws.small_done || item_problems(items, cur, false) != 0 || !small_fits(item_at(items, cur));
+    if (t0 != item_at(items, cur).tile_begin && kept) {
       prime_carry(items, t0, cur, uint32_t(lane), carry, cache);
     } else {
       carry = RangeCarry{kNoItem, 0u, 0u, 0.0f};
@@ -1603,6 +1616,214 @@ __global__ void __launch_bounds__(kFlatThreads, 1) dec_flat(const __grid_constan
                  1u + uint32_t(p), ws, StoreHandoff{nullptr, nullptr, nullptr});
 }
 
+// ---------------------------------------------------------------- small tensors
+// Out-of-place decode of tables of small tensors (sz_decode_many over
+// tensors of at most two tiles on average, e.g. the blocks of a paged KV
+// cache; the pages' decode_torch, tensor by tensor).  dec_flat's first tile
+// waits for a chain of dependent loads (tensor search, meta, chunk_id search)
+// before its first copy; here a tensor's whole payload (at most kSdPay
+// bytes) is copied into shared memory after one table read and one meta read,
+// and one group of 8 warps decodes it straight to HBM:
+//   * an evaluation warp checks the CTA's tensors 32 at a time (one lane
+//     each: item checks, meta, dec_lut) into a double-buffered table;
+//   * a copy warp copies each payload by TMA into a ring of kSdBufs buffers;
+//   * groups of 8 warps take the tensors in turn: each thread decodes 8
+//     elements per step (dec_lut in 4 registers) and stores 16 bytes; after a
+//     group barrier the escapes are written over their elements (sign and
+//     mantissa from the sm byte, exponent from esc_val), which is all an
+//     escape changes.
+// A tensor with more elements, or a larger payload, is left to dec_flat:
+// the header's `large` bit tells it to run.
+constexpr uint32_t kSdGroups = 3;
+constexpr uint32_t kSdGroupThreads = 256;
+constexpr uint32_t kSdEvalWarp = kSdGroups * 8;     // 24
+constexpr uint32_t kSdCopyWarp = kSdEvalWarp + 1;   // 25
+constexpr uint32_t kSdThreads = (kSdCopyWarp + 1) * 32;  // 832
+constexpr uint32_t kSdBufs = 8;
+constexpr uint32_t kSdBatch = 32;  // tensors per evaluation batch
+constexpr uint32_t kSdDecode = 0u, kSdSkip = 1u;
+
+struct SdInfo {  // one tensor, as the evaluation warp leaves it
+  const uint8_t* payload;
+  uint16_t* out;
+  uint32_t n, e, comp, off_sm, off_cid, off_lpos, off_ev;
+  uint32_t status;  // kSdDecode, or kSdSkip (bad, gated, empty, or left to dec_flat)
+  uint4 dec_lut;
+};
+static_assert(sizeof(SdInfo) == 64, "64 bytes");
+
+struct SdShared {
+  alignas(128) uint8_t pay[kSdBufs][kSdPay + 128];  // a tensor's payload (+ slack for over-reads of its last group)
+  SdInfo info[2][kSdBatch];
+  SdInfo slot[kSdBufs];   // the tensor of pay[b]
+  uint32_t slot_item[kSdBufs];
+  uint64_t full[kSdBufs], empty[kSdBufs];
+  uint64_t info_full[2], info_empty[2];
+};
+static_assert(sizeof(SdShared) <= 227u * 1024u, "one CTA per SM");
+
+__global__ void __launch_bounds__(kSdThreads, 1) dec_small(const __grid_constant__ Items items, DecWs ws) {
+  constexpr unsigned FULL = 0xFFFFFFFFu;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  SdShared& sh = *reinterpret_cast<SdShared*>(smem_raw);
+  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
+  pdl_trigger();  // dec_flat, launched after, waits for this grid before it reads the header
+  if (tid == 0) {
+    for (uint32_t b = 0; b < kSdBufs; ++b) {
+      mbar_init(&sh.full[b], 1 + 32);
+      mbar_init(&sh.empty[b], 8);
+    }
+    for (uint32_t h = 0; h < 2; ++h) {
+      mbar_init(&sh.info_full[h], 1);
+      mbar_init(&sh.info_empty[h], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint32_t G = gridDim.x;
+  const uint32_t K = blockIdx.x < items.count ? (items.count - 1u - blockIdx.x) / G + 1u : 0u;  // the CTA's tensors
+
+  if (warp == kSdEvalWarp) {
+    // ---------------------------------------------------------------- evaluation warp
+    for (uint32_t bt = 0; bt * kSdBatch < K; ++bt) {
+      const uint32_t h = bt & 1u;
+      if (bt >= 2 && !__all_sync(FULL, mbar_wait(&sh.info_empty[h], ((bt >> 1) - 1) & 1u))) {
+        if (lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+        return;
+      }
+      const uint32_t k = bt * kSdBatch + lane;
+      SdInfo inf{};
+      inf.status = kSdSkip;
+      if (k < K) {
+        const uint32_t i = blockIdx.x + k * G;
+        const uint32_t bad = item_problems(items, i, false);
+        const sz_item& it = item_at(items, i);
+        if (bad & ~kItemGated) {
+          set_flag(ws.hdr, bad & ~kItemGated);
+        } else if (!bad && it.n > 0) {
+          if (!small_fits(it)) {
+            atomicOr(&ws.hdr->large, 1u);  // dec_flat decodes it
+          } else {
+            const sz_meta* mp = it.meta;
+            inf.payload = it.payload;
+            inf.out = it.out;
+            inf.n = uint32_t(it.n);
+            inf.e = uint32_t(mp->n_esc);
+            inf.comp = uint32_t(mp->comp_bytes);
+            inf.off_sm = uint32_t(mp->off_sm);
+            inf.off_cid = uint32_t(mp->off_cid);
+            inf.off_lpos = uint32_t(mp->off_lpos);
+            inf.off_ev = uint32_t(mp->off_ev);
+            inf.dec_lut = *reinterpret_cast<const uint4*>(it.codebook->dec_lut);
+            inf.status = kSdDecode;
+          }
+        }
+      }
+      sh.info[h][lane] = inf;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.info_full[h]);
+    }
+    return;
+  }
+
+  if (warp == kSdCopyWarp) {
+    // ---------------------------------------------------------------- copy warp
+    // Tensor k into buffer k % kSdBufs once the group done with tensor
+    // k - kSdBufs has released it; after the K tensors, one end slot per group.
+    for (uint32_t k = 0; k < K + kSdGroups; ++k) {
+      const uint32_t b = k % kSdBufs;
+      if (k >= kSdBufs && !__all_sync(FULL, mbar_wait(&sh.empty[b], ((k / kSdBufs) - 1) & 1u))) {
+        if (lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+        return;
+      }
+      uint32_t bytes = 0;
+      const uint8_t* src = nullptr;
+      if (k < K) {
+        const uint32_t bt = k / kSdBatch, h = bt & 1u, j = k % kSdBatch;
+        if (j == 0 && !__all_sync(FULL, mbar_wait(&sh.info_full[h], (bt >> 1) & 1u))) {
+          if (lane == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+          return;
+        }
+        const SdInfo& inf = sh.info[h][j];
+        if (lane < 16) reinterpret_cast<uint32_t*>(&sh.slot[b])[lane] = reinterpret_cast<const uint32_t*>(&inf)[lane];
+        if (inf.status == kSdDecode) {
+          bytes = inf.comp;
+          src = inf.payload;
+        }
+        __syncwarp();
+        if (lane == 0 && (j + 1 == kSdBatch || k + 1 == K)) mbar_arrive(&sh.info_empty[h]);  // the batch is copied out
+      }
+      if (lane == 0) sh.slot_item[b] = k < K ? k : kNoItem;
+      __syncwarp();  // the slot is written before the barrier's arrivals
+      const uint32_t bulk = bytes & ~15u;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&sh.full[b], bulk);
+        if (bulk) bulk_g2s(sh.pay[b], src, bulk, &sh.full[b]);
+      } else if (lane == 1 && bytes > bulk) {
+        cp_async16_zfill(sh.pay[b] + bulk, src + bulk, bytes - bulk);
+      }
+      cp_async_mbar_arrive_noinc(&sh.full[b]);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ decoding groups
+  const uint32_t g = warp / 8u, gt = tid % kSdGroupThreads, bar_id = 1u + g;
+  bool bad_escape = false;
+  for (uint32_t k = g;; k += kSdGroups) {
+    const uint32_t b = k % kSdBufs;
+    const bool ok = mbar_wait(&sh.full[b], (k / kSdBufs) & 1u);
+    if (named_bar_red_or(bar_id, kSdGroupThreads, !ok)) {
+      if (gt == 0) set_flag(ws.hdr, SZ_FLAG_TIMEOUT);
+      break;
+    }
+    if (sh.slot_item[b] == kNoItem) break;
+    const SdInfo& sl = sh.slot[b];
+    if (sl.status == kSdDecode) {
+      const uint8_t* const pay = sh.pay[b];
+      const uint32_t n = sl.n, e = sl.e, off_sm = sl.off_sm;
+      uint16_t* const out = sl.out;
+      const uint4 dl = sl.dec_lut;
+      // dense decode, 8 elements a thread per step (the last group may read
+      // past the payload's end into the buffer's slack: those lanes' values
+      // beyond n are not stored)
+      for (uint32_t q = gt; 8u * q < n; q += kSdGroupThreads) {
+        const uint32_t c8 = *reinterpret_cast<const uint32_t*>(pay + 4u * q);
+        const uint32_t s_lo = *reinterpret_cast<const uint32_t*>(pay + off_sm + 8u * q);
+        const uint32_t s_hi = *reinterpret_cast<const uint32_t*>(pay + off_sm + 8u * q + 4u);
+        const uint2 lo = decode4(c8 & 0xFFFFu, s_lo, dl.x, dl.y, dl.z, dl.w);
+        const uint2 hi = decode4(c8 >> 16, s_hi, dl.x, dl.y, dl.z, dl.w);
+        if (8u * q + 8u <= n) {
+          *reinterpret_cast<uint4*>(out + 8u * q) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        } else {
+          for (uint32_t r = 0; 8u * q + r < n; ++r) {
+            const uint32_t w = r < 2u ? lo.x : (r < 4u ? lo.y : (r < 6u ? hi.x : hi.y));
+            out[8u * q + r] = uint16_t(w >> (16u * (r & 1u)));
+          }
+        }
+      }
+      // the escapes over their elements (after every dense store of the group)
+      named_bar_sync(bar_id, kSdGroupThreads);
+      const uint32_t chunks = (n + kChunk - 1u) / kChunk;
+      for (uint32_t j = gt; j < e; j += kSdGroupThreads) {
+        const uint32_t c = *reinterpret_cast<const uint32_t*>(pay + sl.off_cid + 4u * j);
+        const uint32_t lp = *reinterpret_cast<const uint16_t*>(pay + sl.off_lpos + 2u * j);
+        const uint32_t ev = pay[sl.off_ev + j];
+        const uint32_t pos = c * kChunk + lp;
+        if (c < chunks && lp < kChunk && pos < n) {
+          const uint32_t sm = pay[off_sm + pos];
+          out[pos] = uint16_t(((sm & 0x80u) << 8) | (ev << 7) | (sm & 0x7Fu));
+        } else {
+          bad_escape = true;
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty[b]);  // this warp is done with pay[b] and slot[b]
+  }
+  if (__any_sync(FULL, bad_escape) && lane == 0) set_flag(ws.hdr, SZ_FLAG_ESCAPE);
+}
+
 }  // namespace
 
 namespace {
@@ -1650,6 +1871,25 @@ cudaError_t launch_decode(const Items& items, void* ws_base, cudaStream_t stream
   if (err != cudaSuccess) return err;
   const uint64_t cap = uint64_t(dev.num_sms);  // one CTA per SM: its two pipelines share the SM's tiles
   const unsigned grid = unsigned(items.total_tiles < cap ? items.total_tiles : cap);
+  if (small_route(items)) {
+    // tables of small tensors: dec_small decodes what fits it, then dec_flat
+    // (programmatic dependent launch) returns at once unless it left a tensor
+    static thread_local int configured_small = -1, per_sm_small = 1;
+    err = configure(reinterpret_cast<const void*>(dec_small), sizeof(SdShared), kSdThreads, dev.device,
+                    &configured_small, &per_sm_small);
+    if (err != cudaSuccess) return err;
+    DecWs ws = dec_ws(ws_base);
+    if (!clear_header && (err = cudaMemsetAsync(&ws.hdr->large, 0, sizeof(uint32_t), stream)) != cudaSuccess)
+      return err;
+    const unsigned sgrid = unsigned(items.count < cap ? items.count : cap);
+    if (g_timing.before) cudaEventRecord(g_timing.before, stream);
+    dec_small<<<sgrid, kSdThreads, sizeof(SdShared), stream>>>(items, ws);
+    err = cudaGetLastError();
+    if (g_timing.after) cudaEventRecord(g_timing.after, stream);
+    if (err != cudaSuccess) return err;
+    ws.small_done = true;
+    return launch_pdl(dec_flat, dim3(grid), dim3(kFlatThreads), smem, stream, items, ws);
+  }
   if (g_timing.before) cudaEventRecord(g_timing.before, stream);
   dec_flat<<<grid, kFlatThreads, smem, stream>>>(items, dec_ws(ws_base));
   err = cudaGetLastError();

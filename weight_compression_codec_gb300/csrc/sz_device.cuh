@@ -227,6 +227,7 @@ struct DecWs {
   uint32_t* tile_item;
   uint32_t* read_done;  // in-place decode: per tile, its in-place input has been read
   uint8_t* stash;       // in-place decode: the bytes copied aside
+  bool small_done;      // out of place: dec_small ran first; dec_flat takes only what it left
 };
 __host__ __device__ inline uint64_t prep_ws_bytes(uint32_t count, uint64_t tiles) {
   return 256 + round_up256(uint64_t(count) * 4) + round_up256(tiles * 8) + tile_map_bytes(dec_uses_tile_map(count), tiles);
@@ -243,6 +244,7 @@ __host__ __device__ inline DecWs prep_ws(void* base, uint32_t count, uint64_t ti
   w.tile_item = dec_uses_tile_map(count) ? reinterpret_cast<uint32_t*>(p) : nullptr;
   w.read_done = nullptr;
   w.stash = nullptr;
+  w.small_done = false;
   return w;
 }
 // the out-of-place decode's view of its workspace: the header alone
@@ -254,6 +256,7 @@ __host__ __device__ inline DecWs dec_ws(void* base) {
   w.tile_item = nullptr;
   w.read_done = nullptr;
   w.stash = nullptr;
+  w.small_done = false;
   return w;
 }
 
