@@ -6,8 +6,9 @@
 // once and nothing is staged.
 //
 // One CTA per SM: a producer warp copies the CTA's tensors (tensors b,
-// b + G, b + 2G, ... of the G CTAs) with their table entries -- and, encoding
-// alone, their codebooks -- into a ring of whole-tensor buffers by TMA;
+// b + G, b + 2G, ... of the G CTAs) with their table entries (fetched four
+// tensors ahead, one load per lane) -- and, encoding alone, their codebooks
+// -- into a ring of whole-tensor buffers by TMA;
 // groups of 8 warps (two calibrating, three encoding alone) take the tensors
 // in turn (group g of G' the tensors k = g, g + G', ... of the CTA), each
 // with its own counters and barrier, so one group's barriers and serial
@@ -22,8 +23,9 @@
 //   3. after one group barrier every chunk's escape count is known, so each
 //      warp writes its chunks' chunk_id / local_pos / esc_val at their final
 //      offsets -- in element order, as the pages' encode_torch lists them;
-//   4. the pads; the buffer goes back to the producer, which then writes the
-//      meta (and, calibrating, the codebook's header).
+//   4. the pads; the buffer goes back to the producer, which writes the
+//      metas (and, calibrating, the codebooks' headers) 32 tensors at a
+//      time, one lane each, so that their scalar work runs side by side.
 // The output is byte for byte that of the general kernels (enc_main,
 // enc_place, enc_regen; cal_hist; ce_main).
 //
