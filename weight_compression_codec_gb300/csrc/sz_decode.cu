@@ -37,6 +37,8 @@
 //                everything else in place (three phases, see ip_phases), each
 //                tile storing once the tiles whose payload bytes lie under it
 //                have read them.
+#include <cstddef>
+
 #include "sz_count.cuh"
 #include "sz_internal.h"
 
@@ -46,7 +48,7 @@ namespace {
 constexpr int kDecStages = 4;
 constexpr int kDecConsumerWarps = 8;
 constexpr int kDecConsumers = kDecConsumerWarps * 32;
-constexpr uint32_t kEcap = 1024;  // escapes per stage; a tile with more is sent as several stages
+constexpr uint32_t kEcap = 1024;  // escapes in a tile's first stage; a tile with more is sent as several stages
 constexpr uint32_t kRangeInvalid = 0xFFFFFFFFu;
 // kStageCont: escapes only, continuing the previous stage's tile;
 // kStageMore: further escape stages of this tile follow.
@@ -84,6 +86,17 @@ struct __align__(128) DecStage {
   uint4 dep;      // in-place decode: tiles (local indices) [x, y] and [z, w] to wait for ...
   uint2 dep2;     // ... and [x, y]
 };
+
+// A tile's further stages carry escapes only: their chunk_id, local_pos and
+// esc_val slices fill the whole stage from pk on (kEcapCont of them, each
+// array with 32 bytes of slack for the aligned copy and its ragged end), so a
+// tile of 6,400 escapes takes three stages instead of seven.
+constexpr uint32_t kEcapCont = 2688;
+constexpr uint32_t kContLpos = (4u * kEcapCont + 32u + 15u) & ~15u;               // byte offset of local_pos
+constexpr uint32_t kContEv = (kContLpos + 2u * kEcapCont + 32u + 15u) & ~15u;     // byte offset of esc_val
+static_assert(offsetof(DecStage, pk) == 0, "continuation arrays start at the stage");
+static_assert(kContEv + kEcapCont + 32u <= offsetof(DecStage, ev) + sizeof(DecStage::ev),
+              "continuation arrays fit in pk .. ev");
 
 // What the producer needs of one tile, resolved by one lane when a window of
 // tiles starts (kept in shared memory, not registers, so the producer's loop
@@ -1029,13 +1042,13 @@ __device__ bool issue_marker(const Ring& r, uint64_t& it, uint32_t flags, uint64
 }
 
 // The stages of one tile: pk, sm and its first kEcap escapes, then one stage
-// per further kEcap escapes.  Each slice's 16-byte-aligned body goes by TMA
+// per further kEcapCont escapes (laid out from pk on).  Each slice's 16-byte-aligned body goes by TMA
 // (lane 0), its ragged end by a zero-filling cp.async (lanes 1-5), so nothing
 // outside the payload is read.
 template <bool INPLACE>
 __device__ bool issue_tile(const Ring& r, uint64_t& it, const TileSrc& t, WsHeader* hdr, uint32_t lane) {
   const uint32_t m = (t.k1 > t.k0) ? t.k1 - t.k0 : 0u;
-  const uint32_t pieces = m ? (m + kEcap - 1) / kEcap : 1u;
+  const uint32_t pieces = m > kEcap ? 1u + (m - kEcap + kEcapCont - 1u) / kEcapCont : 1u;
   const uint64_t g = uint64_t(t.lt) * kTile;
   const Slice spk = slice_of(g >> 1, (t.nt + 1) >> 1);
   const Slice ssm = slice_of(t.off_sm + g, t.nt);
@@ -1045,8 +1058,13 @@ __device__ bool issue_tile(const Ring& r, uint64_t& it, const TileSrc& t, WsHead
     DecStage& st = r.st[s];
     uint64_t* const full = &r.full[s];
     const bool first = pc == 0;
-    const uint32_t pk0 = t.k0 + pc * kEcap;
-    const uint32_t pm = m ? ((m - pc * kEcap < kEcap) ? m - pc * kEcap : kEcap) : 0u;
+    const uint32_t before = first ? 0u : kEcap + (pc - 1u) * kEcapCont;  // escapes of the tile in earlier stages
+    const uint32_t cap = first ? kEcap : kEcapCont;
+    const uint32_t pk0 = t.k0 + before;
+    const uint32_t pm = m > before ? ((m - before < cap) ? m - before : cap) : 0u;
+    uint8_t* const dcid = first ? reinterpret_cast<uint8_t*>(st.cid) : st.pk;
+    uint8_t* const dlpos = first ? reinterpret_cast<uint8_t*>(st.lpos) : st.pk + kContLpos;
+    uint8_t* const dev = first ? st.ev : st.pk + kContEv;
     const Slice scid = slice_of(t.off_cid + 4ull * pk0, 4ull * pm);
     const Slice slp = slice_of(t.off_lpos + 2ull * pk0, 2ull * pm);
     const Slice sev = slice_of(t.off_ev + pk0, pm);
@@ -1072,21 +1090,19 @@ __device__ bool issue_tile(const Ring& r, uint64_t& it, const TileSrc& t, WsHead
       mbar_arrive_expect_tx(full, tx);
       if (first && spk.a1 > spk.a0) bulk_g2s(st.pk, t.pk_src + spk.a0, uint32_t(spk.a1 - spk.a0), full);
       if (first && ssm.a1 > ssm.a0) bulk_g2s(st.sm, t.base + ssm.a0, uint32_t(ssm.a1 - ssm.a0), full);
-      if (pm && scid.a1 > scid.a0) bulk_g2s(st.cid, t.esc_src + scid.a0, uint32_t(scid.a1 - scid.a0), full);
-      if (pm && slp.a1 > slp.a0) bulk_g2s(st.lpos, t.esc_src + slp.a0, uint32_t(slp.a1 - slp.a0), full);
-      if (pm && sev.a1 > sev.a0) bulk_g2s(st.ev, t.esc_src + sev.a0, uint32_t(sev.a1 - sev.a0), full);
+      if (pm && scid.a1 > scid.a0) bulk_g2s(dcid, t.esc_src + scid.a0, uint32_t(scid.a1 - scid.a0), full);
+      if (pm && slp.a1 > slp.a0) bulk_g2s(dlpos, t.esc_src + slp.a0, uint32_t(slp.a1 - slp.a0), full);
+      if (pm && sev.a1 > sev.a0) bulk_g2s(dev, t.esc_src + sev.a0, uint32_t(sev.a1 - sev.a0), full);
     } else if (first && lane == 1 && spk.end > spk.a1) {
       cp_async16_zfill(st.pk + (spk.a1 - spk.a0), t.pk_src + spk.a1, uint32_t(spk.end - spk.a1));
     } else if (first && lane == 2 && ssm.end > ssm.a1) {
       cp_async16_zfill(st.sm + (ssm.a1 - ssm.a0), t.base + ssm.a1, uint32_t(ssm.end - ssm.a1));
     } else if (pm && lane == 3 && scid.end > scid.a1) {
-      cp_async16_zfill(reinterpret_cast<uint8_t*>(st.cid) + (scid.a1 - scid.a0), t.esc_src + scid.a1,
-                       uint32_t(scid.end - scid.a1));
+      cp_async16_zfill(dcid + (scid.a1 - scid.a0), t.esc_src + scid.a1, uint32_t(scid.end - scid.a1));
     } else if (pm && lane == 4 && slp.end > slp.a1) {
-      cp_async16_zfill(reinterpret_cast<uint8_t*>(st.lpos) + (slp.a1 - slp.a0), t.esc_src + slp.a1,
-                       uint32_t(slp.end - slp.a1));
+      cp_async16_zfill(dlpos + (slp.a1 - slp.a0), t.esc_src + slp.a1, uint32_t(slp.end - slp.a1));
     } else if (pm && lane == 5 && sev.end > sev.a1) {
-      cp_async16_zfill(st.ev + (sev.a1 - sev.a0), t.esc_src + sev.a1, uint32_t(sev.end - sev.a1));
+      cp_async16_zfill(dev + (sev.a1 - sev.a0), t.esc_src + sev.a1, uint32_t(sev.end - sev.a1));
     }
     cp_async_mbar_arrive_noinc(full);
     ++it;
@@ -1175,10 +1191,15 @@ __device__ void consume(const Ring& r, uint16_t (*out)[kTile], uint32_t ctid, ui
       // sign and mantissa: the patch rewrites the exponent field only
       named_bar_sync(bar, kDecConsumers);
       const uint32_t chunk0 = st.lt * kChunksPerTile;
+      // a tile's further stages hold their escapes from pk on (kEcapCont layout)
+      const bool cont = (flags & kStageCont) != 0;
+      const uint32_t* const cidb = cont ? reinterpret_cast<const uint32_t*>(st.pk) : st.cid;
+      const uint16_t* const lposb = cont ? reinterpret_cast<const uint16_t*>(st.pk + kContLpos) : st.lpos;
+      const uint8_t* const evb = cont ? st.pk + kContEv : st.ev;
       for (uint32_t k = ctid; k < m; k += kDecConsumers) {
-        const uint32_t c = st.cid[(st.cid_shift >> 2) + k];
-        const uint32_t p = st.lpos[(st.lpos_shift >> 1) + k];
-        const uint32_t ev = st.ev[st.ev_shift + k];
+        const uint32_t c = cidb[(st.cid_shift >> 2) + k];
+        const uint32_t p = lposb[(st.lpos_shift >> 1) + k];
+        const uint32_t ev = evb[st.ev_shift + k];
         const uint32_t rel = c - chunk0;
         const uint32_t pos = rel * kChunk + p;
         if (rel < kChunksPerTile && p < kChunk && pos < nt) {
