@@ -530,12 +530,18 @@ __device__ uint32_t bound_window(const int32_t* cid, uint32_t e, uint32_t k_star
 }
 
 // Asks L2 for the chunk_ids the next window will count or probe (about
-// `expect` of them from escape k, at least kCountEntries, at most 64 Ki),
-// one window ahead: whole 16-byte lines inside the stream.
+// `expect` of them from escape k, at least kCountEntries), one window ahead:
+// whole 16-byte lines inside the stream.  The producers read these lines a
+// window later, after more than L2 holds has streamed through it, so every
+// prefetched line is read from DRAM twice; a window of more than
+// kPrefetchMax escapes is not prefetched: its lanes' guided searches touch a
+// few sectors each, and the lanes whose ends lie past a capped prefetch
+// would wait on DRAM all the same.
+constexpr uint32_t kPrefetchMax = 8192;
 __device__ __forceinline__ void prefetch_count(const uint8_t* payload, uint64_t off_cid, uint32_t e, uint32_t k,
                                                uint32_t expect, uint32_t lane) {
-  if (lane != 0 || k >= e) return;
-  uint64_t cnt = expect < kCountEntries ? kCountEntries : (expect > 65536u ? 65536u : expect);
+  if (lane != 0 || k >= e || expect > kPrefetchMax) return;
+  uint64_t cnt = expect < kCountEntries ? kCountEntries : expect;
   if (uint64_t(k) + cnt > e) cnt = e - k;
   const uint64_t a = (reinterpret_cast<uint64_t>(payload) + off_cid + 4ull * k) & ~uint64_t(15);
   const uint64_t b = (reinterpret_cast<uint64_t>(payload) + off_cid + 4ull * (k + cnt)) & ~uint64_t(15);
