@@ -70,6 +70,13 @@ def test_fused_tensor_larger_than_a_group_then_small_ones():
     _fused_vs_separate(arrays)
 
 
+def test_fused_tensors_each_spanning_several_groups():
+    # 3 tensors of 6,244 tiles: each covers the start of three 2048-tile
+    # groups, so most groups are empty and the schedule runs over the others
+    arrays = [inputs.gaussian(6244 * 8192 - 5 * i, 0.02, seed=40 + i) for i in range(3)]
+    _fused_vs_separate(arrays)
+
+
 def test_fused_many_small_tensors():
     arrays = [inputs.paged_kv_block(i) for i in range(3000)]
     _fused_vs_separate(arrays, oracle_check=False)

@@ -289,20 +289,30 @@ __global__ void __launch_bounds__(kCeThreads, kCeCtasPerSm) ce_main(const __grid
       }
       return true;
     };
-    // count(g0), count(g1), count(g2), encode(g0), count(g3), encode(g1), ...:
-    // every CTA counts the same share of each group, kLookahead groups ahead
-    // of the group it encodes, so codebooks are ready when encoding starts
-    for (uint64_t g = 0; g < groups + kLookahead; ++g) {
-      if (g < groups) {
-        const uint64_t a = ws.group_first[g], z = ws.group_first[g + 1];
+    // The first non-empty group at or after g (groups if none): a tensor
+    // larger than a group leaves the groups whose start it covers empty.
+    auto next_group = [&](uint64_t g) -> uint64_t {
+      while (g < groups && ws.group_first[g] == ws.group_first[g + 1]) ++g;
+      return g;
+    };
+    // count(g0), count(g1), count(g2), encode(g0), count(g3), encode(g1), ...
+    // over the non-empty groups: every CTA counts the same share of each
+    // group, kLookahead groups ahead of the group it encodes, so codebooks
+    // are ready when encoding starts
+    uint64_t gc = next_group(0), ge = gc;
+    for (uint64_t k = 0; gc < groups || ge < groups; ++k) {
+      if (gc < groups) {
+        const uint64_t a = ws.group_first[gc], z = ws.group_first[gc + 1];
         const uint64_t per = (z - a + gridDim.x - 1) / gridDim.x;
         const uint64_t s0 = min(z, a + uint64_t(blockIdx.x) * per), s1 = min(z, s0 + per);
         if (!job(s0, s1, true)) return;
+        gc = next_group(gc + 1);
       }
-      if (g >= kLookahead) {
-        // encode(g - kLookahead): runs of kCeRun tiles from the group's ticket,
-        // so CTAs that count faster encode more
-        const uint64_t e = g - kLookahead;
+      if (k >= kLookahead || gc >= groups) {
+        // encode(ge): runs of kCeRun tiles from the group's ticket, so CTAs
+        // that count faster encode more
+        const uint64_t e = ge;
+        ge = next_group(ge + 1);
         const uint64_t a = ws.group_first[e], z = ws.group_first[e + 1];
         for (;;) {
           uint32_t rb = 0;
