@@ -367,26 +367,27 @@ SZ_API int sz_encode_gated_many(const sz_item* d_items, uint32_t count, uint64_t
                                 double min_coverage, sz_gate_report* d_report,
                                 void* d_workspace, size_t workspace_bytes, sz_stream stream);
 
-/* ------------------------------------------------------------------ calibrate + encode in one pass */
+/* ------------------------------------------------------------------ calibrate + encode in one call */
 
 /* Calibration followed by encode ("splitzip_codec.py" calibrate_codebook,
  * then encode_torch + assemble_payload with the codebook it returns) in one
- * call that reads each input from its memory once: the tensors are taken in
- * groups of about 32 MiB, each group counted and, two groups later, encoded
- * while it is still in L2; a table of small tensors (as in sz_encode_many)
- * is counted, ranked and encoded one whole tensor at a time in shared
- * memory.  The codebooks, payloads, metas and flags are
- * those of sz_calibrate (or sz_calibrate_many) followed by sz_encode
- * (sz_encode_many), byte for byte; the table fields read and written are the
- * union of the two calls'.  The main kernel is a cooperative launch (all its
- * CTAs resident at once); SZ_ERR_CUDA if the device cannot run it.
- * On a GB300 with the input in HBM the two separate calls are faster for
- * large tensors (the split-and-pack pass is bound by instruction issue, not
- * by HBM, so the saved read does not shorten it, and the per-group codebook
- * hand-off costs time); for tables of small tensors this call is the faster
- * one (8192 tensors of 16,384 elements: 161 against 171 us).  It halves the
- * input traffic, which matters where reading the input is the bottleneck.  The pages calibrate offline, one tensor at a time, and
- * encode after a host round trip; this fusion has no counterpart there. */
+ * call.  A table of small tensors (as in sz_encode_many) is counted, ranked
+ * and encoded one whole tensor at a time in shared memory, each input read
+ * from HBM once.  Other tables go through one cooperative kernel (all its
+ * CTAs resident at once; SZ_ERR_CUDA if the device cannot run it): the
+ * tensors are taken in groups of about 32 MiB, and each group is counted and,
+ * two groups later, encoded.  That second read was meant to hit L2, but the
+ * traffic between the two passes is larger than L2, so on a GB300 it comes
+ * from HBM (391 MB read for 201 MB of KV-cache input).  The codebooks,
+ * payloads, metas and flags are those of sz_calibrate (or sz_calibrate_many)
+ * followed by sz_encode (sz_encode_many), byte for byte; the table fields read
+ * and written are the union of the two calls'.
+ * On a GB300 with the input in HBM this call is the faster one for tables of
+ * small tensors (8192 tensors of 16,384 elements: 164 against 171 us); for
+ * large tensors the two separate calls are as fast or faster (0.95-0.98 x
+ * on the KV-cache, weight and 4 GiB tables).  The pages calibrate offline,
+ * one tensor at a time, and encode after a host round trip; this fusion has
+ * no counterpart there. */
 SZ_API int sz_calibrate_encode(const uint16_t* d_x, uint64_t n, sz_codebook* d_codebook,
                                uint8_t* d_payload, uint64_t capacity, sz_meta* d_meta,
                                void* d_workspace, size_t workspace_bytes, sz_stream stream);

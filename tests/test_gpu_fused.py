@@ -1,4 +1,4 @@
-"""sz_calibrate_encode(_many): one pass over HBM, results identical to
+"""sz_calibrate_encode(_many): one call, results identical to
 sz_calibrate(_many) followed by sz_encode(_many) and to the CPU oracle."""
 from __future__ import annotations
 

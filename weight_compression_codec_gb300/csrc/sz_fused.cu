@@ -1,4 +1,4 @@
-// Calibration and encode in one pass over HBM ("splitzip_codec.py"
+// Calibration and encode in one call ("splitzip_codec.py"
 // calibrate_codebook followed by encode_torch + assemble_payload, for many
 // tensors).  The results are those of sz_calibrate_many followed by
 // sz_encode_many, byte for byte; only the order of the work differs.
@@ -11,6 +11,8 @@
 // every CTA counting its own slice of each group and then taking runs of the
 // group's tiles to encode from a ticket, so a group's input is read again
 // soon after it was counted (two other groups' count passes lie in between).
+// On a GB300 the traffic in between is larger than L2 and the second read
+// comes from HBM; the gain over the separate calls is the launches saved.
 //
 // Launches per call (after a 256-byte header memset):
 //   ce_prepare  validates the table for both passes, zeroes histograms,
