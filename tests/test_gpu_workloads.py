@@ -1,10 +1,9 @@
 """GPU parity at the full sizes of the five benchmark workloads.
 
 Every tensor is compared with the CPU oracle byte for byte (codebook, meta,
-payload) and its decode bit for bit, except the largest size-sweep points,
-where the oracle checks the exact codebook and escape count and a sample of
-1024-element chunks (pk, sm and escape entries), and the round trip is
-checked on the GPU.
+payload) and its decode bit for bit; for the size-sweep points above 2^26
+elements the decode is checked against the input on the GPU instead of
+through the oracle's decode.
 """
 from __future__ import annotations
 
@@ -89,35 +88,15 @@ def test_c5_paged_kv_8192_blocks():
     _many_exact(arrays)
 
 
-def _sampled_check(x: np.ndarray, payload: torch.Tensor, m, cb_dev: torch.Tensor, samples: int = 64) -> None:
-    """Exact codebook and escape count from the oracle over the whole tensor;
-    pk, sm and escape entries of sampled 1024-element chunks against the
-    oracle run on each chunk with the same codebook."""
+def _whole_check(x: np.ndarray, payload: torch.Tensor, m, cb_dev: torch.Tensor) -> None:
+    """Codebook, meta and every payload byte against the oracle run on the
+    whole tensor."""
     ocb = oracle.calibrate(x)
     check_codebook(sz.read_codebook(cb_dev), ocb, x.size)
-    assert m.n_esc == oracle.count_escapes(x, ocb)
-    lay = oracle.layout(x.size, m.n_esc)
-    assert m.as_tuple() == lay.as_tuple()
-    cid = payload[m.off_cid:m.off_cid + 4 * m.n_esc].view(torch.int32)
-    rng = np.random.default_rng(x.size)
-    chunks = (x.size + 1023) // 1024
-    for c in sorted(set(rng.integers(0, chunks, size=samples).tolist()) | {0, chunks - 1}):
-        lo, hi = c * 1024, min(x.size, c * 1024 + 1024)
-        opay, om = oracle.encode(x[lo:hi], ocb)
-        n = hi - lo
-        pk = payload[m.off_pk + lo // 2:m.off_pk + lo // 2 + (n + 1) // 2].cpu().numpy()
-        assert np.array_equal(pk, opay[:(n + 1) // 2]), f"pk of chunk {c}"
-        smb = payload[m.off_sm + lo:m.off_sm + hi].cpu().numpy()
-        assert np.array_equal(smb, opay[om.off_sm:om.off_sm + n]), f"sm of chunk {c}"
-        k0 = int(torch.searchsorted(cid, torch.tensor([c], dtype=torch.int32, device=cid.device)).item())
-        e = om.n_esc
-        got_cid = cid[k0:k0 + e].cpu().numpy()
-        got_lp = payload[m.off_lpos + 2 * k0:m.off_lpos + 2 * (k0 + e)].cpu().numpy()
-        got_ev = payload[m.off_ev + k0:m.off_ev + k0 + e].cpu().numpy()
-        assert np.all(got_cid == c)
-        assert k0 + e == m.n_esc or int(cid[k0 + e].item()) > c, f"extra escapes in chunk {c}"
-        assert np.array_equal(got_lp, opay[om.off_lpos:om.off_lpos + 2 * e]), f"local_pos of chunk {c}"
-        assert np.array_equal(got_ev, opay[om.off_ev:om.off_ev + e]), f"esc_val of chunk {c}"
+    opay, om = oracle.encode(x, ocb)
+    assert m.as_tuple() == om.as_tuple()
+    got = payload[:m.comp_bytes].cpu().numpy()
+    assert np.array_equal(got, opay), f"payload differs from byte {int(np.argmax(got != opay))}"
 
 
 @pytest.mark.parametrize("n", inputs.sweep_sizes())
@@ -135,4 +114,4 @@ def test_c5_size_sweep(n):
     assert m.status == 0
     assert torch.equal(out, xd), "GPU round trip"
     del out
-    _sampled_check(x, payload, m, cb)
+    _whole_check(x, payload, m, cb)
