@@ -392,9 +392,9 @@ def measure(arrays: list[np.ndarray], K: int, warmup: int, dev, gpu_id: str, wor
     metas = [sz.meta_from_bytes(m) for m in batch.metas.cpu().numpy()]
     comp_total = sum(m.comp_bytes for m in metas)
 
-    # Kernel events, set through the library's timing hook around each call's
-    # streaming kernel, are the only events inside the timed steps; the calls
-    # (API call to API call) are timed in a separate pass afterwards.
+    # The timed steps have no event inside them. The streaming kernels are then
+    # timed in a second pass, through the library's timing hook around each
+    # call's main kernel, and the calls (API call to API call) in a third.
     ev = {k: [torch.cuda.Event(enable_timing=True) for _ in range(K)] for k in
           ("cb", "ca", "eb", "ea", "db", "da", "o0", "o1", "o2", "o3")}
     for lst in ev.values():  # create the underlying CUDA events
@@ -411,6 +411,15 @@ def measure(arrays: list[np.ndarray], K: int, warmup: int, dev, gpu_id: str, wor
     torch.cuda.synchronize()
     step_start.record(stream)
     for k in range(K):
+        step()
+    step_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if barrier:
+        torch.distributed.barrier()
+    total_ms = step_start.elapsed_time(step_end)
+    step_start.record(stream)
+    for k in range(K):
         sz.sz_set_timing_events(ev["cb"][k], ev["ca"][k])
         sz.sz_calibrate_many(batch.table, workspace=ws_cal)
         sz.sz_set_timing_events(ev["eb"][k], ev["ea"][k])
@@ -420,10 +429,7 @@ def measure(arrays: list[np.ndarray], K: int, warmup: int, dev, gpu_id: str, wor
     sz.sz_set_timing_events(None, None)
     step_end.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
-    if barrier:
-        torch.distributed.barrier()
-    total_ms = step_start.elapsed_time(step_end)
+    kernel_pass_ms = step_start.elapsed_time(step_end)
     t_kern = {"calibrate": [ev["cb"][k].elapsed_time(ev["ca"][k]) for k in range(K)],
               "encode": [ev["eb"][k].elapsed_time(ev["ea"][k]) for k in range(K)],
               "decode": [ev["db"][k].elapsed_time(ev["da"][k]) for k in range(K)]}
@@ -492,7 +498,8 @@ def measure(arrays: list[np.ndarray], K: int, warmup: int, dev, gpu_id: str, wor
            for k in t_ops}
     ops["calibrate_encode"]["vs_separate_calls"] = (t_ops["calibrate"] + t_ops["encode"]) / t_ops["calibrate_encode"]
     return {"xs": xs, "batch": batch, "metas": metas, "stream": stream, "raw_bytes": raw_bytes,
-            "n_total": n_total, "comp_total": comp_total, "ms_step": total_ms / K, "ms": ms, "t_ops": t_ops,
+            "n_total": n_total, "comp_total": comp_total, "ms_step": total_ms / K,
+            "ms_step_kernel_pass": kernel_pass_ms / K, "ms": ms, "t_ops": t_ops,
             "kernels": kernels, "ops": ops, "clocks": clk}
 
 
@@ -530,7 +537,8 @@ SUB_CONFIGS = [
 
 def sub_record(m: dict) -> dict:
     """What a sub-record keeps of measure()'s result."""
-    return {"ms_per_step": m["ms_step"], "raw_gbs_step": m["raw_bytes"] / (m["ms_step"] * 1e-3) / 1e9,
+    return {"ms_per_step": m["ms_step"], "ms_per_step_kernel_pass": m["ms_step_kernel_pass"],
+            "raw_gbs_step": m["raw_bytes"] / (m["ms_step"] * 1e-3) / 1e9,
             "tensors": len(m["metas"]), "elements": m["n_total"], "raw_bytes": m["raw_bytes"],
             "l2": l2_note(m["raw_bytes"]), "ratio": m["comp_total"] / m["raw_bytes"],
             "n_esc": int(sum(x.n_esc for x in m["metas"])), "kernels": m["kernels"], "ops": m["ops"],
@@ -559,6 +567,7 @@ def run_ours(args, world, rank, local):
     xs, batch, metas, stream = head["xs"], head["batch"], head["metas"], head["stream"]
     raw_bytes, n_total, comp_total = head["raw_bytes"], head["n_total"], head["comp_total"]
     total_ms = head["ms_step"] * K
+    kernel_pass_ms = head["ms_step_kernel_pass"]
     t_ops = head["t_ops"]
     m_kernels, m_ops, m_ms, clk = head["kernels"], head["ops"], head["ms"], head["clocks"]
     n_esc_total = int(sum(x.n_esc for x in metas))
@@ -800,10 +809,13 @@ def run_ours(args, world, rank, local):
         cpu = cpu_oracle_sample([a[:1 << 24] for a in arrays], args.cpu_seconds)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": ms_step, "ms_per_step_kernel_pass": kernel_pass_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "u16", "data": "synthetic",
         "config": {"workload": workload_name(args), "tensors": len(arrays), "elements": n_total, "raw_bytes": raw_bytes,
                    "step": "calibrate+encode+decode", "l2": l2_note(raw_bytes),
+                   "kernel_timing": "CUDA events around each call's main kernel (library timing hook) in a "
+                                    "second pass of the same K steps; the timed steps carry no event inside a "
+                                    "call, as one between a kernel and its programmatic dependent delays it",
                    "parallelism": f"{world} independent shards" if world > 1 else "single GPU"},
         "ratio": comp_total / raw_bytes, "compression": raw_bytes / comp_total,
         "n_esc": n_esc_total,
