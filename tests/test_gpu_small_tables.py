@@ -119,6 +119,36 @@ def test_small_table_many_blocks_and_escape_heavy_blocks():
     _check_against_oracle(sub, [arrays[i] for i in sample])
 
 
+def _tie_tensor(n: int, bins: int, seed: int) -> np.ndarray:
+    """n patterns spread evenly over `bins` exponents (equal counts where n
+    allows: ties broken by ascending exponent), random sign and mantissa."""
+    rng = np.random.default_rng(seed)
+    e = (90 + np.arange(n) % bins).astype(np.uint16)
+    rng.shuffle(e)
+    return (rng.integers(0, 2, n, dtype=np.uint16) << 15) | (e << 7) | rng.integers(0, 128, n, dtype=np.uint16)
+
+
+def test_small_table_calibrate_alone_matches_the_oracle():
+    # sz_calibrate_many on its own: every codebook byte against the oracle's,
+    # over paged blocks, ragged sizes, one-bin, tied and escape-heavy tensors
+    arrays = [inputs.paged_kv_block(i) for i in range(600)]
+    arrays += _ragged_table()
+    arrays += [np.full(n, v, np.uint16) for n, v in ((16_384, 0x3F80), (5, 0x0000), (9, 0x8001))]
+    arrays += [_tie_tensor(n, bins, 990 + k) for k, (n, bins) in
+               enumerate(((16_384, 16), (16_384, 17), (16_000, 20), (8_191, 40), (12_289, 256), (33, 33)))]
+    assert _small_routed(arrays) and max(a.size for a in arrays) <= SMALL_MAX
+    b = sz.Batch([to_dev(a) for a in arrays])
+    b.codebooks.fill_(0xAB)
+    ws = sz.Workspace(DEV)
+    sz.sz_calibrate_many(b.table, workspace=ws)
+    torch.cuda.synchronize()
+    assert sz.sz_workspace_flags(ws.buf) == 0
+    cbs = b.codebooks.cpu().numpy()
+    for i, x in enumerate(arrays):
+        want = np.frombuffer(gpu_util.oracle_codebook_bytes(oracle.calibrate(x), x.size), np.uint8)
+        assert np.array_equal(cbs[i][:want.size], want), f"codebook {i} (n={x.size})"
+
+
 def test_small_table_with_one_large_tensor_goes_to_the_general_kernels():
     arrays = [inputs.gaussian(40_000, 0.02, seed=950)] + [inputs.edge_case(1000 + 37 * k, seed=951 + k)
                                                            for k in range(30)]
