@@ -225,11 +225,14 @@ SZ_API int sz_decode(const uint8_t* d_payload, uint64_t payload_bytes, const sz_
  * total_tiles = its total).  Work is spread over all SMs tile by tile, so a
  * few large tensors and many mid-size ones run equally well.  A table whose
  * tensors average at most two tiles (16,384 elements, e.g. the blocks of a
- * paged KV cache) is encoded whole-tensor by whole-tensor in shared memory
- * instead, reading each input once and staging nothing; if one of its
- * tensors is larger than two tiles the call falls back, inside the same
- * launches, to the tile-by-tile kernels.  Either way the results are the
- * same bytes.
+ * paged KV cache) is encoded and decoded whole-tensor by whole-tensor in
+ * shared memory instead: encode reads each input once and stages nothing,
+ * decode copies each payload whole (at most 26 KiB) before decoding it.
+ * Inside the same launches, encode hands the whole table to the tile-by-tile
+ * kernels if one of its tensors is larger than two tiles, and decode leaves
+ * them the tensors it cannot hold (more than two tiles, or a larger
+ * payload).  Either way the results are the same bytes.  Calibration takes
+ * the tile-by-tile kernel for every table.
  *   calibrate: reads x, n, tile_begin; writes *codebook.
  *   encode:    reads x, n, codebook, payload, capacity, tile_begin; writes payload, *meta.
  *   decode:    reads payload (capacity readable bytes), meta, codebook, n, tile_begin; writes out.
